@@ -1,0 +1,368 @@
+"""GPTQ seconds per layer on one B300: Hessian + damping/factor + sweep (+ deferred GEMMs) + packing.
+
+One step = one pass of the whole path over one synthetic layer:
+    H = 0; gptq_hessian_accumulate(H, X); gptq_quantize_layer(W, H, ...)
+with X and W resident in HBM.  X (2.15 GB for the default workload) is larger
+than the 126 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line.  Under torchrun (N > 1) every rank quantizes its own copy
+of the layer (independent replicas, no collective on the data path) and
+rank 0 prints the aggregate: layers processed by all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synthetic import LAYERS, generate, generate_rows  # noqa: E402
+
+METRIC = "GPTQ sec per layer (Hessian+Cholesky+sweep+pack) at 1 B300; % of roofline"
+DEFAULT_WORKLOAD = "llama7b_q_proj_4096x4096"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def launches_per_step(rows: int, cols: int, block: int) -> int:
+    """Kernels of libgq launched by one step (Hessian + factor + sweep)."""
+    nb_panel = 64
+    panels = -(-cols // nb_panel)
+    factor = 2 + panels + 2 * (panels - 1) + 1  # diag sum, reversal; potrf per panel; trsm + gemm but last; finalize
+    nblk = -(-cols // block)
+    sweep = 1 + nblk + (nblk - 1)  # block inverses; one sweep per block; one deferred GEMM per split
+    return 1 + factor + sweep
+
+
+# --------------------------------------------------------------------------- ours
+def run_ours(args, rank: int, world: int):
+    import torch
+
+    import post_weight_quantization_30_b300 as gq
+
+    spec = LAYERS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+
+    # Inputs: seeded host generation (spawn pool), then resident in HBM.
+    t0 = time.time()
+    x_host = torch.empty((spec.n, spec.cols), dtype=torch.int16, pin_memory=True)
+    generate(spec.X, out=x_host.numpy().view(np.uint16))
+    w_host = torch.empty((spec.rows, spec.cols), dtype=torch.int16, pin_memory=True)
+    generate(spec.W, out=w_host.numpy().view(np.uint16))
+    gen_s = time.time() - t0
+    X = x_host.to(dev).view(torch.bfloat16)
+    W = w_host.to(dev).view(torch.bfloat16)
+    R, C, N = spec.rows, spec.cols, spec.n
+    H = torch.zeros((C, C), dtype=torch.float32, device=dev)
+    ws = torch.empty(gq.lib.gptq_quantize_layer_workspace_size(R, C, spec.block), dtype=torch.uint8, device=dev)
+    out = gq._lib._sweep_outputs(R, C, spec.bits, spec.group, dev, codes=False, W_hat=False, row_err=False)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        H.zero_()
+        if ev is not None:
+            ev[0].record(stream)
+        gq.gptq_hessian_accumulate(H, X)
+        if ev is not None:
+            ev[1].record(stream)
+        gq.gptq_quantize_layer(W, H, spec.bits, spec.group, spec.block, spec.damp, workspace=ws, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    import torch.distributed as dist
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        start.record(stream)
+        for k in range(args.steps):
+            step(hev[k])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    ms_total = start.elapsed_time(stop)
+    h_ms = [a.elapsed_time(b) for a, b in hev]
+    if world > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_per_step = ms_total / args.steps
+
+    # Per-phase breakdown (untimed for the headline): factor and sweep separately.
+    phase = {}
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    F = torch.empty((C, C), dtype=torch.float32, device=dev)
+    dead = torch.empty(C, dtype=torch.uint8, device=dev)
+    fws = torch.empty(max(256, gq.lib.gptq_factor_workspace_size(C)), dtype=torch.uint8, device=dev)
+    sws = torch.empty(gq.lib.gptq_sweep_workspace_size(R, C, spec.block), dtype=torch.uint8, device=dev)
+    import ctypes
+
+    reps = 3
+    acc = {"hessian": 0.0, "factor": 0.0, "sweep": 0.0}
+    for _ in range(reps):
+        H.zero_()
+        e[0].record(stream)
+        gq.gptq_hessian_accumulate(H, X)
+        e[1].record(stream)
+        info = ctypes.c_int64(-1)
+        st = gq.lib.gptq_factor(ctypes.c_void_p(H.data_ptr()), C, spec.damp, ctypes.c_void_p(F.data_ptr()),
+                                ctypes.c_void_p(dead.data_ptr()), ctypes.c_void_p(fws.data_ptr()), fws.numel(),
+                                ctypes.c_void_p(stream.cuda_stream), ctypes.byref(info))
+        assert st == 0, st
+        e[2].record(stream)
+        gq.gptq_sweep(W, F, dead, spec.bits, spec.group, spec.block, codes=False, W_hat=False, row_err=False,
+                      workspace=sws)
+        e[3].record(stream)
+        torch.cuda.synchronize(dev)
+        acc["hessian"] += e[0].elapsed_time(e[1])
+        acc["factor"] += e[1].elapsed_time(e[2])
+        acc["sweep"] += e[2].elapsed_time(e[3])
+    phase = {k: v / reps for k, v in acc.items()}
+
+    # End to end through the public API from pinned host buffers, every step:
+    # H2D of X and W, the whole path, D2H of the packed result.
+    res_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items() if v is not None}
+    h2d = x_host.numel() * 2 + w_host.numel() * 2
+    d2h = sum(v.numel() * v.element_size() for v in res_host.values())
+    Xd = torch.empty_like(X)
+    Wd = torch.empty_like(W)
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(2, min(args.steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        Xd.view(torch.int16).copy_(x_host, non_blocking=True)
+        Wd.view(torch.int16).copy_(w_host, non_blocking=True)
+        H.zero_()
+        gq.gptq_hessian_accumulate(H, Xd)
+        gq.gptq_quantize_layer(Wd, H, spec.bits, spec.group, spec.block, spec.damp, workspace=ws, out=out)
+        for k, v in res_host.items():
+            v.copy_(out[k], non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+
+    peaks, peak_kind = _peaks()
+    flops = float(N) * C * (C + 1)  # symmetric work of H += 2 X^T X
+    h_avg_s = statistics.mean(h_ms) / 1e3
+    achieved = flops / h_avg_s / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    traffic = _read_traffic()
+
+    result = {
+        "metric": METRIC,
+        "value": round(ms_per_step / 1e3 / world, 6),
+        "unit": "s/layer",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16/f32",
+        "data": "synthetic (seeded; Student-t(4) activations with 41 outlier channels x30, N(0,0.02^2) weights)",
+        "config": {
+            "workload": args.workload, "rows": R, "cols": C, "tokens": N, "bits": spec.bits, "group": spec.group,
+            "block": spec.block, "damp": spec.damp, "x_dtype": spec.X.dtype, "w_dtype": spec.W.dtype,
+            "l2": "inputs larger than L2 (X %.2f GB > 126 MB), no flush" % (spec.X.nbytes / 1e9),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "phases_ms": {k: round(v, 4) for k, v in phase.items()},
+        "roofline": {
+            "kernel": "hessian (H += 2 X^T X)",
+            "bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} bf16 sustained",
+            "flops_per_launch": flops, "traffic": traffic,
+        },
+        "e2e": {"value": round(e2e_s, 6), "unit": "s/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step(R, C, spec.block) * args.steps,
+        "clocks": clocks.summary(),
+        "input_generation_s": round(gen_s, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        result["cpu_baseline"] = cpu_baseline(spec, budget_s=args.cpu_budget)
+    return result
+
+
+def _read_traffic():
+    """DRAM bytes per launch of the Hessian kernel from the committed ncu summary, if current."""
+    p = os.path.join(ROOT, "profiles", "hessian_traffic.json")
+    try:
+        with open(p) as f:
+            return json.load(f).get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------- oracle (CPU)
+def cpu_baseline(spec, budget_s: float = 20.0) -> dict:
+    """The float64 oracle, as it stands, on a bounded sample of the same layer,
+    extrapolated to seconds per layer: H on a token sample (scaled by N / n_s),
+    the full damping + inverse + Cholesky, the sweep on a sample of rows (scaled
+    by rows / r_s), packing of those rows (scaled likewise)."""
+    from oracle import gptq as og
+    from oracle import pack as opk
+    from synthetic import bf16_bits_to_f32
+
+    cores = len(os.sched_getaffinity(0))
+    n_s = 4096 if spec.n >= 4096 else spec.n
+    r_s = 16 if spec.rows >= 16 else spec.rows
+    x = bf16_bits_to_f32(generate_rows(spec.X, 0, n_s, workers=1)) if spec.X.dtype == "bf16" else \
+        generate_rows(spec.X, 0, n_s, workers=1)
+    w = generate_rows(spec.W, 0, r_s, workers=1)
+    w = (bf16_bits_to_f32(w) if spec.W.dtype == "bf16" else w).astype(np.float64)
+    t0 = time.perf_counter()
+    H = og.hessian(x.astype(np.float64)) * (spec.n / n_s)
+    t1 = time.perf_counter()
+    Hd, dead = og.prepare_hessian(H, spec.damp)
+    U = og.inverse_cholesky_upper(Hd)
+    t2 = time.perf_counter()
+    res = og.sweep(w, U, spec.bits, spec.group, dead=dead)
+    t3 = time.perf_counter()
+    opk.pack_qweight(res["codes"], spec.bits)
+    t4 = time.perf_counter()
+    per_layer = (t1 - t0) * (spec.n / n_s) + (t2 - t1) + (t3 - t2) * (spec.rows / r_s) + (t4 - t3) * (spec.rows / r_s)
+    return {
+        "value": round(per_layer, 3), "unit": "s/layer", "cores": cores, "kind": "oracle",
+        "sample": f"H on {n_s} of {spec.n} tokens (x{spec.n / n_s:g}); full float64 inverse + Cholesky of "
+                  f"{spec.cols}x{spec.cols}; eager sweep + pack on {r_s} of {spec.rows} rows (x{spec.rows / r_s:g})",
+        "sample_s": round(t4 - t0, 2),
+        "phases_s": {"hessian": round((t1 - t0) * spec.n / n_s, 3), "factor": round(t2 - t1, 3),
+                     "sweep": round((t3 - t2) * spec.rows / r_s, 3), "pack": round((t4 - t3) * spec.rows / r_s, 3)},
+    }
+
+
+def run_reference(args):
+    spec = LAYERS[args.workload]
+    for _ in range(args.warmup):
+        cpu_baseline(spec)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(spec))
+    wall = time.perf_counter() - t0
+    v = statistics.mean(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = round(v, 3)
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(v, 3), "unit": "s/layer", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 1), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "rows": spec.rows, "cols": spec.cols, "tokens": spec.n,
+                   "bits": spec.bits, "group": spec.group, "block": spec.block},
+        "cpu_baseline": cb,
+        "e2e": {"value": round(v, 3), "unit": "s/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(LAYERS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+/*
+ * gq.h -- GPTQ layer quantization and EoRA compensation on one NVIDIA B300 (sm_103a).
+ *
+ * C ABI of libgq.so.  Every pointer argument is a CUDA DEVICE pointer unless its
+ * comment says "host".  The caller owns every buffer; the library never
+ * allocates or frees device memory: scratch space is the caller's workspace
+ * `ws` of at least the size that the matching *_workspace_size() query returns,
+ * 256-byte aligned.  All device work is enqueued on `stream` (a cudaStream_t;
+ * NULL = the legacy default stream).  Matrices are row-major and dense.
+ *
+ * Shapes follow the linear layer y = x W^T: W is rows x cols = out x in, the
+ * calibration activations X are n x cols (n tokens), H is cols x cols.
+ *
+ * Errors: argument errors are found on the host before anything is enqueued and
+ * are returned as GQ_EINVAL / GQ_EUNSUPPORTED / GQ_EWORKSPACE.  A launch error is
+ * returned as GQ_ECUDA.  Calls that factor H synchronize `stream` once, after the
+ * factorization, to read the device status word; they return GQ_ENOTPD with
+ * *info = the first input column whose pivot was not positive.  On any non-OK
+ * return the contents of the outputs are unspecified.
+ *
+ * Pages the operations follow (cited by title and section):
+ *   [GPTQ-wiki]  "GPTQ", wikiprompt.org encyclopedia entry, "Enfoque Técnico".
+ *   [LowBit]     "El balance de errores de la inferencia de pocos bits: escalas de
+ *                cuantización, calibración y ahorro real de memoria", auturnal.com,
+ *                sections 1 (format) and 2 (input covariance).
+ *   [EoRA-blog]  "Aumento de la precisión de LLM de 2 bits con EoRA", 7minutos.es,
+ *                "Bucear en el espacio propio en busca de un adaptador".
+ */
+#ifndef GQ_H
+#define GQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gq_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    GQ_OK = 0,
+    GQ_EINVAL = -1,       /* null required pointer, bad shape, stride or size rule */
+    GQ_ENOTPD = -2,       /* damped H not positive definite; *info = column */
+    GQ_EUNSUPPORTED = -3, /* bits not in {2,3,4}, unknown dtype */
+    GQ_ECUDA = -4,        /* CUDA runtime / launch error */
+    GQ_ENONFINITE = -5,   /* non-finite value found in an input */
+    GQ_ETIMEOUT = -6,     /* a bounded device-side wait gave up */
+    GQ_EWORKSPACE = -7    /* workspace missing, too small or not 256-byte aligned */
+} gq_status;
+
+typedef enum { GQ_F32 = 0, GQ_BF16 = 1 } gq_dtype;
+
+/* Version of this ABI (bumped on any signature change). */
+int gq_abi_version(void);
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char *gq_status_string(gq_status s);
+
+/*
+ * H += 2 X^T X.
+ *
+ * The second-order statistics of the layer inputs: the Hessian of the layer's
+ * squared output error with respect to each weight row ([GPTQ-wiki] "Enfoque
+ * Técnico"; [LowBit] section 2).  Both triangles of H are updated.
+ *
+ *   H     cols x cols float32, in/out (accumulated into; zero it for a fresh H).
+ *   X     n x cols, element type xt (GQ_BF16 or GQ_F32), leading dimension ldx
+ *         (elements, >= cols).  For GQ_BF16: X 16-byte aligned, ldx % 8 == 0.
+ *   n     number of tokens; n == 0 is a no-op.
+ * Accumulation is float32 (every bf16 x bf16 product is exact in float32).
+ * Deterministic: the same inputs give bit-identical H.  Asynchronous.
+ */
+gq_status gptq_hessian_accumulate(float *H, int64_t cols, const void *X, gq_dtype xt, int64_t n,
+                                  int64_t ldx, gq_stream_t stream);
+
+/*
+ * Factor of the damped Hessian.
+ *
+ * Dead inputs (H_ii == 0) get H_ii = 1; then H_d = H + damp * mean(diag H) * I.
+ * Writes the upper-triangular F with H_d = F F^T (strictly-lower part set to 0),
+ * obtained as the lower Cholesky factor of the index-reversed H_d.  Its inverse
+ * U = F^-1 is the upper Cholesky factor of H_d^-1 (U^T U = H_d^-1), the matrix
+ * whose rows drive GPTQ's error compensation ([GPTQ-wiki] "Enfoque Técnico");
+ * the sweep uses F directly and never forms U.
+ *
+ *   H     cols x cols float32, read only (both triangles read; must be symmetric).
+ *   F     cols x cols float32 output.
+ *   dead  cols bytes output (1 = dead input), may be NULL.
+ *   ws    >= gptq_factor_workspace_size(cols) bytes.
+ *   info  host pointer, may be NULL; on GQ_ENOTPD receives the failing column.
+ * Synchronizes `stream` once.
+ */
+size_t gptq_factor_workspace_size(int64_t cols);
+gq_status gptq_factor(const float *H, int64_t cols, float damp, float *F, uint8_t *dead, void *ws,
+                      size_t ws_bytes, gq_stream_t stream, int64_t *info);
+
+/*
+ * The GPTQ column sweep, given the factor F of gptq_factor.
+ *
+ * Columns are quantized in order, one group of `group` columns sharing a scale
+ * and zero point per row ([LowBit] section 1; [GPTQ-wiki] "Enfoque Técnico":
+ * per-group scale).  At a group's first column, from the weights as updated by
+ * every earlier column: xmin = min(0, min w), xmax = max(0, max w) (both 0 ->
+ * -1, +1), s = (xmax - xmin) / maxq, z = rint(-xmin / s), maxq = 2^bits - 1.
+ * Each column: q = clamp(rint(w / s) + z, 0, maxq), ŵ = s (q - z), and the error
+ * is propagated into the columns not yet quantized (closed-form OBQ update).
+ * Blocks of `block` columns are swept in shared memory; the update of later
+ * blocks is deferred and applied as GEMMs.  Decisions are float32 with IEEE
+ * division and round-half-to-even.
+ *
+ *   W        rows x cols, type wt, read only (never modified).
+ *   F, dead  from gptq_factor (dead may be NULL = no dead inputs).
+ *   bits     2, 3 or 4.  group % 32 == 0, cols % group == 0, block % group == 0,
+ *            block <= 128, rows % 32 == 0, cols % 32 == 0.
+ * Outputs (packing layout: little-endian bitstream of b-bit codes along the
+ * packed axis, code k at bits [k*b, k*b+b) of the stream, cut into 32-bit words):
+ *   qweight  [cols*bits/32][rows] int32: the codes of each output row packed
+ *            along the input axis.
+ *   scales   [cols/group][rows] float32.
+ *   qzeros   [cols/group][rows*bits/32] int32: zero points packed along rows.
+ *   codes    rows x cols uint8, may be NULL.
+ *   W_hat    rows x cols float32 dequantized weights, may be NULL.
+ *   row_err  rows float32, may be NULL: sum over columns of e_j^2 with
+ *            e_j = (w_j - ŵ_j) / U_jj, which equals ΔW_r H_d ΔW_r^T.
+ *   ws       >= gptq_sweep_workspace_size(rows, cols, block) bytes.
+ * Asynchronous.
+ */
+size_t gptq_sweep_workspace_size(int64_t rows, int64_t cols, int block);
+gq_status gptq_sweep(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *F,
+                     const uint8_t *dead, int bits, int group, int block, int32_t *qweight,
+                     float *scales, int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err,
+                     void *ws, size_t ws_bytes, gq_stream_t stream);
+
+/*
+ * One layer: gptq_factor (into the workspace) followed by gptq_sweep.
+ * Same arguments and rules as the two calls; H is read only.
+ * Synchronizes `stream` once (after the factorization).
+ */
+size_t gptq_quantize_layer_workspace_size(int64_t rows, int64_t cols, int block);
+gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *H,
+                              int bits, int group, int block, float damp, int32_t *qweight,
+                              float *scales, int32_t *qzeros, uint8_t *codes, float *W_hat,
+                              float *row_err, void *ws, size_t ws_bytes, gq_stream_t stream,
+                              int64_t *info);
+
+/*
+ * Standalone packing of codes (rows x cols uint8, each < 2^bits) into
+ * qweight [cols*bits/32][rows] int32, and its inverse.  Same layout as
+ * gptq_sweep.  rows % 32 == 0 is not required; cols*bits % 32 == 0 is.
+ * Asynchronous.
+ */
+gq_status gptq_pack(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight,
+                    gq_stream_t stream);
+gq_status gptq_unpack(const int32_t *qweight, int64_t rows, int64_t cols, int bits, uint8_t *codes,
+                      gq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GQ_H */

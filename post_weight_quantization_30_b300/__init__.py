@@ -1,0 +1,18 @@
+"""GPTQ layer quantization (+ EoRA compensation) native to NVIDIA B300 (sm_103a).
+
+The compute path is libgq.so (CUDA kernels behind a C ABI, include/gq.h); this
+package is its thin Python binding.  Importing it loads the library and fails
+if the library has not been built.
+"""
+from ._lib import (  # noqa: F401
+    GQError,
+    LIB_PATH,
+    SIGNATURES,
+    gptq_factor,
+    gptq_hessian_accumulate,
+    gptq_pack,
+    gptq_quantize_layer,
+    gptq_sweep,
+    gptq_unpack,
+    lib,
+)

@@ -1,0 +1,185 @@
+"""ctypes binding of libgq.so: argument marshalling only.
+
+Every function here forwards to the C entry point of the same name declared in
+include/gq.h.  Output and workspace buffers are allocated with PyTorch (device
+memory is PyTorch's job; the library never allocates), pointers and the
+current CUDA stream are passed through, and a non-OK status raises GQError.
+There is no other code path: if libgq.so is missing, importing this module
+fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgq.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m post_weight_quantization_30_b300.build` "
+        "(this package has no fallback path)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+GQ_F32, GQ_BF16 = 0, 1
+STATUS = {0: "GQ_OK", -1: "GQ_EINVAL", -2: "GQ_ENOTPD", -3: "GQ_EUNSUPPORTED", -4: "GQ_ECUDA",
+          -5: "GQ_ENONFINITE", -6: "GQ_ETIMEOUT", -7: "GQ_EWORKSPACE"}
+
+# name -> (restype, argtypes); the full exported surface of include/gq.h
+SIGNATURES = {
+    "gq_abi_version": (_i, []),
+    "gq_status_string": (ctypes.c_char_p, [_i]),
+    "gptq_hessian_accumulate": (_i, [_p, _i64, _p, _i, _i64, _i64, _p]),
+    "gptq_factor_workspace_size": (_sz, [_i64]),
+    "gptq_factor": (_i, [_p, _i64, _f, _p, _p, _p, _sz, _p, ctypes.POINTER(_i64)]),
+    "gptq_sweep_workspace_size": (_sz, [_i64, _i64, _i]),
+    "gptq_sweep": (_i, [_p, _i, _i64, _i64, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "gptq_quantize_layer_workspace_size": (_sz, [_i64, _i64, _i]),
+    "gptq_quantize_layer": (_i, [_p, _i, _i64, _i64, _p, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p, _sz, _p,
+                                 ctypes.POINTER(_i64)]),
+    "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
+    "gptq_unpack": (_i, [_p, _i64, _i64, _i, _p, _p]),
+}
+
+for _name, (_res, _args) in SIGNATURES.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class GQError(RuntimeError):
+    def __init__(self, status: int, where: str, info: int | None = None):
+        self.status = status
+        self.info = info
+        msg = lib.gq_status_string(status).decode()
+        super().__init__(f"{where}: {msg}" + (f" (info={info})" if info is not None and info >= 0 else ""))
+
+
+def _check(status: int, where: str, info: int | None = None):
+    if status != 0:
+        raise GQError(status, where, info)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GQ_BF16
+    if t.dtype == torch.float32:
+        return GQ_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must be CUDA device tensors")
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ entry points
+def gptq_hessian_accumulate(H: torch.Tensor, X: torch.Tensor) -> torch.Tensor:
+    """H += 2 X^T X (in place; returns H).  X: n x cols, row stride >= cols."""
+    _need_cuda(H, X)
+    n, cols = X.shape
+    if X.stride(1) != 1:
+        raise ValueError("X must have unit stride along its feature axis")
+    if H.dtype != torch.float32 or tuple(H.shape) != (cols, cols) or not H.is_contiguous():
+        raise ValueError("H must be a contiguous cols x cols float32 tensor")
+    _check(lib.gptq_hessian_accumulate(_ptr(H), cols, _ptr(X), _dtype_code(X), n, X.stride(0), _stream(X.device)),
+           "gptq_hessian_accumulate")
+    return H
+
+
+def gptq_factor(H: torch.Tensor, damp: float = 0.01):
+    """Returns (F, dead): H + damp*mean(diag)*I = F F^T with F upper; dead inputs."""
+    _need_cuda(H)
+    cols = H.shape[0]
+    F = torch.empty((cols, cols), dtype=torch.float32, device=H.device)
+    dead = torch.empty(cols, dtype=torch.uint8, device=H.device)
+    ws_bytes = lib.gptq_factor_workspace_size(cols)
+    ws = _workspace(ws_bytes, H.device)
+    info = _i64(-1)
+    _check(lib.gptq_factor(_ptr(H.contiguous()), cols, float(damp), _ptr(F), _ptr(dead), _ptr(ws), ws_bytes,
+                           _stream(H.device), ctypes.byref(info)), "gptq_factor", info.value)
+    return F, dead
+
+
+def _sweep_outputs(rows, cols, bits, group, device, codes, W_hat, row_err):
+    out = dict(
+        qweight=torch.empty((cols * bits // 32, rows), dtype=torch.int32, device=device),
+        scales=torch.empty((cols // group, rows), dtype=torch.float32, device=device),
+        qzeros=torch.empty((cols // group, rows * bits // 32), dtype=torch.int32, device=device),
+        codes=torch.empty((rows, cols), dtype=torch.uint8, device=device) if codes else None,
+        W_hat=torch.empty((rows, cols), dtype=torch.float32, device=device) if W_hat else None,
+        row_err=torch.empty(rows, dtype=torch.float32, device=device) if row_err else None,
+    )
+    return out
+
+
+def gptq_sweep(W: torch.Tensor, F: torch.Tensor, dead: torch.Tensor | None, bits: int, group: int, block: int = 128,
+               codes: bool = True, W_hat: bool = True, row_err: bool = True, workspace: torch.Tensor | None = None):
+    _need_cuda(W, F, dead)
+    rows, cols = W.shape
+    W = W.contiguous()
+    o = _sweep_outputs(rows, cols, bits, group, W.device, codes, W_hat, row_err)
+    ws_bytes = lib.gptq_sweep_workspace_size(rows, cols, block)
+    ws = workspace if workspace is not None else _workspace(ws_bytes, W.device)
+    _check(lib.gptq_sweep(_ptr(W), _dtype_code(W), rows, cols, _ptr(F), _ptr(dead), bits, group, block,
+                          _ptr(o["qweight"]), _ptr(o["scales"]), _ptr(o["qzeros"]), _ptr(o["codes"]),
+                          _ptr(o["W_hat"]), _ptr(o["row_err"]), _ptr(ws), ws.numel(), _stream(W.device)),
+           "gptq_sweep")
+    return o
+
+
+def gptq_quantize_layer(W: torch.Tensor, H: torch.Tensor, bits: int, group: int, block: int = 128,
+                        damp: float = 0.01, codes: bool = True, W_hat: bool = True, row_err: bool = True,
+                        workspace: torch.Tensor | None = None, out: dict | None = None):
+    """Dead inputs + damping, factor, sweep, packing.  Returns a dict of device tensors."""
+    _need_cuda(W, H)
+    rows, cols = W.shape
+    W = W.contiguous()
+    o = out if out is not None else _sweep_outputs(rows, cols, bits, group, W.device, codes, W_hat, row_err)
+    ws_bytes = lib.gptq_quantize_layer_workspace_size(rows, cols, block)
+    ws = workspace if workspace is not None else _workspace(ws_bytes, W.device)
+    info = _i64(-1)
+    _check(lib.gptq_quantize_layer(_ptr(W), _dtype_code(W), rows, cols, _ptr(H.contiguous()), bits, group, block,
+                                   float(damp), _ptr(o["qweight"]), _ptr(o["scales"]), _ptr(o["qzeros"]),
+                                   _ptr(o.get("codes")), _ptr(o.get("W_hat")), _ptr(o.get("row_err")), _ptr(ws),
+                                   ws.numel(), _stream(W.device), ctypes.byref(info)),
+           "gptq_quantize_layer", info.value)
+    return o
+
+
+def gptq_pack(codes: torch.Tensor, bits: int) -> torch.Tensor:
+    _need_cuda(codes)
+    rows, cols = codes.shape
+    qw = torch.empty((cols * bits // 32, rows), dtype=torch.int32, device=codes.device)
+    _check(lib.gptq_pack(_ptr(codes.contiguous()), rows, cols, bits, _ptr(qw), _stream(codes.device)), "gptq_pack")
+    return qw
+
+
+def gptq_unpack(qweight: torch.Tensor, rows: int, cols: int, bits: int) -> torch.Tensor:
+    _need_cuda(qweight)
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=qweight.device)
+    _check(lib.gptq_unpack(_ptr(qweight.contiguous()), rows, cols, bits, _ptr(codes), _stream(qweight.device)),
+           "gptq_unpack")
+    return codes

@@ -1,0 +1,210 @@
+// C ABI of libgq (declared in include/gq.h): argument validation, workspace
+// layout and the order of the stream-ordered launches.
+#include <climits>
+#include <cstring>
+
+#include "common.cuh"
+
+using namespace gq;
+
+namespace {
+
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+inline cudaStream_t cs(gq_stream_t s) { return (cudaStream_t)s; }
+
+size_t sweep_ws_bytes(int64_t rows, int64_t cols, int block) {
+    const int64_t nblk = (cols + block - 1) / block;
+    return align_up((size_t)nblk * block * block * sizeof(float)) + align_up((size_t)rows * cols * sizeof(float));
+}
+
+gq_status check_sweep_args(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *F, int bits,
+                           int group, int block, const int32_t *qweight, const float *scales,
+                           const int32_t *qzeros, const uint8_t *codes, const float *W_hat, const float *row_err) {
+    if (wt != GQ_F32 && wt != GQ_BF16) return GQ_EUNSUPPORTED;
+    if (bits != 2 && bits != 3 && bits != 4) return GQ_EUNSUPPORTED;
+    if (!W || !F || !qweight || !scales || !qzeros) return GQ_EINVAL;
+    if (rows <= 0 || cols <= 0 || rows % 32 || cols % 32) return GQ_EINVAL;
+    if (group <= 0 || group % 32 || cols % group) return GQ_EINVAL;
+    if (block <= 0 || block > 128 || block % group) return GQ_EINVAL;
+    if (!aligned(W, wt == GQ_F32 ? 16 : 8) || !aligned(scales, 16) || !aligned(qweight, 4) || !aligned(qzeros, 4))
+        return GQ_EINVAL;
+    if ((codes && !aligned(codes, 4)) || (W_hat && !aligned(W_hat, 16)) || (row_err && !aligned(row_err, 4)))
+        return GQ_EINVAL;
+    return GQ_OK;
+}
+
+struct SweepCtx {
+    const void *W;
+    bool bf16;
+    int64_t rows, cols;
+    const float *F;
+    const uint8_t *dead;
+    int bits, group, block;
+    int32_t *qweight;
+    float *scales;
+    int32_t *qzeros;
+    uint8_t *codes;
+    float *W_hat, *row_err;
+    float *Uinv, *D;
+    cudaStream_t s;
+};
+
+// Blocks [a, b): sweep the left half, apply its deferred update to the right
+// half as one GEMM, sweep the right half.  Same sums as updating after every
+// block, in fewer and larger GEMMs.
+cudaError_t sweep_range(const SweepCtx &c, int64_t a, int64_t b) {
+    const int64_t B = c.block;
+    if (b - a == 1) {
+        const int64_t c0 = a * B;
+        const int bw = (int)((c.cols - c0) < B ? (c.cols - c0) : B);
+        return sweep_block_launch(c.W, c.bf16, c.rows, c.cols, c0, bw, c.Uinv + a * B * B, c.dead, c.bits, c.group,
+                                  c.D, c.qweight, c.scales, c.qzeros, c.codes, c.W_hat, c.row_err, c.s);
+    }
+    const int64_t m = (a + b) / 2;
+    cudaError_t e = sweep_range(c, a, m);
+    if (e != cudaSuccess) return e;
+    const int64_t k0 = a * B, k1 = m * B, n1 = (b * B < c.cols) ? b * B : c.cols;
+    e = sgemm<float>(c.rows, n1 - k1, k1 - k0, 1.f, c.D + k0, c.cols, false, c.F + k0 * c.cols + k1, c.cols, false, 1.f,
+                     c.D + k1, c.cols, 0, c.s);
+    if (e != cudaSuccess) return e;
+    return sweep_range(c, m, b);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gq_abi_version(void) { return 1; }
+
+const char *gq_status_string(gq_status s) {
+    switch (s) {
+        case GQ_OK: return "GQ_OK";
+        case GQ_EINVAL: return "GQ_EINVAL: invalid argument";
+        case GQ_ENOTPD: return "GQ_ENOTPD: damped Hessian not positive definite";
+        case GQ_EUNSUPPORTED: return "GQ_EUNSUPPORTED: unsupported bit width or dtype";
+        case GQ_ECUDA: return "GQ_ECUDA: CUDA error";
+        case GQ_ENONFINITE: return "GQ_ENONFINITE: non-finite input";
+        case GQ_ETIMEOUT: return "GQ_ETIMEOUT: device wait gave up";
+        case GQ_EWORKSPACE: return "GQ_EWORKSPACE: workspace too small or misaligned";
+    }
+    return "GQ_?: unknown status";
+}
+
+gq_status gptq_hessian_accumulate(float *H, int64_t cols, const void *X, gq_dtype xt, int64_t n, int64_t ldx,
+                                  gq_stream_t stream) {
+    if (xt != GQ_F32 && xt != GQ_BF16) return GQ_EUNSUPPORTED;
+    if (cols <= 0 || n < 0 || ldx < cols) return GQ_EINVAL;
+    if (n == 0) return GQ_OK;
+    if (!H || !X) return GQ_EINVAL;
+    cudaError_t e;
+    if (xt == GQ_BF16) {
+        if (hessian_bf16_tc_supported(cols, X, ldx))
+            e = hessian_bf16_tc(H, cols, (const __nv_bfloat16 *)X, n, ldx, cs(stream));
+        else
+            e = sgemm<__nv_bfloat16>(cols, cols, n, 2.f, (const __nv_bfloat16 *)X, ldx, true, (const __nv_bfloat16 *)X,
+                                     ldx, false, 1.f, H, cols, 2, cs(stream));
+    } else {
+        e = sgemm<float>(cols, cols, n, 2.f, (const float *)X, ldx, true, (const float *)X, ldx, false, 1.f, H, cols, 2,
+                         cs(stream));
+    }
+    return e == cudaSuccess ? GQ_OK : GQ_ECUDA;
+}
+
+size_t gptq_factor_workspace_size(int64_t cols) {
+    (void)cols;
+    return factor_scratch_bytes();
+}
+
+gq_status gptq_factor(const float *H, int64_t cols, float damp, float *F, uint8_t *dead, void *ws, size_t ws_bytes,
+                      gq_stream_t stream, int64_t *info) {
+    if (cols <= 0 || !H || !F) return GQ_EINVAL;
+    if (!(damp >= 0.f)) return GQ_EINVAL;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < gptq_factor_workspace_size(cols)) return GQ_EWORKSPACE;
+    cudaStream_t s = cs(stream);
+    DeviceStatus *st = (DeviceStatus *)ws;
+    float *Linv = (float *)((char *)ws + align_up(sizeof(DeviceStatus)));
+    GQ_CUDA_TRY(cudaMemsetAsync(st, 0xFF, sizeof(DeviceStatus), s));
+    GQ_CUDA_TRY(factor_prepare(H, cols, damp, F, dead, st, s));
+    GQ_CUDA_TRY(cholesky_lower_inplace(F, cols, st, Linv, s));
+    GQ_CUDA_TRY(factor_finalize(F, cols, s));
+    unsigned long long bad = 0;
+    GQ_CUDA_TRY(cudaMemcpyAsync(&bad, &st->bad_pivot, sizeof(bad), cudaMemcpyDeviceToHost, s));
+    GQ_CUDA_TRY(cudaStreamSynchronize(s));
+    if (bad != ULLONG_MAX) {
+        if (info) *info = cols - 1 - (int64_t)bad;
+        return GQ_ENOTPD;
+    }
+    if (info) *info = -1;
+    return GQ_OK;
+}
+
+size_t gptq_sweep_workspace_size(int64_t rows, int64_t cols, int block) {
+    if (rows <= 0 || cols <= 0 || block <= 0) return 0;
+    return sweep_ws_bytes(rows, cols, block);
+}
+
+gq_status gptq_sweep(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *F, const uint8_t *dead,
+                     int bits, int group, int block, int32_t *qweight, float *scales, int32_t *qzeros, uint8_t *codes,
+                     float *W_hat, float *row_err, void *ws, size_t ws_bytes, gq_stream_t stream) {
+    gq_status st = check_sweep_args(W, wt, rows, cols, F, bits, group, block, qweight, scales, qzeros, codes, W_hat,
+                                    row_err);
+    if (st != GQ_OK) return st;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < sweep_ws_bytes(rows, cols, block)) return GQ_EWORKSPACE;
+    cudaStream_t s = cs(stream);
+    const int64_t nblk = (cols + block - 1) / block;
+    SweepCtx c;
+    c.W = W; c.bf16 = (wt == GQ_BF16); c.rows = rows; c.cols = cols; c.F = F; c.dead = dead;
+    c.bits = bits; c.group = group; c.block = block;
+    c.qweight = qweight; c.scales = scales; c.qzeros = qzeros; c.codes = codes; c.W_hat = W_hat; c.row_err = row_err;
+    c.Uinv = (float *)ws;
+    c.D = (float *)((char *)ws + align_up((size_t)nblk * block * block * sizeof(float)));
+    c.s = s;
+    GQ_CUDA_TRY(cudaMemsetAsync(c.D, 0, (size_t)rows * cols * sizeof(float), s));
+    if (row_err) GQ_CUDA_TRY(cudaMemsetAsync(row_err, 0, (size_t)rows * sizeof(float), s));
+    GQ_CUDA_TRY(block_inverses(F, cols, block, c.Uinv, s));
+    GQ_CUDA_TRY(sweep_range(c, 0, nblk));
+    return GQ_OK;
+}
+
+size_t gptq_quantize_layer_workspace_size(int64_t rows, int64_t cols, int block) {
+    if (rows <= 0 || cols <= 0 || block <= 0) return 0;
+    return align_up((size_t)cols * cols * sizeof(float)) + align_up((size_t)cols) + gptq_factor_workspace_size(cols) +
+           sweep_ws_bytes(rows, cols, block);
+}
+
+gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *H, int bits,
+                              int group, int block, float damp, int32_t *qweight, float *scales, int32_t *qzeros,
+                              uint8_t *codes, float *W_hat, float *row_err, void *ws, size_t ws_bytes,
+                              gq_stream_t stream, int64_t *info) {
+    if (!H) return GQ_EINVAL;
+    gq_status st = check_sweep_args(W, wt, rows, cols, H, bits, group, block, qweight, scales, qzeros, codes, W_hat,
+                                    row_err);
+    if (st != GQ_OK) return st;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < gptq_quantize_layer_workspace_size(rows, cols, block))
+        return GQ_EWORKSPACE;
+    char *p = (char *)ws;
+    float *F = (float *)p;
+    p += align_up((size_t)cols * cols * sizeof(float));
+    uint8_t *dead = (uint8_t *)p;
+    p += align_up((size_t)cols);
+    void *fws = p;
+    p += gptq_factor_workspace_size(cols);
+    st = gptq_factor(H, cols, damp, F, dead, fws, gptq_factor_workspace_size(cols), stream, info);
+    if (st != GQ_OK) return st;
+    return gptq_sweep(W, wt, rows, cols, F, dead, bits, group, block, qweight, scales, qzeros, codes, W_hat, row_err, p,
+                      sweep_ws_bytes(rows, cols, block), stream);
+}
+
+gq_status gptq_pack(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight, gq_stream_t stream) {
+    if (bits != 2 && bits != 3 && bits != 4) return GQ_EUNSUPPORTED;
+    if (!codes || !qweight || rows <= 0 || cols <= 0 || (cols * bits) % 32) return GQ_EINVAL;
+    return pack_launch(codes, rows, cols, bits, qweight, cs(stream)) == cudaSuccess ? GQ_OK : GQ_ECUDA;
+}
+
+gq_status gptq_unpack(const int32_t *qweight, int64_t rows, int64_t cols, int bits, uint8_t *codes, gq_stream_t stream) {
+    if (bits != 2 && bits != 3 && bits != 4) return GQ_EUNSUPPORTED;
+    if (!codes || !qweight || rows <= 0 || cols <= 0 || (cols * bits) % 32) return GQ_EINVAL;
+    return unpack_launch(qweight, rows, cols, bits, codes, cs(stream)) == cudaSuccess ? GQ_OK : GQ_ECUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Shared definitions of the libgq CUDA sources (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gq.h"
+
+#define GQ_CUDA_TRY(expr)                                     \
+    do {                                                      \
+        cudaError_t err__ = (expr);                           \
+        if (err__ != cudaSuccess) return GQ_ECUDA;            \
+    } while (0)
+
+#define GQ_LAUNCH_CHECK()                                     \
+    do {                                                      \
+        if (cudaGetLastError() != cudaSuccess) return GQ_ECUDA; \
+    } while (0)
+
+namespace gq {
+
+// Device status block kept in the workspace.  `bad_pivot` holds the first input
+// column (in original index order) whose Cholesky pivot was not positive, or
+// INT64_MAX when every pivot was fine.
+struct DeviceStatus {
+    unsigned long long bad_pivot;
+    double diag_sum;
+    float delta;
+    int pad;
+};
+
+static constexpr size_t kAlign = 256;
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+template <typename T>
+__device__ __forceinline__ float load_f32(const T *p);
+template <>
+__device__ __forceinline__ float load_f32<float>(const float *p) { return *p; }
+template <>
+__device__ __forceinline__ float load_f32<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+// ----------------------------------------------------------------------------
+// Kernel launchers implemented in the .cu files (all enqueue on `s`).
+// ----------------------------------------------------------------------------
+
+// C[m, n] = beta * C[m, n] + alpha * sum_k A(m, k) B(k, n) in float32 on the SIMT
+// pipes.  A(m, k) = a_t ? A[k * lda + m] : A[m * lda + k];
+// B(k, n) = b_t ? B[n * ldb + k] : B[k * ldb + n].
+// tri: 0 = full; 1 = only tiles that touch the lower triangle (m >= n);
+//      2 = only tiles that touch the upper triangle, each off-diagonal tile
+//      also written transposed (symmetric output).
+template <typename TA>
+cudaError_t sgemm(int64_t M, int64_t N, int64_t K, float alpha, const TA *A, int64_t lda, bool a_t,
+                  const TA *B, int64_t ldb, bool b_t, float beta, float *C, int64_t ldc, int tri,
+                  cudaStream_t s);
+
+// Hessian accumulation on the tensor cores (bf16 inputs, tcgen05 + TMA).
+cudaError_t hessian_bf16_tc(float *H, int64_t cols, const __nv_bfloat16 *X, int64_t n, int64_t ldx,
+                            cudaStream_t s);
+bool hessian_bf16_tc_supported(int64_t cols, const void *X, int64_t ldx);
+
+// Factor pieces.
+cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, uint8_t *dead,
+                           DeviceStatus *st, cudaStream_t s);
+// Linv: 64 x 64 float32 scratch.
+cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *Linv, cudaStream_t s);
+cudaError_t factor_finalize(float *F, int64_t cols, cudaStream_t s);
+size_t factor_scratch_bytes();
+
+// Sweep pieces.
+cudaError_t block_inverses(const float *F, int64_t cols, int block, float *Uinv, cudaStream_t s);
+cudaError_t sweep_block_launch(const void *W, bool w_bf16, int64_t rows, int64_t cols, int64_t c0,
+                               int bw, const float *Uinv_blk, const uint8_t *dead, int bits, int group,
+                               float *D, int32_t *qweight, float *scales, int32_t *qzeros,
+                               uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s);
+
+cudaError_t pack_launch(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight,
+                        cudaStream_t s);
+cudaError_t unpack_launch(const int32_t *qweight, int64_t rows, int64_t cols, int bits,
+                          uint8_t *codes, cudaStream_t s);
+
+}  // namespace gq

@@ -1,0 +1,74 @@
+// Standalone packing of b-bit codes into 32-bit words and its inverse.  Layout
+// (this library's reading of the packing layout that [LowBit] section 1 says a
+// format must fix): little-endian bitstream along the input axis, code k at
+// bits [k*b, k*b + b), cut into 32-bit words; qweight is [cols*b/32][rows].
+#include "common.cuh"
+
+namespace gq {
+namespace {
+
+template <int BITS>
+__global__ void pack_kernel(const uint8_t *__restrict__ codes, int64_t rows, int64_t cols,
+                            int32_t *__restrict__ qweight) {
+    const int64_t nw = cols * BITS / 32;
+    const int64_t total = nw * rows;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t w = idx / rows, r = idx % rows;  // consecutive threads -> consecutive rows
+        const uint8_t *v = codes + r * cols;
+        uint32_t word = 0;
+        const int64_t k_lo = (32 * w) / BITS, k_hi = (32 * w + 31) / BITS;
+        for (int64_t k = k_lo; k <= k_hi && k < cols; ++k) {
+            const int64_t pos = k * BITS - 32 * w;
+            const uint32_t x = v[k] & ((1u << BITS) - 1u);
+            if (pos >= 0)
+                word |= (pos < 32) ? (x << pos) : 0u;
+            else
+                word |= x >> (-pos);
+        }
+        qweight[idx] = (int32_t)word;
+    }
+}
+
+template <int BITS>
+__global__ void unpack_kernel(const int32_t *__restrict__ qweight, int64_t rows, int64_t cols,
+                              uint8_t *__restrict__ codes) {
+    const int64_t total = rows * cols;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = idx / cols, k = idx % cols;
+        const int64_t pos = k * BITS, w = pos / 32, sh = pos % 32;
+        uint64_t v = (uint32_t)qweight[w * rows + r];
+        if (sh + BITS > 32) v |= (uint64_t)(uint32_t)qweight[(w + 1) * rows + r] << 32;
+        codes[idx] = (uint8_t)((v >> sh) & ((1u << BITS) - 1u));
+    }
+}
+
+unsigned grid_for(int64_t total) {
+    int64_t g = (total + 255) / 256;
+    return (unsigned)(g < 148 * 16 ? (g < 1 ? 1 : g) : 148 * 16);
+}
+
+}  // namespace
+
+cudaError_t pack_launch(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight,
+                        cudaStream_t s) {
+    const unsigned g = grid_for(cols * bits / 32 * rows);
+    if (bits == 2) pack_kernel<2><<<g, 256, 0, s>>>(codes, rows, cols, qweight);
+    else if (bits == 3) pack_kernel<3><<<g, 256, 0, s>>>(codes, rows, cols, qweight);
+    else if (bits == 4) pack_kernel<4><<<g, 256, 0, s>>>(codes, rows, cols, qweight);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t unpack_launch(const int32_t *qweight, int64_t rows, int64_t cols, int bits, uint8_t *codes,
+                          cudaStream_t s) {
+    const unsigned g = grid_for(rows * cols);
+    if (bits == 2) unpack_kernel<2><<<g, 256, 0, s>>>(qweight, rows, cols, codes);
+    else if (bits == 3) unpack_kernel<3><<<g, 256, 0, s>>>(qweight, rows, cols, codes);
+    else if (bits == 4) unpack_kernel<4><<<g, 256, 0, s>>>(qweight, rows, cols, codes);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace gq

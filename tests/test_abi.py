@@ -1,0 +1,76 @@
+"""The C ABI: the library loads, exports every declared entry point, and rejects bad
+arguments on the host before touching the GPU.  CPU only (no kernel runs)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("if", "typedef"):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def gq():
+    import post_weight_quantization_30_b300 as gq
+
+    return gq
+
+
+def test_every_declared_symbol_is_exported(gq):
+    declared = _declared_functions()
+    assert "gptq_quantize_layer" in declared and "gptq_hessian_accumulate" in declared
+    for name in declared:
+        assert hasattr(gq.lib, name), f"{name} declared in include/ but not exported"
+        assert name in gq.SIGNATURES, f"{name} has no binding"
+
+
+def test_abi_version_and_status_strings(gq):
+    assert gq.lib.gq_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert gq.lib.gq_status_string(code).decode().startswith("GQ_")
+
+
+def test_workspace_queries(gq):
+    r, c, b = 4096, 4096, 128
+    sw = gq.lib.gptq_sweep_workspace_size(r, c, b)
+    assert sw >= r * c * 4 + (c // b) * b * b * 4
+    ql = gq.lib.gptq_quantize_layer_workspace_size(r, c, b)
+    assert ql >= sw + c * c * 4
+    assert gq.lib.gptq_sweep_workspace_size(0, c, b) == 0
+
+
+def _call_sweep(gq, bits=4, group=128, block=128, rows=64, cols=256, W=1, F=1, ws=None, ws_bytes=0):
+    p = ctypes.c_void_p
+    return gq.lib.gptq_sweep(p(W), 1, rows, cols, p(F), None, bits, group, block, p(256), p(256), p(256), None, None,
+                             None, p(ws), ws_bytes, None)
+
+
+def test_host_side_validation(gq):
+    assert _call_sweep(gq, bits=5) == -3          # unsupported bit width
+    assert _call_sweep(gq, bits=1) == -3
+    assert _call_sweep(gq, group=48) == -1        # group must be a multiple of 32
+    assert _call_sweep(gq, block=192) == -1       # block <= 128
+    assert _call_sweep(gq, group=128, block=64) == -1  # block % group
+    assert _call_sweep(gq, rows=48) == -1         # rows % 32
+    assert _call_sweep(gq, cols=200, group=32, block=32) == -1
+    assert _call_sweep(gq, W=0) == -1             # null input
+    assert _call_sweep(gq, W=256, F=256) == -7    # missing workspace
+    # n == 0 is a no-op that returns before any CUDA call
+    assert gq.lib.gptq_hessian_accumulate(None, 256, None, 1, 0, 256, None) == 0
+    assert gq.lib.gptq_hessian_accumulate(None, 256, None, 7, 0, 256, None) == -3
+    assert gq.lib.gptq_hessian_accumulate(None, 256, None, 1, 10, 100, None) == -1  # ldx < cols
+    assert gq.lib.gptq_pack(None, 4, 32, 3, None, None) == -1
+    assert gq.lib.gptq_pack(ctypes.c_void_p(16), 4, 36, 3, ctypes.c_void_p(16), None) == -1  # cols*bits % 32
