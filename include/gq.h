@@ -58,6 +58,13 @@ int gq_abi_version(void);
 const char *gq_status_string(gq_status s);
 
 /*
+ * Synchronizes `stream`, then reports whether any bounded device-side wait of
+ * the library's kernels gave up since the previous call (GQ_ETIMEOUT; the
+ * affected outputs are then invalid) and clears that record.  GQ_OK otherwise.
+ */
+gq_status gq_check_device(gq_stream_t stream);
+
+/*
  * H += 2 X^T X.
  *
  * The second-order statistics of the layer inputs: the Hessian of the layer's

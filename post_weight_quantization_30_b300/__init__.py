@@ -14,5 +14,6 @@ from ._lib import (  # noqa: F401
     gptq_quantize_layer,
     gptq_sweep,
     gptq_unpack,
+    gq_check_device,
     lib,
 )

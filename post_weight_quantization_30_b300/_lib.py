@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libgq.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m post_weight_quantization_30_b300.build` "
+        f"{LIB_PATH} is missing: build it with `python post_weight_quantization_30_b300/build.py` "
         "(this package has no fallback path)")
 
 lib = ctypes.CDLL(LIB_PATH)
@@ -38,6 +38,7 @@ STATUS = {0: "GQ_OK", -1: "GQ_EINVAL", -2: "GQ_ENOTPD", -3: "GQ_EUNSUPPORTED", -
 SIGNATURES = {
     "gq_abi_version": (_i, []),
     "gq_status_string": (ctypes.c_char_p, [_i]),
+    "gq_check_device": (_i, [_p]),
     "gptq_hessian_accumulate": (_i, [_p, _i64, _p, _i, _i64, _i64, _p]),
     "gptq_factor_workspace_size": (_sz, [_i64]),
     "gptq_factor": (_i, [_p, _i64, _f, _p, _p, _p, _sz, _p, ctypes.POINTER(_i64)]),
@@ -167,6 +168,12 @@ def gptq_quantize_layer(W: torch.Tensor, H: torch.Tensor, bits: int, group: int,
                                    ws.numel(), _stream(W.device), ctypes.byref(info)),
            "gptq_quantize_layer", info.value)
     return o
+
+
+def gq_check_device(device=None):
+    """Raise GQError(GQ_ETIMEOUT) if a bounded device-side wait gave up since the last check."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(lib.gq_check_device(_stream(dev)), "gq_check_device")
 
 
 def gptq_pack(codes: torch.Tensor, bits: int) -> torch.Tensor:

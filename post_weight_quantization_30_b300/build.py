@@ -1,6 +1,7 @@
 """Build libgq.so (all CUDA sources under csrc/) for sm_103a, in place.
 
-Usage: python -m post_weight_quantization_30_b300.build [--verbose]
+Usage: python post_weight_quantization_30_b300/build.py [--verbose]
+(run by path: importing the package itself loads the library it builds)
 """
 from __future__ import annotations
 

@@ -90,6 +90,13 @@ const char *gq_status_string(gq_status s) {
     return "GQ_?: unknown status";
 }
 
+gq_status gq_check_device(gq_stream_t stream) {
+    if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return GQ_ECUDA;
+    const unsigned int e = read_and_clear_device_error();
+    if (e == ~0u) return GQ_ECUDA;
+    return e ? GQ_ETIMEOUT : GQ_OK;
+}
+
 gq_status gptq_hessian_accumulate(float *H, int64_t cols, const void *X, gq_dtype xt, int64_t n, int64_t ldx,
                                   gq_stream_t stream) {
     if (xt != GQ_F32 && xt != GQ_BF16) return GQ_EUNSUPPORTED;

@@ -60,6 +60,8 @@ cudaError_t sgemm(int64_t M, int64_t N, int64_t K, float alpha, const TA *A, int
 cudaError_t hessian_bf16_tc(float *H, int64_t cols, const __nv_bfloat16 *X, int64_t n, int64_t ldx,
                             cudaStream_t s);
 bool hessian_bf16_tc_supported(int64_t cols, const void *X, int64_t ldx);
+// Error bits recorded by bounded device-side waits since the last call (then cleared).
+unsigned int read_and_clear_device_error();
 
 // Factor pieces.
 cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, uint8_t *dead,

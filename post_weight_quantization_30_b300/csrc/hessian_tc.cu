@@ -1,18 +1,382 @@
 // Hessian accumulation H += 2 X^T X for bf16 X on the fifth-generation tensor
-// cores (tcgen05, TMEM accumulators, TMA loads).  Placeholder until the kernel
-// lands: the SIMT float32 GEMM serves every shape meanwhile.
+// cores: the second-order statistics of the layer inputs that GPTQ's updates
+// are built from ([GPTQ-wiki] "Enfoque Técnico"; [LowBit] section 2).
+//
+// Design (sm_103a):
+// * One CTA per output tile of 128 x 256 features, only for tiles that touch the
+//   upper triangle; each element of H is written by exactly one CTA: the
+//   upper triangle (c >= r) directly and the strict lower triangle as the
+//   mirror, so H stays bit-for-bit symmetric and the result is deterministic.
+// * A = X^T[i-tile, tokens] and B = X[tokens, j-tile] are both read straight
+//   from the row-major X (features contiguous): MN-major operands, loaded by
+//   TMA as 64-token x 64-feature boxes with 128-byte swizzle.  Four-stage
+//   mbarrier pipeline, 48 KB per stage.
+// * Warp 0 / lane 0 issues the TMA loads, warp 1 / lane 0 issues
+//   tcgen05.mma (kind::f16, bf16 x bf16 -> f32, M = 128, N = 256, K = 16) into a
+//   256-column TMEM accumulator; tcgen05.commit releases shared-memory stages
+//   and finally signals the epilogue.
+// * Epilogue: the four warps read their 32 TMEM lanes (one output row each)
+//   with tcgen05.ld and add 2 * acc into H.
+// * Every wait on an mbarrier is bounded (clock64 budget); on expiry the CTA
+//   records an error flag, drains what it issued, frees TMEM and returns.
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace gq {
 
+__device__ unsigned int g_device_error = 0;  // bit 0: a bounded wait gave up
+
+namespace {
+
+constexpr int TM = 128, TN = 256, TK = 64;  // tile rows, cols, tokens per stage
+constexpr int STAGES = 4;
+constexpr int BOX_BYTES = TK * 64 * 2;             // one 64-token x 64-feature bf16 box
+constexpr int A_BYTES = 2 * BOX_BYTES;             // 128 features
+constexpr int B_BYTES = 4 * BOX_BYTES;             // 256 features
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 48 KB
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr long long WAIT_BUDGET = 4000000000LL;    // clock cycles (~2 s)
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false if the phase did not complete within the budget.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > WAIT_BUDGET) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading / stride
+// byte offsets, fixed version bits 0b001 at [46, 49), 128-byte swizzle (2) at [61, 64).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both MN-major, N, M.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Warp roles: 0 = TMA producer, 1 = MMA issuer, 2..9 = accumulator warps.
+// The tensor-core accumulator is summed over KF k-tiles (256 tokens) at a
+// time in one of two TMEM buffers; the accumulator warps add each partial
+// sum into float32 registers (round-to-nearest) while the MMAs fill the other
+// buffer.  Long in-TMEM accumulation is avoided because each accumulate step
+// of the tensor core loses about half an ulp of the running sum.
+constexpr int KF = 4;
+constexpr int NWARPS = 10;
+constexpr int EPI_WARPS = 8;
+
+__global__ void __launch_bounds__(NWARPS * 32, 1)
+    hessian_tc_kernel(const __grid_constant__ CUtensorMap xmap, float *__restrict__ H, int cols, int n) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    __shared__ __align__(8) uint64_t tfull[2];
+    __shared__ __align__(8) uint64_t tempty[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // Tile of this CTA among the tiles that touch the upper triangle, row-major.
+    const int nbi = (cols + TM - 1) / TM, nbj = (cols + TN - 1) / TN;
+    int t = blockIdx.x, bi = 0;
+    for (; bi < nbi; ++bi) {
+        const int cnt = nbj - (bi * TM) / TN;
+        if (t < cnt) break;
+        t -= cnt;
+    }
+    const int bj = (bi * TM) / TN + t;
+    const int r0 = bi * TM, c0 = bj * TN;
+    const int ktiles = (n + TK - 1) / TK;
+    const int periods = (ktiles + KF - 1) / KF;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], EPI_WARPS);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(2 * TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kt = 0; kt < ktiles; ++kt) {
+                const int s = kt % STAGES;
+                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                if (!mbar_wait(&empty_bar[s], ph ^ 1u) || *(volatile int *)&abort_flag) {
+                    atomicOr(&g_device_error, 1u);
+                    abort_flag = 1;
+                    break;
+                }
+                unsigned char *st = smem + s * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
+                const int y = kt * TK;
+                tma_load_2d(st + 0 * BOX_BYTES, &xmap, r0, y, &full_bar[s]);
+                tma_load_2d(st + 1 * BOX_BYTES, &xmap, r0 + 64, y, &full_bar[s]);
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    tma_load_2d(st + A_BYTES + b * BOX_BYTES, &xmap, c0 + 64 * b, y, &full_bar[s]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(TM, TN);
+            bool ok = true;
+            for (int p = 0; p < periods && ok; ++p) {
+                const int b = p & 1;
+                const uint32_t u = (uint32_t)(p >> 1) & 1u;
+                if (!mbar_wait(&tempty[b], u ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const uint32_t acc = tmem + (uint32_t)(b * TMEM_COLS);
+                const int k_end = (p + 1) * KF < ktiles ? (p + 1) * KF : ktiles;
+                for (int kt = p * KF; kt < k_end; ++kt) {
+                    const int s = kt % STAGES;
+                    const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                    if (!mbar_wait(&full_bar[s], ph)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t a0 = smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < TK / 16; ++kk) {
+                        // 16 tokens = two 8-row core-matrix groups (SBO = 1024 B apart);
+                        // 64-feature chunks are whole boxes (LBO = box size apart).
+                        const uint64_t ad = smem_desc(a0 + kk * 2048, BOX_BYTES, 1024);
+                        const uint64_t bd = smem_desc(b0 + kk * 2048, BOX_BYTES, 1024);
+                        mma_bf16(acc, ad, bd, idesc, (kt > p * KF || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&empty_bar[s]);
+                }
+                mma_commit(&tfull[b]);
+            }
+            if (!ok) {
+                atomicOr(&g_device_error, 1u);
+                abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // Accumulator warps: TMEM lane quarter = warp % 4 (hardware rule), column
+        // half = (warp - 2) / 4.  Each thread owns one row x 128 columns.
+        const int q = warp & 3, half = (warp - 2) >> 2;
+        float master[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) master[i] = 0.f;
+        bool ok = true;
+        for (int p = 0; p < periods; ++p) {
+            const int b = p & 1;
+            const uint32_t u = (uint32_t)(p >> 1) & 1u;
+            if (!mbar_wait(&tfull[b], u)) {
+                ok = false;
+                break;
+            }
+            __syncwarp();
+            fence_after();
+            const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TMEM_COLS + half * 128);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                float v[32];
+                tmem_ld32(base + ch * 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) master[ch * 32 + i] += v[i];
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+        }
+        if (!ok) {
+            atomicOr(&g_device_error, 1u);
+            abort_flag = 1;
+        }
+        __syncwarp();
+        // H += 2 * master: upper triangle directly, strict lower as the mirror.
+        const int r = r0 + q * 32 + lane;
+        const int cb = c0 + half * 128;
+        if (ok && r < cols && periods > 0) {
+#pragma unroll
+            for (int j = 0; j < 128; ++j) {
+                const int c = cb + j;
+                if (c < cols && c >= r) {
+                    const float add = 2.f * master[j];
+                    H[(int64_t)r * cols + c] += add;
+                    if (c > r) H[(int64_t)c * cols + r] += add;
+                }
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * TMEM_COLS)
+                     : "memory");
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+}  // namespace
+
+unsigned int read_and_clear_device_error() {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return ~0u;
+    const unsigned int zero = 0;
+    if (v) cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    return v;
+}
+
 bool hessian_bf16_tc_supported(int64_t cols, const void *X, int64_t ldx) {
-    (void)cols; (void)X; (void)ldx;
-    return false;
+    if (cols < 64 || cols > (1 << 20) || cols % 8) return false;
+    if (((uintptr_t)X) % 16 || ldx % 8) return false;
+    return encode_fn() != nullptr;
 }
 
 cudaError_t hessian_bf16_tc(float *H, int64_t cols, const __nv_bfloat16 *X, int64_t n, int64_t ldx, cudaStream_t s) {
-    (void)H; (void)cols; (void)X; (void)n; (void)ldx; (void)s;
-    return cudaErrorNotSupported;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int64_t max_chunk = (int64_t)1 << 30;  // token coordinates are 32-bit
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(hessian_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int nbi = (int)((cols + TM - 1) / TM), nbj = (int)((cols + TN - 1) / TN);
+    int tiles = 0;
+    for (int bi = 0; bi < nbi; ++bi) tiles += nbj - (bi * TM) / TN;
+    for (int64_t t0 = 0; t0 < n; t0 += max_chunk) {
+        const int64_t nc = (n - t0) < max_chunk ? (n - t0) : max_chunk;
+        CUtensorMap map;
+        cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)nc};
+        cuuint64_t gstride[1] = {(cuuint64_t)ldx * 2};
+        cuuint32_t box[2] = {64, TK};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)(X + t0 * ldx), gdim, gstride, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        hessian_tc_kernel<<<tiles, NWARPS * 32, SMEM_BYTES, s>>>(map, H, (int)cols, (int)nc);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace gq

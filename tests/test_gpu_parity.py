@@ -48,7 +48,7 @@ def test_pack_unpack_bit_exact(gq, bits, rows, cols):
 
 # ------------------------------------------------------------------ hessian ---
 @pytest.mark.parametrize("n,cols,dtype", [(1000, 96, "bf16"), (4099, 384, "bf16"), (2048, 256, "f32"),
-                                          (777, 200, "f32"), (8192, 1024, "bf16")])
+                                          (777, 200, "f32"), (8192, 1024, "bf16"), (65536, 512, "bf16")])
 def test_hessian_parity(gq, n, cols, dtype):
     spec = custom_layer("h", 32, cols, n, dtype=dtype, n_outliers=max(1, cols // 100), key=(11, n, cols)).X
     a, x64 = host_arrays(spec)
