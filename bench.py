@@ -99,11 +99,11 @@ class ClockSampler:
 
 def launches_per_step(rows: int, cols: int, block: int) -> int:
     """Kernels of libgq launched by one step (Hessian + factor + sweep)."""
-    nb_panel = 64
+    nb_panel = 128
     panels = -(-cols // nb_panel)
-    factor = 2 + panels + 2 * (panels - 1) + 1  # diag sum, reversal; potrf per panel; trsm + gemm but last; finalize
+    factor = 2 + panels + 2 * (panels - 1) + 1  # diag sum, reversal; diagonal block per panel; solve + update but last; finalize
     nblk = -(-cols // block)
-    sweep = 1 + nblk + (nblk - 1)  # block inverses; one sweep per block; one deferred GEMM per split
+    sweep = 2 + nblk + (nblk - 1)  # block inverses, premultiply; one sweep per block; one deferred GEMM per split
     return 1 + factor + sweep
 
 

@@ -12,9 +12,11 @@ namespace {
 inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline cudaStream_t cs(gq_stream_t s) { return (cudaStream_t)s; }
 
+// Sweep workspace: [Uinv: nblk x block x block][V: cols x cols][D: rows x cols], float32.
 size_t sweep_ws_bytes(int64_t rows, int64_t cols, int block) {
     const int64_t nblk = (cols + block - 1) / block;
-    return align_up((size_t)nblk * block * block * sizeof(float)) + align_up((size_t)rows * cols * sizeof(float));
+    return align_up((size_t)nblk * block * block * sizeof(float)) + align_up((size_t)cols * cols * sizeof(float)) +
+           align_up((size_t)rows * cols * sizeof(float));
 }
 
 gq_status check_sweep_args(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *F, int bits,
@@ -45,7 +47,7 @@ struct SweepCtx {
     int32_t *qzeros;
     uint8_t *codes;
     float *W_hat, *row_err;
-    float *Uinv, *D;
+    float *Uinv, *V, *D;
     cudaStream_t s;
 };
 
@@ -57,14 +59,14 @@ cudaError_t sweep_range(const SweepCtx &c, int64_t a, int64_t b) {
     if (b - a == 1) {
         const int64_t c0 = a * B;
         const int bw = (int)((c.cols - c0) < B ? (c.cols - c0) : B);
-        return sweep_block_launch(c.W, c.bf16, c.rows, c.cols, c0, bw, c.Uinv + a * B * B, c.dead, c.bits, c.group,
+        return sweep_block_launch(c.W, c.bf16, c.rows, c.cols, c0, bw, c.Uinv + a * B * B, c.F, c.dead, c.bits, c.group,
                                   c.D, c.qweight, c.scales, c.qzeros, c.codes, c.W_hat, c.row_err, c.s);
     }
     const int64_t m = (a + b) / 2;
     cudaError_t e = sweep_range(c, a, m);
     if (e != cudaSuccess) return e;
     const int64_t k0 = a * B, k1 = m * B, n1 = (b * B < c.cols) ? b * B : c.cols;
-    e = sgemm<float>(c.rows, n1 - k1, k1 - k0, 1.f, c.D + k0, c.cols, false, c.F + k0 * c.cols + k1, c.cols, false, 1.f,
+    e = sgemm<float>(c.rows, n1 - k1, k1 - k0, 1.f, c.D + k0, c.cols, false, c.V + k0 * c.cols + k1, c.cols, false, 1.f,
                      c.D + k1, c.cols, 0, c.s);
     if (e != cudaSuccess) return e;
     return sweep_range(c, m, b);
@@ -164,11 +166,13 @@ gq_status gptq_sweep(const void *W, gq_dtype wt, int64_t rows, int64_t cols, con
     c.bits = bits; c.group = group; c.block = block;
     c.qweight = qweight; c.scales = scales; c.qzeros = qzeros; c.codes = codes; c.W_hat = W_hat; c.row_err = row_err;
     c.Uinv = (float *)ws;
-    c.D = (float *)((char *)ws + align_up((size_t)nblk * block * block * sizeof(float)));
+    c.V = (float *)((char *)ws + align_up((size_t)nblk * block * block * sizeof(float)));
+    c.D = (float *)((char *)c.V + align_up((size_t)cols * cols * sizeof(float)));
     c.s = s;
     GQ_CUDA_TRY(cudaMemsetAsync(c.D, 0, (size_t)rows * cols * sizeof(float), s));
     if (row_err) GQ_CUDA_TRY(cudaMemsetAsync(row_err, 0, (size_t)rows * sizeof(float), s));
     GQ_CUDA_TRY(block_inverses(F, cols, block, c.Uinv, s));
+    GQ_CUDA_TRY(premultiply(F, cols, block, c.Uinv, c.V, s));
     GQ_CUDA_TRY(sweep_range(c, 0, nblk));
     return GQ_OK;
 }

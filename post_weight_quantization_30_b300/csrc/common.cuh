@@ -66,15 +66,17 @@ unsigned int read_and_clear_device_error();
 // Factor pieces.
 cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, uint8_t *dead,
                            DeviceStatus *st, cudaStream_t s);
-// Linv: 64 x 64 float32 scratch.
+// Linv: 128 x 128 float32 scratch.
 cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *Linv, cudaStream_t s);
 cudaError_t factor_finalize(float *F, int64_t cols, cudaStream_t s);
 size_t factor_scratch_bytes();
 
 // Sweep pieces.
 cudaError_t block_inverses(const float *F, int64_t cols, int block, float *Uinv, cudaStream_t s);
+// V[rows above block b, blk_b] = F[..., blk_b] Uinv_b for every block column b (V may alias F).
+cudaError_t premultiply(const float *F, int64_t cols, int block, const float *Uinv, float *V, cudaStream_t s);
 cudaError_t sweep_block_launch(const void *W, bool w_bf16, int64_t rows, int64_t cols, int64_t c0,
-                               int bw, const float *Uinv_blk, const uint8_t *dead, int bits, int group,
+                               int bw, const float *Uinv_blk, const float *F, const uint8_t *dead, int bits, int group,
                                float *D, int32_t *qweight, float *scales, int32_t *qzeros,
                                uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s);
 

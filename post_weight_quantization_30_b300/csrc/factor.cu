@@ -10,19 +10,17 @@
 // Steps (all float32):
 //   1. prepare: dead inputs (H_ii == 0 -> 1), damping delta = damp * mean(diag),
 //      index reversal into F (lower triangle of J H_d J; the upper part zeroed);
-//   2. blocked right-looking Cholesky of F in place, panel width 64: the
-//      diagonal block is factored in shared memory by one CTA (which also
-//      inverts it), the panel below is solved with that inverse, and the
-//      trailing lower triangle is updated with the float32 SIMT GEMM;
+//   2. blocked right-looking Cholesky of F in place, panel width 128: the
+//      diagonal block is factored and inverted in shared memory by one CTA,
+//      the panel below is multiplied by the transposed inverse, and the
+//      trailing lower triangle is updated, both with the float32 SIMT GEMM;
 //   3. finalize: F <- J L J in place (strictly-lower part zeroed).
-#include <cfloat>
-
 #include "common.cuh"
 
 namespace gq {
 namespace {
 
-constexpr int NB = 64;
+constexpr int NB = 128;  // panel width
 
 __global__ void diag_sum_kernel(const float *__restrict__ H, int64_t cols, float damp, DeviceStatus *st) {
     __shared__ double red[32];
@@ -63,86 +61,91 @@ __global__ void reverse_damp_kernel(const float *__restrict__ H, int64_t cols, f
     }
 }
 
-// Unblocked Cholesky of the kb x kb diagonal block at (k0, k0) in shared memory,
-// followed by the inverse of the factor (written to Linv, kb x kb row-major).
-__global__ void __launch_bounds__(256) potrf_diag_kernel(float *__restrict__ F, int64_t cols, int64_t k0,
-                                                         int kb, float *__restrict__ Linv,
-                                                         DeviceStatus *st) {
-    __shared__ float A[NB][NB + 1];
-    __shared__ float Y[NB][NB + 1];
+// Cholesky of the kb x kb diagonal block at (k0, k0) (kb <= NB) in shared
+// memory, followed by the inverse of the factor (written to Linv, NB x NB
+// row-major, zero above the diagonal).  Each thread owns a fixed set of
+// lower-triangle elements.  Elimination step j subtracts a_ij a_kj / a_jj from
+// every a_ik with j < k <= i, using column j as left by the earlier steps
+// (unscaled), so a step needs one barrier; the factor is a_ij / sqrt(a_jj)
+// afterwards.  The inverse is built the same way (right-looking, one barrier
+// per step): R_ic -= (L_ik / L_kk) R_kc, then Y_ic = R_ic / L_ii.
+constexpr int DIAG_THREADS = 512;
+constexpr int TRI = NB * (NB + 1) / 2;
+constexpr int DIAG_OWN = (TRI + DIAG_THREADS - 1) / DIAG_THREADS;
+constexpr size_t DIAG_SMEM = 2 * NB * (NB + 1) * sizeof(float);
+
+__global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restrict__ F, int64_t cols, int64_t k0,
+                                                                  int kb, float *__restrict__ Linv,
+                                                                  DeviceStatus *st) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float(*A)[NB + 1] = reinterpret_cast<float(*)[NB + 1]>(smem_raw);
+    float(*Y)[NB + 1] = A + NB;
     const int t = threadIdx.x;
-    for (int idx = t; idx < NB * NB; idx += blockDim.x) {
-        int i = idx / NB, j = idx % NB;
+    int own[DIAG_OWN];
+#pragma unroll
+    for (int q = 0; q < DIAG_OWN; ++q) {
+        const int e = t + q * DIAG_THREADS;
+        int i = (int)((sqrtf(8.f * (float)e + 1.f) - 1.f) * 0.5f);
+        while ((i + 1) * (i + 2) / 2 <= e) ++i;
+        while (i * (i + 1) / 2 > e) --i;
+        const int k = e - i * (i + 1) / 2;
+        own[q] = (e < TRI && i < kb) ? ((i << 16) | k) : -1;
+    }
+    for (int idx = t; idx < NB * NB; idx += DIAG_THREADS) {
+        const int i = idx / NB, j = idx % NB;
         A[i][j] = (i < kb && j <= i) ? F[(k0 + i) * cols + (k0 + j)] : 0.f;
     }
     __syncthreads();
     for (int j = 0; j < kb; ++j) {
-        if (t == 0) {
-            float d = A[j][j];
-            if (!(d > 0.f)) {  // also catches NaN
-                atomicMin(&st->bad_pivot, (unsigned long long)(k0 + j));
-            }
-            A[j][j] = sqrtf(d);
-        }
-        __syncthreads();
-        const float l = A[j][j];
-        for (int i = j + 1 + t; i < kb; i += blockDim.x) A[i][j] = A[i][j] / l;
-        __syncthreads();
-        const int m = kb - j - 1;  // trailing size
-        for (int idx = t; idx < m * m; idx += blockDim.x) {
-            int i = j + 1 + idx / m, k = j + 1 + idx % m;
-            if (k <= i) A[i][k] = fmaf(-A[i][j], A[k][j], A[i][k]);
-        }
-        __syncthreads();
-    }
-    // Inverse of the lower factor, one column per thread (forward substitution).
-    if (t < kb) {
-        const int c = t;
-        for (int i = 0; i < c; ++i) Y[i][c] = 0.f;
-        Y[c][c] = 1.f / A[c][c];
-        for (int i = c + 1; i < kb; ++i) {
-            float acc = 0.f;
-            for (int k = c; k < i; ++k) acc = fmaf(A[i][k], Y[k][c], acc);
-            Y[i][c] = -acc / A[i][i];
-        }
-    }
-    __syncthreads();
-    for (int idx = t; idx < kb * kb; idx += blockDim.x) {
-        int i = idx / kb, j = idx % kb;
-        if (j <= i) F[(k0 + i) * cols + (k0 + j)] = A[i][j];
-        Linv[i * NB + j] = (j <= i) ? Y[i][j] : 0.f;
-    }
-}
-
-// Panel solve: rows r >= k0 + kb of columns [k0, k0 + kb): P <- P L^-T.
-__global__ void __launch_bounds__(256) trsm_panel_kernel(float *__restrict__ F, int64_t cols, int64_t k0,
-                                                         int kb, const float *__restrict__ Linv) {
-    __shared__ float Li[NB][NB + 1];
-    __shared__ float P[NB][NB + 1];
-    const int t = threadIdx.x;
-    const int64_t r0 = k0 + kb + (int64_t)blockIdx.x * NB;
-    for (int idx = t; idx < NB * NB; idx += blockDim.x) {
-        int i = idx / NB, j = idx % NB;
-        Li[i][j] = (i < kb && j < kb) ? Linv[i * NB + j] : 0.f;
-        int64_t r = r0 + i;
-        P[i][j] = (r < cols && j < kb) ? F[r * cols + k0 + j] : 0.f;
-    }
-    __syncthreads();
-    // X[r][c] = sum_{k <= c} P[r][k] * Linv[c][k]; thread -> row t/4, 16 columns.
-    const int r = t / 4, cb = (t % 4) * 16;
-    float out[16];
+        const float d = A[j][j];
+        if (t == 0 && !(d > 0.f)) atomicMin(&st->bad_pivot, (unsigned long long)(k0 + j));
+        const float rd = 1.f / d;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) out[c] = 0.f;
+        for (int q = 0; q < DIAG_OWN; ++q) {
+            if (own[q] < 0) continue;
+            const int i = own[q] >> 16, k = own[q] & 0xffff;
+            if (k > j) A[i][k] = fmaf(-A[i][j] * rd, A[k][j], A[i][k]);
+        }
+        __syncthreads();
+    }
+    // Scale to the Cholesky factor (L_ij = a_ij / sqrt(a_jj)); then Y starts as I.
+#pragma unroll
+    for (int q = 0; q < DIAG_OWN; ++q) {
+        if (own[q] < 0) continue;
+        const int i = own[q] >> 16, k = own[q] & 0xffff;
+        const float l = sqrtf(A[k][k]);
+        Y[i][k] = (i == k) ? l : A[i][k] / l;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < DIAG_OWN; ++q) {
+        if (own[q] < 0) continue;
+        const int i = own[q] >> 16, k = own[q] & 0xffff;
+        A[i][k] = Y[i][k];
+        Y[i][k] = (i == k) ? 1.f : 0.f;
+    }
+    __syncthreads();
     for (int k = 0; k < kb; ++k) {
-        const float pk = P[r][k];
+        const float rl = 1.f / A[k][k];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) out[c] = fmaf(pk, Li[cb + c][k], out[c]);
+        for (int q = 0; q < DIAG_OWN; ++q) {
+            if (own[q] < 0) continue;
+            const int i = own[q] >> 16, c = own[q] & 0xffff;
+            if (i > k && c <= k) Y[i][c] = fmaf(-A[i][k] * rl, Y[k][c], Y[i][c]);
+        }
+        __syncthreads();
     }
-    const int64_t gr = r0 + r;
-    if (gr < cols) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-            if (cb + c < kb) F[gr * cols + k0 + cb + c] = out[c];
+    for (int q = 0; q < DIAG_OWN; ++q) {
+        if (own[q] < 0) continue;
+        const int i = own[q] >> 16, c = own[q] & 0xffff;
+        Y[i][c] = Y[i][c] / A[i][i];
+    }
+    __syncthreads();
+    for (int idx = t; idx < NB * NB; idx += DIAG_THREADS) {
+        const int i = idx / NB, j = idx % NB;
+        if (i < kb && j <= i) F[(k0 + i) * cols + (k0 + j)] = A[i][j];
+        Linv[idx] = (i < kb && j <= i) ? Y[i][j] : 0.f;
     }
 }
 
@@ -176,16 +179,24 @@ cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, u
 }
 
 cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *Linv, cudaStream_t s) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(potrf_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DIAG_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
     for (int64_t k0 = 0; k0 < cols; k0 += NB) {
         const int kb = (int)((cols - k0) < NB ? (cols - k0) : NB);
-        potrf_diag_kernel<<<1, 256, 0, s>>>(F, cols, k0, kb, Linv, st);
+        potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, s>>>(F, cols, k0, kb, Linv, st);
         const int64_t k1 = k0 + kb;
         if (k1 < cols) {
             const int64_t rest = cols - k1;
-            trsm_panel_kernel<<<(unsigned)((rest + NB - 1) / NB), 256, 0, s>>>(F, cols, k0, kb, Linv);
-            cudaError_t e = sgemm<float>(rest, rest, kb, -1.f, F + k1 * cols + k0, cols, false,
-                                         F + k1 * cols + k0, cols, true, 1.f, F + k1 * cols + k1, cols,
-                                         /*tri=*/1, s);
+            float *P = F + k1 * cols + k0;  // rest x kb panel below the diagonal block
+            // P <- P L^-T in place: each 128-row tile reads its rows completely before writing them.
+            cudaError_t e = sgemm<float>(rest, kb, kb, 1.f, P, cols, false, Linv, NB, true, 0.f, P, cols, 0, s);
+            if (e != cudaSuccess) return e;
+            e = sgemm<float>(rest, rest, kb, -1.f, P, cols, false, P, cols, true, 1.f, F + k1 * cols + k1, cols,
+                             /*tri=*/1, s);
             if (e != cudaSuccess) return e;
         }
     }

@@ -2,7 +2,9 @@
 // update of the blocked Cholesky and the deferred trailing update of the GPTQ
 // sweep.  (A tensor-float32 product would flip too many codes: see the sweep's
 // precision notes.)  128 x 128 output tile per CTA, 256 threads, 8 x 8 outputs
-// per thread, BK = 16, register-staged double buffering.
+// per thread, BK = 16, register-staged double buffering.  C may alias A when
+// N <= 128 (one column tile): every CTA reads all of its A rows before it
+// writes the same rows of C.
 #include "common.cuh"
 
 namespace gq {
@@ -54,9 +56,9 @@ __device__ __forceinline__ void store_tile(float (*S)[BM + 4], const float (&reg
 
 template <typename TA, bool AT, bool BT>
 __global__ void __launch_bounds__(NT) sgemm_kernel(int64_t M, int64_t N, int64_t K, float alpha,
-                                                   const TA *__restrict__ A, int64_t lda,
+                                                   const TA *A, int64_t lda,
                                                    const TA *__restrict__ B, int64_t ldb, float beta,
-                                                   float *__restrict__ C, int64_t ldc, int tri) {
+                                                   float *C, int64_t ldc, int tri) {
     const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
     if (tri == 1 && n0 > m0 + BM - 1) return;  // tile entirely above the diagonal
     if (tri == 2 && m0 > n0 + BN - 1) return;  // tile entirely below the diagonal

@@ -1,39 +1,45 @@
 // The GPTQ column sweep ([GPTQ-wiki] "Enfoque Técnico"; grid per [LowBit] section 1).
 //
-// Work split.  Columns are processed in blocks of `bw` <= 128 columns.  The
-// buffer D (rows x cols float32, in the workspace) holds, for a block not yet
-// swept, T = ΔW[:, <s] F[<s, blk] accumulated by the deferred trailing GEMMs
-// (F = the upper factor of H_d = F F^T, ΔW = W - Ŵ); once a block is swept its
-// columns of D hold ΔW.  Because U = F^-1 is upper triangular, the weights of
-// the block as updated by every earlier column are
-//     W_blk + T_blk Uinv_blk,   Uinv_blk = F[blk, blk]^-1 = U[blk, blk],
-// and inside the block the ordinary per-column update runs with Uinv_blk.
+// Work split.  Columns are processed in blocks of `bw` <= 128 columns.  With F
+// the upper factor of H_d = F F^T and U = F^-1 (upper triangular), the weights
+// of block b as updated by every earlier column are
+//     W_blk + ΔW[:, <s] F[<s, blk] Uinv_b,   Uinv_b = F[blk, blk]^-1 = U[blk, blk],
+// with ΔW = W - Ŵ.  V = F blockdiag(Uinv_b) (rows above each diagonal block) is
+// formed once, so the buffer D (rows x cols float32, in the workspace) holds,
+// for a block not yet swept, sum over earlier blocks of ΔW_prev V_prev,blk,
+// accumulated by the deferred trailing GEMMs; once a block is swept its
+// columns of D hold ΔW.  Inside the block the ordinary per-column update runs
+// with Uinv_b.
 //
-// Kernel layout.  One CTA = 32 output rows x one block, 8 warps x 4 rows.  Lane
-// l of a warp owns block columns 4l..4l+3 of its 4 rows, in registers.  Per
-// column j: the owning lane quantizes (IEEE division, round-half-even), the
-// scaled error e_j = (w_j - ŵ_j) / U_jj is broadcast by a warp shuffle, and
-// every lane updates its columns with row j of Uinv_blk (shared memory,
-// broadcast to all warps).  Group min/max are warp-shuffle butterflies.  The
-// epilogue writes ΔW back to D, the optional codes / Ŵ / row errors, the
-// scales, and packs codes and zero points into 32-bit words (coalesced
-// word-rows of 32 output rows).
-#include <cfloat>
-
+// Kernel layout.  One CTA = 32 output rows x one block, 16 warps x 2 rows; 16
+// lanes per row, each owning 8 consecutive block columns in registers.  Per
+// column j the owning lane of each row quantizes (round-half-even; the code
+// decision equals the one from IEEE division w / s, see rint_div), the scaled
+// error e_j = (w_j - ŵ_j) F_jj (= (w_j - ŵ_j) / U_jj) is broadcast within the
+// row's 16 lanes by a shuffle, and every lane updates its columns with row j of
+// Uinv_b (shared memory, broadcast to all warps).  Group min/max are shuffle
+// butterflies.  The epilogue writes ΔW back to D, the optional codes / Ŵ / row
+// errors, the scales, and packs codes and zero points into 32-bit words
+// (coalesced word-rows of 32 output rows).
 #include "common.cuh"
 
 namespace gq {
 namespace {
 
-constexpr int ROWS = 32;         // rows per CTA
-constexpr int RPW = 4;           // rows per warp
-constexpr int MAXB = 128;        // max block width
-constexpr int MAXG = MAXB / 32;  // max groups per block (group >= 32)
+constexpr int ROWS = 32;                   // rows per CTA
+constexpr int LPR = 16;                    // lanes per row
+constexpr int CPL = 8;                     // block columns per lane
+constexpr int RPW = 32 / LPR;              // rows per warp (2)
+constexpr int NTHREADS = ROWS / RPW * 32;  // 512
+constexpr int MAXB = LPR * CPL;            // max block width (128)
+constexpr int MAXG = MAXB / 32;            // max groups per block (group >= 32)
 
 struct SweepSmem {
-    float U[MAXB][MAXB];                 // Uinv_blk, upper triangle (lower part zero)
-    uint8_t codes[ROWS][MAXB + 4];       // staging for the qweight packing
-    uint8_t zeros[MAXG][ROWS];           // staging for the qzeros packing
+    float U[MAXB][MAXB];            // Uinv_b, upper triangle (lower part zero)
+    float fdiag[MAXB];              // F_jj = 1 / U_jj
+    uint8_t codes[ROWS][MAXB + 8];  // staging for the qweight packing (8-byte aligned rows)
+    uint8_t zeros[MAXG][ROWS];      // staging for the qzeros packing
+    float scales[MAXG][ROWS];       // staging for coalesced scale stores
 };
 
 // Word w of the little-endian bitstream of BITS-bit values v[0..]: bits [32w, 32w + 32).
@@ -53,202 +59,255 @@ __device__ __forceinline__ uint32_t pack_word(const uint8_t *v, int w, int n) {
 }
 
 template <typename TW>
-__device__ __forceinline__ void load4(const TW *p, float (&o)[4]);
+__device__ __forceinline__ void load8(const TW *p, float (&o)[8]);
 template <>
-__device__ __forceinline__ void load4<float>(const float *p, float (&o)[4]) {
-    float4 v = *reinterpret_cast<const float4 *>(p);
-    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+__device__ __forceinline__ void load8<float>(const float *p, float (&o)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 template <>
-__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16 *p, float (&o)[4]) {
-    uint2 v = *reinterpret_cast<const uint2 *>(p);
-    o[0] = __uint_as_float(v.x << 16);
-    o[1] = __uint_as_float(v.x & 0xffff0000u);
-    o[2] = __uint_as_float(v.y << 16);
-    o[3] = __uint_as_float(v.y & 0xffff0000u);
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, float (&o)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(u[i] << 16);
+        o[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+
+// rint(w / s) with w / s rounded as IEEE division does, without dividing in the
+// common case.  r = w * RN(1/s) differs from the exact quotient t by at most
+// 2^-23 |t| and the IEEE quotient differs from t by at most 2^-24 |t|, so both
+// lie on the same side of every half-integer unless r is within 2^-22 |t| of
+// one; only then (threshold 2^-20 (|r| + 1), and for non-finite r) is the
+// exact division taken.
+__device__ __forceinline__ float rint_div(float w, float s, float inv_s) {
+    const float r = w * inv_s;
+    const float k = rintf(r);
+    if (fabsf(fabsf(r - k) - 0.5f) > 9.5367431640625e-07f * (fabsf(r) + 1.f)) return k;
+    return rintf(__fdiv_rn(w, s));
 }
 
 template <int BITS, typename TW>
-__global__ void __launch_bounds__(256) sweep_kernel(const TW *__restrict__ W, int64_t rows, int64_t cols,
-                                                    int64_t c0, int bw, const float *__restrict__ Uinv,
-                                                    const uint8_t *__restrict__ dead, int group,
-                                                    float *__restrict__ D, int32_t *__restrict__ qweight,
-                                                    float *__restrict__ scales, int32_t *__restrict__ qzeros,
-                                                    uint8_t *__restrict__ codes, float *__restrict__ W_hat,
-                                                    float *__restrict__ row_err) {
+__global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ W, int64_t rows, int64_t cols,
+                                                         int64_t c0, int bw, const float *__restrict__ Uinv,
+                                                         const float *__restrict__ F, const uint8_t *__restrict__ dead,
+                                                         int group, float *__restrict__ D,
+                                                         int32_t *__restrict__ qweight, float *__restrict__ scales,
+                                                         int32_t *__restrict__ qzeros, uint8_t *__restrict__ codes,
+                                                         float *__restrict__ W_hat, float *__restrict__ row_err) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SweepSmem &sm = *reinterpret_cast<SweepSmem *>(smem_raw);
     constexpr float maxq = (float)((1 << BITS) - 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane / LPR, l16 = lane % LPR;  // row within the warp, lane within the row
+    const int rl = warp * RPW + sub;               // row within the CTA
     const int64_t row0 = (int64_t)blockIdx.x * ROWS;
-    const int64_t rbase = row0 + warp * RPW;
-    const int cl = lane * 4;               // first block column owned by this lane
+    const int64_t row = row0 + rl;
+    const int cl = l16 * CPL;                      // first block column of this lane
     const bool lane_on = cl < bw;
+    const unsigned src_base = (unsigned)(sub * LPR);
 
-    // Uinv_blk -> shared memory (bw x bw, row stride MAXB).
-    for (int idx = threadIdx.x; idx < MAXB * MAXB / 4; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < MAXB * MAXB / 4; idx += NTHREADS) {
         const int i = idx / (MAXB / 4), j4 = (idx % (MAXB / 4)) * 4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < bw && j4 < bw) v = *reinterpret_cast<const float4 *>(Uinv + (int64_t)i * bw + j4);
         *reinterpret_cast<float4 *>(&sm.U[i][j4]) = v;
     }
+    for (int i = threadIdx.x; i < MAXB; i += NTHREADS) sm.fdiag[i] = (i < bw) ? F[(c0 + i) * cols + c0 + i] : 1.f;
 
-    // Weights of the block and the accumulated T = ΔW_{<s} F_{<s, blk}.
-    float w[RPW][4], t[RPW][4];
-    uint8_t dmask[4] = {0, 0, 0, 0};
-    if (dead && lane_on) {
+    // Weights of the block as updated by every earlier block: W + D.  Dead inputs are zero.
+    float w[CPL];
+    bool dmask[CPL];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dmask[c] = dead[c0 + cl + c];
+    for (int c = 0; c < CPL; ++c) {
+        w[c] = 0.f;
+        dmask[c] = false;
     }
+    if (lane_on && row < rows) {
+        float t[CPL];
+        load8<TW>(W + row * cols + c0 + cl, w);
+        load8<float>(D + row * cols + c0 + cl, t);
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        const int64_t row = rbase + r;
-        if (lane_on && row < rows) {
-            load4<TW>(W + row * cols + c0 + cl, w[r]);
-            float4 tv = *reinterpret_cast<const float4 *>(D + row * cols + c0 + cl);
-            t[r][0] = tv.x; t[r][1] = tv.y; t[r][2] = tv.z; t[r][3] = tv.w;
-        } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) w[r][c] = t[r][c] = 0.f;
+        for (int c = 0; c < CPL; ++c) {
+            if (dead) dmask[c] = dead[c0 + cl + c] != 0;
+            w[c] = (dmask[c] ? 0.f : w[c]) + t[c];
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if (dmask[c]) w[r][c] = 0.f;
     }
     __syncthreads();
 
-    // w += T Uinv_blk (row vector times upper-triangular block).
-    for (int o = 0; o < bw / 4; ++o) {
+    float s = 1.f, inv_s = 1.f, z = 0.f, e2 = 0.f;
+    float wq[CPL];
+    uint32_t qlo = 0u, qhi = 0u;
 #pragma unroll
-        for (int ci = 0; ci < 4; ++ci) {
-            const int i = o * 4 + ci;
-            const float4 u = *reinterpret_cast<const float4 *>(&sm.U[i][cl]);
-#pragma unroll
-            for (int r = 0; r < RPW; ++r) {
-                const float ti = __shfl_sync(0xffffffffu, t[r][ci], o);
-                w[r][0] = fmaf(ti, u.x, w[r][0]);
-                w[r][1] = fmaf(ti, u.y, w[r][1]);
-                w[r][2] = fmaf(ti, u.z, w[r][2]);
-                w[r][3] = fmaf(ti, u.w, w[r][3]);
-            }
-        }
-    }
+    for (int c = 0; c < CPL; ++c) wq[c] = 0.f;
 
-    float s[RPW], z[RPW], e2[RPW], wq[RPW][4];
-    uint32_t q4[RPW];
+    for (int o = 0; o < bw / CPL; ++o) {
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        s[r] = 1.f; z[r] = 0.f; e2[r] = 0.f; q4[r] = 0u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) wq[r][c] = 0.f;
-    }
-
-    for (int o = 0; o < bw / 4; ++o) {
-#pragma unroll
-        for (int ci = 0; ci < 4; ++ci) {
-            const int j = o * 4 + ci;
+        for (int ci = 0; ci < CPL; ++ci) {
+            const int j = o * CPL + ci;
             if (ci == 0 && (j % group) == 0) {
                 // Group parameters from the current weights of columns [j, j + group).
+                float lo = 3.402823466e38f, hi = -3.402823466e38f;
 #pragma unroll
-                for (int r = 0; r < RPW; ++r) {
-                    float lo = FLT_MAX, hi = -FLT_MAX;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int col = cl + c;
-                        if (col >= j && col < j + group && col < bw) {
-                            lo = fminf(lo, w[r][c]);
-                            hi = fmaxf(hi, w[r][c]);
-                        }
+                for (int c = 0; c < CPL; ++c) {
+                    const int col = cl + c;
+                    if (col >= j && col < j + group && col < bw) {
+                        lo = fminf(lo, w[c]);
+                        hi = fmaxf(hi, w[c]);
                     }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-                        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
-                    }
-                    float xmin = fminf(lo, 0.f), xmax = fmaxf(hi, 0.f);
-                    if (xmin == 0.f && xmax == 0.f) {
-                        xmin = -1.f;
-                        xmax = 1.f;
-                    }
-                    s[r] = __fdiv_rn(xmax - xmin, maxq);
-                    z[r] = rintf(__fdiv_rn(-xmin, s[r]));
                 }
-                const int g = j / group;
-                if (lane == 0) {
-                    const int64_t gi = (c0 + j) / group;
-                    if (rbase < rows)
-                        *reinterpret_cast<float4 *>(scales + gi * rows + rbase) = make_float4(s[0], s[1], s[2], s[3]);
 #pragma unroll
-                    for (int r = 0; r < RPW; ++r) sm.zeros[g][warp * RPW + r] = (uint8_t)z[r];
+                for (int off = LPR / 2; off > 0; off >>= 1) {
+                    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+                    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+                }
+                float xmin = fminf(lo, 0.f), xmax = fmaxf(hi, 0.f);
+                if (xmin == 0.f && xmax == 0.f) {
+                    xmin = -1.f;
+                    xmax = 1.f;
+                }
+                s = __fdiv_rn(xmax - xmin, maxq);
+                inv_s = __fdiv_rn(1.f, s);
+                z = rintf(__fdiv_rn(-xmin, s));
+                if (l16 == 0) {
+                    sm.zeros[j / group][rl] = (uint8_t)z;
+                    sm.scales[j / group][rl] = s;
                 }
             }
-            const float udiag = sm.U[j][j];
-            float e[RPW] = {0.f, 0.f, 0.f, 0.f};
-            if (lane == o) {
-#pragma unroll
-                for (int r = 0; r < RPW; ++r) {
-                    const float wv = w[r][ci];
-                    const float q = fminf(fmaxf(rintf(__fdiv_rn(wv, s[r])) + z[r], 0.f), maxq);
-                    const float dq = s[r] * (q - z[r]);
-                    wq[r][ci] = dq;
-                    q4[r] |= ((uint32_t)q) << (8 * ci);
-                    e[r] = __fdiv_rn(wv - dq, udiag);
-                    e2[r] = fmaf(e[r], e[r], e2[r]);
-                }
+            float e = 0.f;
+            if (l16 == o) {
+                const float wv = w[ci];
+                const float q = fminf(fmaxf(rint_div(wv, s, inv_s) + z, 0.f), maxq);
+                const float dq = s * (q - z);
+                wq[ci] = dq;
+                if (ci < 4)
+                    qlo |= ((uint32_t)q) << (8 * ci);
+                else
+                    qhi |= ((uint32_t)q) << (8 * (ci - 4));
+                e = (wv - dq) * sm.fdiag[j];
+                e2 = fmaf(e, e, e2);
             }
-            const float4 u = *reinterpret_cast<const float4 *>(&sm.U[j][cl]);
-#pragma unroll
-            for (int r = 0; r < RPW; ++r) {
-                const float eb = __shfl_sync(0xffffffffu, e[r], o);
-                // Uinv is upper triangular: columns < j get zero updates; column j
-                // itself is already quantized and its working value is unused.
-                w[r][0] = fmaf(-eb, u.x, w[r][0]);
-                w[r][1] = fmaf(-eb, u.y, w[r][1]);
-                w[r][2] = fmaf(-eb, u.z, w[r][2]);
-                w[r][3] = fmaf(-eb, u.w, w[r][3]);
-            }
+            const float eb = __shfl_sync(0xffffffffu, e, src_base + (unsigned)o);
+            const float4 u0 = *reinterpret_cast<const float4 *>(&sm.U[j][cl]);
+            const float4 u1 = *reinterpret_cast<const float4 *>(&sm.U[j][cl + 4]);
+            // Uinv_b is upper triangular: columns < j get zero updates; column j
+            // itself is already quantized and its working value is unused.
+            w[0] = fmaf(-eb, u0.x, w[0]);
+            w[1] = fmaf(-eb, u0.y, w[1]);
+            w[2] = fmaf(-eb, u0.z, w[2]);
+            w[3] = fmaf(-eb, u0.w, w[3]);
+            w[4] = fmaf(-eb, u1.x, w[4]);
+            w[5] = fmaf(-eb, u1.y, w[5]);
+            w[6] = fmaf(-eb, u1.z, w[6]);
+            w[7] = fmaf(-eb, u1.w, w[7]);
         }
     }
 
-    // Epilogue: ΔW -> D, optional outputs, staging for packing.
+    // Epilogue.
+    float err = e2;
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        const int64_t row = rbase + r;
-        float err = e2[r];
+    for (int off = LPR / 2; off > 0; off >>= 1) err += __shfl_xor_sync(0xffffffffu, err, off);
+    if (row < rows) {
+        if (l16 == 0 && row_err) row_err[row] += err;
+        if (lane_on) {
+            float w0[CPL], dw[CPL];
+            load8<TW>(W + row * cols + c0 + cl, w0);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) err += __shfl_xor_sync(0xffffffffu, err, off);
-        if (row >= rows) continue;
-        if (lane == 0 && row_err) row_err[row] += err;
-        if (!lane_on) continue;
-        float w0[4];
-        load4<TW>(W + row * cols + c0 + cl, w0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if (dmask[c]) w0[c] = 0.f;
-        *reinterpret_cast<float4 *>(D + row * cols + c0 + cl) =
-            make_float4(w0[0] - wq[r][0], w0[1] - wq[r][1], w0[2] - wq[r][2], w0[3] - wq[r][3]);
-        if (W_hat)
-            *reinterpret_cast<float4 *>(W_hat + row * cols + c0 + cl) = make_float4(wq[r][0], wq[r][1], wq[r][2], wq[r][3]);
-        if (codes) *reinterpret_cast<uint32_t *>(codes + row * cols + c0 + cl) = q4[r];
-        *reinterpret_cast<uint32_t *>(&sm.codes[warp * RPW + r][cl]) = q4[r];
+            for (int c = 0; c < CPL; ++c) dw[c] = (dmask[c] ? 0.f : w0[c]) - wq[c];
+            float *dp = D + row * cols + c0 + cl;
+            *reinterpret_cast<float4 *>(dp) = make_float4(dw[0], dw[1], dw[2], dw[3]);
+            *reinterpret_cast<float4 *>(dp + 4) = make_float4(dw[4], dw[5], dw[6], dw[7]);
+            if (W_hat) {
+                float *hp = W_hat + row * cols + c0 + cl;
+                *reinterpret_cast<float4 *>(hp) = make_float4(wq[0], wq[1], wq[2], wq[3]);
+                *reinterpret_cast<float4 *>(hp + 4) = make_float4(wq[4], wq[5], wq[6], wq[7]);
+            }
+            if (codes) *reinterpret_cast<uint2 *>(codes + row * cols + c0 + cl) = make_uint2(qlo, qhi);
+            *reinterpret_cast<uint2 *>(&sm.codes[rl][cl]) = make_uint2(qlo, qhi);
+        }
     }
     __syncthreads();
 
+    // scales [cols/group][rows]: 32 consecutive rows per group.
+    const int ng = bw / group;
+    for (int idx = threadIdx.x; idx < ng * ROWS; idx += NTHREADS) {
+        const int g = idx / ROWS, rr = idx % ROWS;
+        if (row0 + rr < rows) scales[((c0 / group) + g) * rows + row0 + rr] = sm.scales[g][rr];
+    }
     // qweight [cols*BITS/32][rows]: words of this block, one word-row of 32 rows at a time.
     const int nw = bw * BITS / 32;
     const int64_t w0i = c0 * BITS / 32;
-    for (int idx = threadIdx.x; idx < nw * ROWS; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < nw * ROWS; idx += NTHREADS) {
         const int wi = idx / ROWS, rr = idx % ROWS;
-        if (row0 + rr < rows)
-            qweight[(w0i + wi) * rows + row0 + rr] = (int32_t)pack_word<BITS>(sm.codes[rr], wi, bw);
+        if (row0 + rr < rows) qweight[(w0i + wi) * rows + row0 + rr] = (int32_t)pack_word<BITS>(sm.codes[rr], wi, bw);
     }
     // qzeros [cols/group][rows*BITS/32]: BITS words per group for these 32 rows.
-    const int ng = bw / group;
     const int64_t zw = rows * BITS / 32;
-    for (int idx = threadIdx.x; idx < ng * BITS; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < ng * BITS; idx += NTHREADS) {
         const int g = idx / BITS, wi = idx % BITS;
         qzeros[((c0 / group) + g) * zw + row0 * BITS / 32 + wi] = (int32_t)pack_word<BITS>(sm.zeros[g], wi, ROWS);
+    }
+}
+
+// V[:, blk] = F[:, blk] Uinv_b for the rows above each diagonal block: the
+// deferred update of block b from the earlier columns is then sum ΔW_prev V_prev,b.
+// One CTA per (128-row tile, block column), 256 threads, 8 x 8 outputs each.
+// A CTA reads its whole input tile before writing the same tile, and tiles are
+// disjoint, so V may alias F.
+__global__ void __launch_bounds__(256) premultiply_kernel(const float *F, int64_t cols, int block,
+                                                          const float *__restrict__ Uinv, float *V) {
+    __shared__ __align__(16) float As[16][128 + 4];
+    __shared__ __align__(16) float Bs[16][128 + 4];
+    const int b = blockIdx.y;
+    const int64_t s0 = (int64_t)b * block;
+    const int bw = (int)((cols - s0) < block ? (cols - s0) : block);
+    const int64_t m0 = (int64_t)blockIdx.x * 128;
+    if (m0 >= s0) return;  // only rows above the diagonal block
+    const float *Ub = Uinv + s0 * block;  // bw x bw, row stride bw
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int k0 = 0; k0 < bw; k0 += 16) {
+        for (int idx = threadIdx.x; idx < 16 * 128; idx += 256) {
+            const int r = idx / 16, k = idx % 16;  // A: F[m0 + r][s0 + k0 + k]
+            const int64_t gr = m0 + r;
+            As[k][r] = (gr < s0 && k0 + k < bw) ? F[gr * cols + s0 + k0 + k] : 0.f;
+            const int kk = idx / 128, n = idx % 128;  // B: Uinv_b[k0 + kk][n]
+            Bs[kk][n] = (k0 + kk < bw && n < bw) ? Ub[(int64_t)(k0 + kk) * bw + n] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            float a[8], bb[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[i] = As[k][ty * 4 + i];
+                a[4 + i] = As[k][64 + ty * 4 + i];
+                bb[i] = Bs[k][tx * 4 + i];
+                bb[4 + i] = Bs[k][64 + tx * 4 + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+        if (m >= s0) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int n = (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+            if (n < bw) V[m * cols + s0 + n] = acc[i][j];
+        }
     }
 }
 
@@ -286,7 +345,7 @@ __global__ void __launch_bounds__(128) block_inverse_kernel(const float *__restr
 
 template <int BITS, typename TW>
 cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, int bw, const float *Uinv,
-                         const uint8_t *dead, int group, float *D, int32_t *qweight, float *scales,
+                         const float *F, const uint8_t *dead, int group, float *D, int32_t *qweight, float *scales,
                          int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s) {
     const size_t smem = sizeof(SweepSmem);
     static bool attr_set = false;  // per template instance
@@ -295,8 +354,8 @@ cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, in
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    sweep_kernel<BITS, TW><<<(unsigned)((rows + ROWS - 1) / ROWS), 256, smem, s>>>(
-        W, rows, cols, c0, bw, Uinv, dead, group, D, qweight, scales, qzeros, codes, W_hat, row_err);
+    sweep_kernel<BITS, TW><<<(unsigned)((rows + ROWS - 1) / ROWS), NTHREADS, smem, s>>>(
+        W, rows, cols, c0, bw, Uinv, F, dead, group, D, qweight, scales, qzeros, codes, W_hat, row_err);
     return cudaGetLastError();
 }
 
@@ -315,17 +374,25 @@ cudaError_t block_inverses(const float *F, int64_t cols, int block, float *Uinv,
     return cudaGetLastError();
 }
 
+cudaError_t premultiply(const float *F, int64_t cols, int block, const float *Uinv, float *V, cudaStream_t s) {
+    const int64_t nblk = (cols + block - 1) / block;
+    if (nblk < 2) return cudaSuccess;
+    dim3 grid((unsigned)(((nblk - 1) * block + 127) / 128), (unsigned)nblk);
+    premultiply_kernel<<<grid, 256, 0, s>>>(F, cols, block, Uinv, V);
+    return cudaGetLastError();
+}
+
 cudaError_t sweep_block_launch(const void *W, bool w_bf16, int64_t rows, int64_t cols, int64_t c0, int bw,
-                               const float *Uinv_blk, const uint8_t *dead, int bits, int group, float *D,
-                               int32_t *qweight, float *scales, int32_t *qzeros, uint8_t *codes,
+                               const float *Uinv_blk, const float *F, const uint8_t *dead, int bits, int group,
+                               float *D, int32_t *qweight, float *scales, int32_t *qzeros, uint8_t *codes,
                                float *W_hat, float *row_err, cudaStream_t s) {
-#define GQ_SWEEP_CASE(B)                                                                                       \
-    if (bits == B) {                                                                                           \
-        if (w_bf16)                                                                                            \
-            return launch_sweep<B, __nv_bfloat16>((const __nv_bfloat16 *)W, rows, cols, c0, bw, Uinv_blk, dead, \
-                                                  group, D, qweight, scales, qzeros, codes, W_hat, row_err, s); \
-        return launch_sweep<B, float>((const float *)W, rows, cols, c0, bw, Uinv_blk, dead, group, D, qweight,   \
-                                      scales, qzeros, codes, W_hat, row_err, s);                               \
+#define GQ_SWEEP_CASE(B)                                                                                         \
+    if (bits == B) {                                                                                             \
+        if (w_bf16)                                                                                              \
+            return launch_sweep<B, __nv_bfloat16>((const __nv_bfloat16 *)W, rows, cols, c0, bw, Uinv_blk, F, dead, \
+                                                  group, D, qweight, scales, qzeros, codes, W_hat, row_err, s);   \
+        return launch_sweep<B, float>((const float *)W, rows, cols, c0, bw, Uinv_blk, F, dead, group, D, qweight,  \
+                                      scales, qzeros, codes, W_hat, row_err, s);                                 \
     }
     GQ_SWEEP_CASE(2)
     GQ_SWEEP_CASE(3)
