@@ -152,6 +152,37 @@ gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t 
                               int64_t *info);
 
 /*
+ * gptq_quantize_layer without a caller-provided workspace, for callers that
+ * cannot allocate device memory: code inside a host application that owns all
+ * device memory through its own pool, a service that must not grow its device
+ * footprint after start-up, a real-time loop where a synchronizing
+ * cudaMalloc is not allowed.  The pages have no counterpart to this call; it
+ * exists only because of how some callers manage memory.
+ *
+ * Same arguments, rules, outputs and status codes as gptq_quantize_layer,
+ * without `ws` / `ws_bytes`.  The scratch is one fixed array of
+ * GQ_NOALLOC_SCRATCH_BYTES (16 MiB) of device memory inside the library,
+ * held by every GPU that loads the library until the process exits.  Nothing
+ * is allocated or freed: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ *   Size limit: gptq_quantize_layer_workspace_size(rows, cols, block) must be
+ *   <= GQ_NOALLOC_SCRATCH_BYTES (e.g. rows = cols = 1024, block = 128 fits);
+ *   larger layers are rejected with GQ_EWORKSPACE before anything is enqueued.
+ *   All buffers must live on the current CUDA device, and `stream` must belong
+ *   to it.  The first call on a device looks up the scratch's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call shares the one array and it keeps the last call's contents; the
+ *   call clears what must start at zero itself.  Calls whose GPU work overlaps
+ *   (other streams, other host threads) race on the array: serialize them.
+ * Synchronizes `stream` once (after the factorization), like gptq_quantize_layer.
+ */
+#define GQ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+gq_status gptq_quantize_layer_noalloc(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *H,
+                                      int bits, int group, int block, float damp, int32_t *qweight, float *scales,
+                                      int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err,
+                                      gq_stream_t stream, int64_t *info);
+
+/*
  * Standalone packing of codes (rows x cols uint8, each < 2^bits) into
  * qweight [cols*bits/32][rows] int32, and its inverse.  Same layout as
  * gptq_sweep.  rows % 32 == 0 is not required; cols*bits % 32 == 0 is.

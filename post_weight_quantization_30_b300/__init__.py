@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     gptq_hessian_accumulate,
     gptq_pack,
     gptq_quantize_layer,
+    gptq_quantize_layer_noalloc,
     gptq_sweep,
     gptq_unpack,
     gq_check_device,

@@ -47,6 +47,8 @@ SIGNATURES = {
     "gptq_quantize_layer_workspace_size": (_sz, [_i64, _i64, _i]),
     "gptq_quantize_layer": (_i, [_p, _i, _i64, _i64, _p, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p, _sz, _p,
                                  ctypes.POINTER(_i64)]),
+    "gptq_quantize_layer_noalloc": (_i, [_p, _i, _i64, _i64, _p, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p,
+                                         ctypes.POINTER(_i64)]),
     "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
     "gptq_unpack": (_i, [_p, _i64, _i64, _i, _p, _p]),
 }
@@ -167,6 +169,36 @@ def gptq_quantize_layer(W: torch.Tensor, H: torch.Tensor, bits: int, group: int,
                                    _ptr(o.get("codes")), _ptr(o.get("W_hat")), _ptr(o.get("row_err")), _ptr(ws),
                                    ws.numel(), _stream(W.device), ctypes.byref(info)),
            "gptq_quantize_layer", info.value)
+    return o
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # GQ_NOALLOC_SCRATCH_BYTES in include/gq.h
+
+
+def gptq_quantize_layer_noalloc(W: torch.Tensor, H: torch.Tensor, bits: int, group: int, block: int = 128,
+                                damp: float = 0.01, out: dict | None = None, codes: bool = True, W_hat: bool = True,
+                                row_err: bool = True):
+    """gptq_quantize_layer with the library's fixed 16 MiB scratch instead of a workspace.
+
+    For callers that must not allocate device scratch.  Output buffers are
+    still the caller's: pass ``out`` (same keys as gptq_quantize_layer returns)
+    to allocate nothing at all.  Layers whose workspace exceeds the fixed
+    scratch are rejected.  Calls that overlap on the GPU race on the scratch.
+    """
+    _need_cuda(W, H)
+    rows, cols = W.shape
+    need = lib.gptq_quantize_layer_workspace_size(rows, cols, block)
+    if need > NOALLOC_SCRATCH_BYTES:
+        raise ValueError(f"layer {rows}x{cols} (block {block}) needs {need} bytes of scratch; the fixed scratch "
+                         f"holds {NOALLOC_SCRATCH_BYTES}: use gptq_quantize_layer with a workspace")
+    W = W.contiguous()
+    o = out if out is not None else _sweep_outputs(rows, cols, bits, group, W.device, codes, W_hat, row_err)
+    info = _i64(-1)
+    _check(lib.gptq_quantize_layer_noalloc(_ptr(W), _dtype_code(W), rows, cols, _ptr(H.contiguous()), bits, group,
+                                           block, float(damp), _ptr(o["qweight"]), _ptr(o["scales"]),
+                                           _ptr(o["qzeros"]), _ptr(o.get("codes")), _ptr(o.get("W_hat")),
+                                           _ptr(o.get("row_err")), _stream(W.device), ctypes.byref(info)),
+           "gptq_quantize_layer_noalloc", info.value)
     return o
 
 
