@@ -14,6 +14,7 @@ rank 0 prints the aggregate: layers processed by all ranks / max-over-ranks time
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -44,7 +45,7 @@ def _peaks():
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -57,7 +58,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
         except OSError:
@@ -76,19 +77,28 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    def mark(self, which: str):
+        """Record the wall-clock start or end of the timed region."""
+        setattr(self, which, datetime.datetime.now())
+
     def summary(self):
+        """Median SM clock and active throttle reasons over the samples taken inside the timed region."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0, t1 = getattr(self, "start", None), getattr(self, "stop", None)
         for ln in self.lines:
             p = [x.strip() for x in ln.split(",")]
-            if len(p) < 9:
+            if len(p) < 10:
                 continue
             try:
-                sm.append(float(p[1]))
-                mx.append(float(p[2]))
+                ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f")
+                if t0 is not None and t1 is not None and not (t0 <= ts <= t1):
+                    continue
+                sm.append(float(p[2]))
+                mx.append(float(p[3]))
             except ValueError:
                 continue
-            for name, v in zip(names, p[5:9]):
+            for name, v in zip(names, p[6:10]):
                 if v.lower() == "active":
                     reasons.add(name)
         if not sm:
@@ -147,19 +157,23 @@ def run_ours(args, rank: int, world: int):
 
     import torch.distributed as dist
 
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
     hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
+        time.sleep(0.3)  # let the sampler start before the timed region
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        clocks.mark("start")
         start.record(stream)
         for k in range(args.steps):
             step(hev[k])
         stop.record(stream)
         torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
+        if world > 1:
+            dist.barrier()
+        clocks.mark("stop")
+        time.sleep(0.15)
     ms_total = start.elapsed_time(stop)
     h_ms = [a.elapsed_time(b) for a, b in hev]
     if world > 1:
@@ -338,7 +352,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(LAYERS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -152,6 +152,37 @@ gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t 
                               int64_t *info);
 
 /*
+ * EoRA compensation of the quantization error ([EoRA-blog] "Bucear en el
+ * espacio propio en busca de un adaptador").
+ *
+ * The error ΔW = W - Ŵ is projected into the eigenspace of the input
+ * covariance, ΔW' = ΔW Q sqrt(Λ) with H = Q Λ Q^T, its SVD is truncated to
+ * rank r, ΔW' ≈ U_r Σ_r V_r^T, and the result is projected back: B = U_r Σ_r,
+ * A = V_r^T (Q sqrt(Λ))^-1, so that B A approximates ΔW and
+ * 1/2 tr((ΔW - B A) H (ΔW - B A)^T) = 1/2 sum_{i>r} σ_i^2 (the layer loss left
+ * after compensation) is minimal over all rank-r products.
+ * Signs: the largest-magnitude entry of each column of B is positive (the
+ * matching row of A carries the same sign).
+ *
+ *   dW     rows x cols float32, read only.
+ *   H      cols x cols float32 (both triangles), used as passed (no damping);
+ *          must be positive definite, else GQ_ENOTPD with *info = a column.
+ *   r      1 <= r <= min(64, rows, cols).
+ *   A      r x cols float32 output.   B  rows x r float32 output.
+ *   sigma  r float32 output, may be NULL: the r largest singular values of the
+ *          projected error ΔW', in descending order.
+ *   ws     >= eora_compensate_workspace_size(rows, cols, r) bytes.
+ * Computed in float32 with a block subspace iteration of width min(2r, cols)
+ * (40 iterations) and a Rayleigh-Ritz step.  When σ_r and σ_{r+1} are close,
+ * the rank-r subspace is not unique and B A may differ from another exact
+ * solution by directions of nearly equal σ; the compensated loss and σ do not.
+ * Synchronizes `stream` once (after the factorization of H).
+ */
+size_t eora_compensate_workspace_size(int64_t rows, int64_t cols, int r);
+gq_status eora_compensate(const float *dW, int64_t rows, int64_t cols, const float *H, int r, float *A, float *B,
+                          float *sigma, void *ws, size_t ws_bytes, gq_stream_t stream, int64_t *info);
+
+/*
  * gptq_quantize_layer without a caller-provided workspace, for callers that
  * cannot allocate device memory: code inside a host application that owns all
  * device memory through its own pool, a service that must not grow its device

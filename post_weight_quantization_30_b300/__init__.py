@@ -8,6 +8,7 @@ from ._lib import (  # noqa: F401
     GQError,
     LIB_PATH,
     SIGNATURES,
+    eora_compensate,
     gptq_factor,
     gptq_hessian_accumulate,
     gptq_pack,

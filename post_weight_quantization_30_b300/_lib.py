@@ -49,6 +49,8 @@ SIGNATURES = {
                                  ctypes.POINTER(_i64)]),
     "gptq_quantize_layer_noalloc": (_i, [_p, _i, _i64, _i64, _p, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p,
                                          ctypes.POINTER(_i64)]),
+    "eora_compensate_workspace_size": (_sz, [_i64, _i64, _i]),
+    "eora_compensate": (_i, [_p, _i64, _i64, _p, _i, _p, _p, _p, _p, _sz, _p, ctypes.POINTER(_i64)]),
     "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
     "gptq_unpack": (_i, [_p, _i64, _i64, _i, _p, _p]),
 }
@@ -199,6 +201,27 @@ def gptq_quantize_layer_noalloc(W: torch.Tensor, H: torch.Tensor, bits: int, gro
                                            _ptr(o["qzeros"]), _ptr(o.get("codes")), _ptr(o.get("W_hat")),
                                            _ptr(o.get("row_err")), _stream(W.device), ctypes.byref(info)),
            "gptq_quantize_layer_noalloc", info.value)
+    return o
+
+
+def eora_compensate(dW: torch.Tensor, H: torch.Tensor, r: int, workspace: torch.Tensor | None = None,
+                    out: dict | None = None):
+    """EoRA factors of the quantization error dW = W - Ŵ: returns dict(A, B, sigma)."""
+    _need_cuda(dW, H)
+    rows, cols = dW.shape
+    dW = dW.contiguous()
+    if dW.dtype != torch.float32 or H.dtype != torch.float32:
+        raise ValueError("dW and H must be float32")
+    o = out if out is not None else dict(
+        A=torch.empty((r, cols), dtype=torch.float32, device=dW.device),
+        B=torch.empty((rows, r), dtype=torch.float32, device=dW.device),
+        sigma=torch.empty(r, dtype=torch.float32, device=dW.device))
+    ws_bytes = lib.eora_compensate_workspace_size(rows, cols, r)
+    ws = workspace if workspace is not None else _workspace(ws_bytes, dW.device)
+    info = _i64(-1)
+    _check(lib.eora_compensate(_ptr(dW), rows, cols, _ptr(H.contiguous()), r, _ptr(o["A"]), _ptr(o["B"]),
+                               _ptr(o.get("sigma")), _ptr(ws), ws.numel(), _stream(dW.device), ctypes.byref(info)),
+           "eora_compensate", info.value)
     return o
 
 

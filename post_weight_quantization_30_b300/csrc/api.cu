@@ -206,6 +206,26 @@ gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t 
                       sweep_ws_bytes(rows, cols, block), stream);
 }
 
+size_t eora_compensate_workspace_size(int64_t rows, int64_t cols, int r) {
+    if (rows <= 0 || cols <= 0 || r <= 0) return 0;
+    return eora_workspace_bytes(rows, cols, r);
+}
+
+gq_status eora_compensate(const float *dW, int64_t rows, int64_t cols, const float *H, int r, float *A, float *B,
+                          float *sigma, void *ws, size_t ws_bytes, gq_stream_t stream, int64_t *info) {
+    if (!dW || !H || !A || !B || rows <= 0 || cols <= 0) return GQ_EINVAL;
+    if (r <= 0 || r > 64 || r > rows || r > cols) return GQ_EINVAL;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < eora_workspace_bytes(rows, cols, r)) return GQ_EWORKSPACE;
+    unsigned long long bad = ULLONG_MAX;
+    if (eora_run(dW, rows, cols, H, r, A, B, sigma, ws, cs(stream), &bad) != cudaSuccess) return GQ_ECUDA;
+    if (bad != ULLONG_MAX) {
+        if (info) *info = cols - 1 - (int64_t)bad;
+        return GQ_ENOTPD;
+    }
+    if (info) *info = -1;
+    return GQ_OK;
+}
+
 gq_status gptq_pack(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight, gq_stream_t stream) {
     if (bits != 2 && bits != 3 && bits != 4) return GQ_EUNSUPPORTED;
     if (!codes || !qweight || rows <= 0 || cols <= 0 || (cols * bits) % 32) return GQ_EINVAL;

@@ -56,6 +56,12 @@ cudaError_t sgemm(int64_t M, int64_t N, int64_t K, float alpha, const TA *A, int
                   const TA *B, int64_t ldb, bool b_t, float beta, float *C, int64_t ldc, int tri,
                   cudaStream_t s);
 
+// C (M x N, row-major, ldc = N) = A B in float32, the K range split into
+// `slices` parts computed by separate CTAs into `partials` (slices * M * N
+// floats) and summed in a fixed order (deterministic).
+cudaError_t sgemm_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, bool a_t, const float *B,
+                         int64_t ldb, bool b_t, float *C, float *partials, int slices, cudaStream_t s);
+
 // Hessian accumulation on the tensor cores (bf16 inputs, tcgen05 + TMA).
 cudaError_t hessian_bf16_tc(float *H, int64_t cols, const __nv_bfloat16 *X, int64_t n, int64_t ldx,
                             cudaStream_t s);
@@ -79,6 +85,14 @@ cudaError_t sweep_block_launch(const void *W, bool w_bf16, int64_t rows, int64_t
                                int bw, const float *Uinv_blk, const float *F, const uint8_t *dead, int bits, int group,
                                float *D, int32_t *qweight, float *scales, int32_t *qzeros,
                                uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s);
+
+// EoRA (eora.cu).  eora_run synchronizes `s` once, after the factorization of
+// H, and reports a non-positive pivot through *bad_pivot_host (ULLONG_MAX = none,
+// else the pivot index in reversed order); nothing after that is launched then.
+size_t eora_workspace_bytes(int64_t rows, int64_t cols, int r);
+int eora_subspace_width(int64_t rows, int64_t cols, int r);
+cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H, int r, float *A, float *B,
+                     float *sigma, void *ws, cudaStream_t s, unsigned long long *bad_pivot_host);
 
 cudaError_t pack_launch(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight,
                         cudaStream_t s);

@@ -62,90 +62,200 @@ __global__ void reverse_damp_kernel(const float *__restrict__ H, int64_t cols, f
 }
 
 // Cholesky of the kb x kb diagonal block at (k0, k0) (kb <= NB) in shared
-// memory, followed by the inverse of the factor (written to Linv, NB x NB
-// row-major, zero above the diagonal).  Each thread owns a fixed set of
-// lower-triangle elements.  Elimination step j subtracts a_ij a_kj / a_jj from
-// every a_ik with j < k <= i, using column j as left by the earlier steps
-// (unscaled), so a step needs one barrier; the factor is a_ij / sqrt(a_jj)
-// afterwards.  The inverse is built the same way (right-looking, one barrier
-// per step): R_ic -= (L_ik / L_kk) R_kc, then Y_ic = R_ic / L_ii.
-constexpr int DIAG_THREADS = 512;
-constexpr int TRI = NB * (NB + 1) / 2;
-constexpr int DIAG_OWN = (TRI + DIAG_THREADS - 1) / DIAG_THREADS;
-constexpr size_t DIAG_SMEM = 2 * NB * (NB + 1) * sizeof(float);
+// memory, and the inverse of the factor (written to Linv, NB x NB row-major,
+// zero above the diagonal).  Rows and columns from kb to NB are padded with
+// the identity, which leaves the leading kb x kb part unchanged.
+//
+// The block is processed in four sub-panels of 32 columns.  For each:
+//   1. warp 0 factors the 32 x 32 diagonal sub-block in registers (lane i
+//      holds row i; the pivot row is broadcast by shuffles, so no CTA-wide
+//      barrier is needed inside the 32 steps) and forms its inverse by
+//      forward substitution (lane c holds column c of the inverse);
+//   2. all warps solve the sub-panel below against it, X = A L_pp^-T, as a
+//      product with the sub-block's inverse;
+//   3. all warps update the trailing lower triangle, A -= X X^T, with 4 x 4
+//      register tiles.
+// Finally the off-diagonal 32 x 32 blocks of L^-1 are assembled block row by
+// block row: Y_pq = -Y_pp sum_{q <= m < p} L_pm Y_mq.
+constexpr int DIAG_THREADS = 256;
+constexpr int SP = 32;           // sub-panel width
+constexpr int LDA = NB + 4;      // shared-memory row stride (floats)
+constexpr size_t DIAG_SMEM = (2 * NB * LDA + SP * LDA + 3 * SP * SP) * sizeof(float);
+
+// Lane i holds row i of a 32 x 32 symmetric block (entries k <= i) and ends
+// with row i of its lower Cholesky factor.  The pivot row is broadcast by
+// shuffles, so the 32 elimination steps need no CTA-wide barrier.  The steps
+// are unrolled by template recursion so that every index into `a` is a
+// compile-time constant (the array stays in registers).
+template <int J>
+struct CholStep {
+    static __device__ __forceinline__ void run(float (&a)[SP], int lane, int64_t gcol0, DeviceStatus *st) {
+        const unsigned full = 0xffffffffu;
+        const float d = __shfl_sync(full, a[J], J);
+        if (lane == 0 && !(d > 0.f)) atomicMin(&st->bad_pivot, (unsigned long long)(gcol0 + J));
+        const float l = sqrtf(d);
+        const float r = 1.f / l;
+        a[J] = (lane > J) ? a[J] * r : (lane == J ? l : a[J]);
+#pragma unroll
+        for (int k = J + 1; k < SP; ++k) {
+            const float lkj = __shfl_sync(full, a[J], k);
+            a[k] = (lane >= k) ? fmaf(-a[J], lkj, a[k]) : a[k];
+        }
+        CholStep<J + 1>::run(a, lane, gcol0, st);
+    }
+};
+template <>
+struct CholStep<SP> {
+    static __device__ __forceinline__ void run(float (&)[SP], int, int64_t, DeviceStatus *) {}
+};
+
+__device__ __forceinline__ void warp_chol32(float (&a)[SP], int lane, int64_t gcol0, DeviceStatus *st) {
+    CholStep<0>::run(a, lane, gcol0, st);
+}
+
+// Column `lane` of the inverse of the 32 x 32 lower factor stored at L (row
+// stride LDA): y_i = (delta_i,lane - sum_{k<i} L_ik y_k) / L_ii.  L is read
+// with shared-memory broadcasts; the result goes to Y (same stride).
+__device__ __forceinline__ void warp_trinv32(const float *L, float *Y, int lane) {
+    float y[SP];
+#pragma unroll
+    for (int i = 0; i < SP; ++i) {
+        float s = (lane == i) ? 1.f : 0.f;
+#pragma unroll
+        for (int k = 0; k < i; ++k) s = fmaf(-L[i * LDA + k], y[k], s);
+        y[i] = s / L[i * LDA + i];
+        Y[i * LDA + lane] = y[i];
+    }
+}
 
 __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restrict__ F, int64_t cols, int64_t k0,
                                                                   int kb, float *__restrict__ Linv,
                                                                   DeviceStatus *st) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    float(*A)[NB + 1] = reinterpret_cast<float(*)[NB + 1]>(smem_raw);
-    float(*Y)[NB + 1] = A + NB;
-    const int t = threadIdx.x;
-    int own[DIAG_OWN];
-#pragma unroll
-    for (int q = 0; q < DIAG_OWN; ++q) {
-        const int e = t + q * DIAG_THREADS;
-        int i = (int)((sqrtf(8.f * (float)e + 1.f) - 1.f) * 0.5f);
-        while ((i + 1) * (i + 2) / 2 <= e) ++i;
-        while (i * (i + 1) / 2 > e) --i;
-        const int k = e - i * (i + 1) / 2;
-        own[q] = (e < TRI && i < kb) ? ((i << 16) | k) : -1;
-    }
+    extern __shared__ __align__(16) float sm[];
+    float *A = sm;                 // [NB][LDA]: the block, lower triangle, becomes L
+    float *Y = A + NB * LDA;       // [NB][LDA]: L^-1, lower triangle
+    float *XT = Y + NB * LDA;      // [SP][LDA]: solved sub-panel, transposed (XT[k][i] = X_ik)
+    float *T = XT + SP * LDA;      // [3][SP][SP]: partial sums of the inverse assembly
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+
     for (int idx = t; idx < NB * NB; idx += DIAG_THREADS) {
         const int i = idx / NB, j = idx % NB;
-        A[i][j] = (i < kb && j <= i) ? F[(k0 + i) * cols + (k0 + j)] : 0.f;
+        float v;
+        if (i < kb && j < kb) v = (j <= i) ? F[(k0 + i) * cols + (k0 + j)] : 0.f;
+        else v = (i == j) ? 1.f : 0.f;
+        A[i * LDA + j] = v;
+        Y[i * LDA + j] = 0.f;
     }
     __syncthreads();
-    for (int j = 0; j < kb; ++j) {
-        const float d = A[j][j];
-        if (t == 0 && !(d > 0.f)) atomicMin(&st->bad_pivot, (unsigned long long)(k0 + j));
-        const float rd = 1.f / d;
+
+    for (int c0 = 0; c0 < NB; c0 += SP) {
+        if (warp == 0) {
+            float a[SP];
 #pragma unroll
-        for (int q = 0; q < DIAG_OWN; ++q) {
-            if (own[q] < 0) continue;
-            const int i = own[q] >> 16, k = own[q] & 0xffff;
-            if (k > j) A[i][k] = fmaf(-A[i][j] * rd, A[k][j], A[i][k]);
+            for (int k = 0; k < SP; ++k) a[k] = (k <= lane) ? A[(c0 + lane) * LDA + c0 + k] : 0.f;
+            warp_chol32(a, lane, k0 + c0, st);
+#pragma unroll
+            for (int k = 0; k < SP; ++k)
+                if (k <= lane) A[(c0 + lane) * LDA + c0 + k] = a[k];
+            __syncwarp();
+            warp_trinv32(A + c0 * LDA + c0, Y + c0 * LDA + c0, lane);
+        }
+        __syncthreads();
+        const int r0 = c0 + SP, R = NB - r0;  // rows below the diagonal sub-block
+        if (R == 0) break;
+        // X_ic = sum_{k <= c} A_ik Y_ck; TPR threads per row, interleaved columns.
+        const int tpr = DIAG_THREADS / R >= 8 ? 8 : (DIAG_THREADS / R >= 4 ? 4 : 2);
+        const int row = t / tpr, sub = t % tpr;
+        float xo[SP / 2];
+        if (row < R) {
+            float ar[SP];
+            const float *ap = A + (r0 + row) * LDA + c0;
+#pragma unroll
+            for (int k = 0; k < SP; k += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(ap + k);
+                ar[k] = v.x; ar[k + 1] = v.y; ar[k + 2] = v.z; ar[k + 3] = v.w;
+            }
+#pragma unroll
+            for (int q = 0; q < SP / 2; ++q) {
+                const int c = sub + q * tpr;
+                float acc = 0.f;
+                if (c < SP) {
+                    const float *yp = Y + (c0 + c) * LDA + c0;
+#pragma unroll
+                    for (int k = 0; k < SP; ++k)
+                        if (k <= c) acc = fmaf(ar[k], yp[k], acc);
+                }
+                xo[q] = acc;
+            }
+        }
+        __syncthreads();
+        if (row < R) {
+#pragma unroll
+            for (int q = 0; q < SP / 2; ++q) {
+                const int c = sub + q * tpr;
+                if (c < SP) {
+                    A[(r0 + row) * LDA + c0 + c] = xo[q];
+                    XT[c * LDA + r0 + row] = xo[q];
+                }
+            }
+        }
+        __syncthreads();
+        // A_ij -= sum_k X_ik X_jk for r0 <= j <= i < NB, in 4 x 4 tiles.
+        const int nt = R / 4, ntiles = nt * (nt + 1) / 2;
+        for (int tile = t; tile < ntiles; tile += DIAG_THREADS) {
+            int ti = (int)((sqrtf(8.f * (float)tile + 1.f) - 1.f) * 0.5f);
+            while ((ti + 1) * (ti + 2) / 2 <= tile) ++ti;
+            while (ti * (ti + 1) / 2 > tile) --ti;
+            const int tj = tile - ti * (ti + 1) / 2;
+            const int i0 = r0 + 4 * ti, j0 = r0 + 4 * tj;
+            float acc[4][4] = {};
+#pragma unroll 8
+            for (int k = 0; k < SP; ++k) {
+                const float4 xi = *reinterpret_cast<const float4 *>(XT + k * LDA + i0);
+                const float4 xj = *reinterpret_cast<const float4 *>(XT + k * LDA + j0);
+                const float vi[4] = {xi.x, xi.y, xi.z, xi.w}, vj[4] = {xj.x, xj.y, xj.z, xj.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(vi[a], vj[b], acc[a][b]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    if (j0 + b <= i0 + a) A[(i0 + a) * LDA + j0 + b] -= acc[a][b];
         }
         __syncthreads();
     }
-    // Scale to the Cholesky factor (L_ij = a_ij / sqrt(a_jj)); then Y starts as I.
-#pragma unroll
-    for (int q = 0; q < DIAG_OWN; ++q) {
-        if (own[q] < 0) continue;
-        const int i = own[q] >> 16, k = own[q] & 0xffff;
-        const float l = sqrtf(A[k][k]);
-        Y[i][k] = (i == k) ? l : A[i][k] / l;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < DIAG_OWN; ++q) {
-        if (own[q] < 0) continue;
-        const int i = own[q] >> 16, k = own[q] & 0xffff;
-        A[i][k] = Y[i][k];
-        Y[i][k] = (i == k) ? 1.f : 0.f;
-    }
-    __syncthreads();
-    for (int k = 0; k < kb; ++k) {
-        const float rl = 1.f / A[k][k];
-#pragma unroll
-        for (int q = 0; q < DIAG_OWN; ++q) {
-            if (own[q] < 0) continue;
-            const int i = own[q] >> 16, c = own[q] & 0xffff;
-            if (i > k && c <= k) Y[i][c] = fmaf(-A[i][k] * rl, Y[k][c], Y[i][c]);
+
+    // Off-diagonal blocks of Y = L^-1, one block row p at a time.
+    for (int p = 1; p < NB / SP; ++p) {
+        // T_q = sum_{m=q}^{p-1} L_pm Y_mq for q < p.
+        for (int idx = t; idx < p * SP * SP; idx += DIAG_THREADS) {
+            const int q = idx / (SP * SP), i = (idx / SP) % SP, c = idx % SP;
+            const float *lp = A + (p * SP + i) * LDA;
+            float acc = 0.f;
+            for (int k = q * SP; k < p * SP; ++k) acc = fmaf(lp[k], Y[k * LDA + q * SP + c], acc);
+            T[idx] = acc;
+        }
+        __syncthreads();
+        // Y_pq = -Y_pp T_q.
+        for (int idx = t; idx < p * SP * SP; idx += DIAG_THREADS) {
+            const int q = idx / (SP * SP), i = (idx / SP) % SP, c = idx % SP;
+            const float *yp = Y + (p * SP + i) * LDA + p * SP;
+            const float *tq = T + q * SP * SP;
+            float acc = 0.f;
+            for (int k = 0; k <= i; ++k) acc = fmaf(yp[k], tq[k * SP + c], acc);
+            Y[(p * SP + i) * LDA + q * SP + c] = -acc;
         }
         __syncthreads();
     }
-#pragma unroll
-    for (int q = 0; q < DIAG_OWN; ++q) {
-        if (own[q] < 0) continue;
-        const int i = own[q] >> 16, c = own[q] & 0xffff;
-        Y[i][c] = Y[i][c] / A[i][i];
-    }
-    __syncthreads();
+
     for (int idx = t; idx < NB * NB; idx += DIAG_THREADS) {
         const int i = idx / NB, j = idx % NB;
-        if (i < kb && j <= i) F[(k0 + i) * cols + (k0 + j)] = A[i][j];
-        Linv[idx] = (i < kb && j <= i) ? Y[i][j] : 0.f;
+        const bool in = i < kb && j <= i;
+        if (in) F[(k0 + i) * cols + (k0 + j)] = A[i * LDA + j];
+        Linv[idx] = in ? Y[i * LDA + j] : 0.f;
     }
 }
 

@@ -58,8 +58,18 @@ template <typename TA, bool AT, bool BT>
 __global__ void __launch_bounds__(NT) sgemm_kernel(int64_t M, int64_t N, int64_t K, float alpha,
                                                    const TA *A, int64_t lda,
                                                    const TA *__restrict__ B, int64_t ldb, float beta,
-                                                   float *C, int64_t ldc, int tri) {
+                                                   float *C, int64_t ldc, int tri, int64_t kslice,
+                                                   int64_t c_zstride) {
     const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
+    if (gridDim.z > 1) {
+        // Split K: slice z covers k in [z * kslice, min(K, (z + 1) * kslice)) and
+        // writes its own partial product at C + z * c_zstride.
+        const int64_t kz = (int64_t)blockIdx.z * kslice;
+        A += AT ? kz * lda : kz;
+        B += BT ? kz : kz * ldb;
+        K = (K - kz) < kslice ? (K - kz) : kslice;
+        C += (int64_t)blockIdx.z * c_zstride;
+    }
     if (tri == 1 && n0 > m0 + BM - 1) return;  // tile entirely above the diagonal
     if (tri == 2 && m0 > n0 + BN - 1) return;  // tile entirely below the diagonal
 
@@ -141,13 +151,45 @@ cudaError_t sgemm(int64_t M, int64_t N, int64_t K, float alpha, const TA *A, int
     if (M <= 0 || N <= 0) return cudaSuccess;
     dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
     if (a_t && b_t)
-        sgemm_kernel<TA, true, true><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri);
+        sgemm_kernel<TA, true, true><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri, K, 0);
     else if (a_t)
-        sgemm_kernel<TA, true, false><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri);
+        sgemm_kernel<TA, true, false><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri, K, 0);
     else if (b_t)
-        sgemm_kernel<TA, false, true><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri);
+        sgemm_kernel<TA, false, true><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri, K, 0);
     else
-        sgemm_kernel<TA, false, false><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri);
+        sgemm_kernel<TA, false, false><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri, K, 0);
+    return cudaGetLastError();
+}
+
+namespace {
+__global__ void sum_slices_kernel(const float *__restrict__ P, int slices, int64_t n, float *__restrict__ C) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float acc = 0.f;
+        for (int z = 0; z < slices; ++z) acc += P[z * n + i];
+        C[i] = acc;
+    }
+}
+}  // namespace
+
+cudaError_t sgemm_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, bool a_t, const float *B,
+                         int64_t ldb, bool b_t, float *C, float *partials, int slices, cudaStream_t s) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    const int64_t kslice = ((K + slices - 1) / slices + BK - 1) / BK * BK;
+    const int z = (int)((K + kslice - 1) / kslice);
+    dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM), (unsigned)(z < 1 ? 1 : z));
+    const int64_t cz = M * N;
+    if (a_t && b_t)
+        sgemm_kernel<float, true, true><<<grid, NT, 0, s>>>(M, N, K, 1.f, A, lda, B, ldb, 0.f, partials, N, 0, kslice, cz);
+    else if (a_t)
+        sgemm_kernel<float, true, false><<<grid, NT, 0, s>>>(M, N, K, 1.f, A, lda, B, ldb, 0.f, partials, N, 0, kslice, cz);
+    else if (b_t)
+        sgemm_kernel<float, false, true><<<grid, NT, 0, s>>>(M, N, K, 1.f, A, lda, B, ldb, 0.f, partials, N, 0, kslice, cz);
+    else
+        sgemm_kernel<float, false, false><<<grid, NT, 0, s>>>(M, N, K, 1.f, A, lda, B, ldb, 0.f, partials, N, 0, kslice, cz);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t n = M * N;
+    sum_slices_kernel<<<(unsigned)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184), 256, 0, s>>>(partials, z < 1 ? 1 : z, n, C);
     return cudaGetLastError();
 }
 

@@ -74,3 +74,14 @@ def test_host_side_validation(gq):
     assert gq.lib.gptq_hessian_accumulate(None, 256, None, 1, 10, 100, None) == -1  # ldx < cols
     assert gq.lib.gptq_pack(None, 4, 32, 3, None, None) == -1
     assert gq.lib.gptq_pack(ctypes.c_void_p(16), 4, 36, 3, ctypes.c_void_p(16), None) == -1  # cols*bits % 32
+
+
+def test_eora_host_side_validation(gq):
+    p = ctypes.c_void_p
+    f = gq.lib.eora_compensate
+    assert f(p(256), 64, 64, p(256), 0, p(256), p(256), None, p(256), 1 << 30, None, None) == -1   # r = 0
+    assert f(p(256), 256, 256, p(256), 65, p(256), p(256), None, p(256), 1 << 30, None, None) == -1  # r > 64
+    assert f(p(256), 8, 64, p(256), 16, p(256), p(256), None, p(256), 1 << 30, None, None) == -1   # r > rows
+    assert f(None, 64, 64, p(256), 4, p(256), p(256), None, p(256), 1 << 30, None, None) == -1     # null dW
+    assert f(p(256), 64, 64, p(256), 4, p(256), p(256), None, p(256), 16, None, None) == -7        # workspace
+    assert gq.lib.eora_compensate_workspace_size(5120, 5120, 64) >= 3 * 5120 * 5120 * 4
