@@ -70,62 +70,63 @@ __global__ void reverse_damp_kernel(const float *__restrict__ H, int64_t cols, f
 //   1. warp 0 factors the 32 x 32 diagonal sub-block in registers (lane i
 //      holds row i; the pivot row is broadcast by shuffles, so no CTA-wide
 //      barrier is needed inside the 32 steps) and forms its inverse by
-//      forward substitution (lane c holds column c of the inverse);
+//      forward substitution (lane c produces column c of the inverse);
 //   2. all warps solve the sub-panel below against it, X = A L_pp^-T, as a
-//      product with the sub-block's inverse;
-//   3. all warps update the trailing lower triangle, A -= X X^T, with 4 x 4
-//      register tiles.
+//      product with the sub-block's inverse (4 x 4 register tiles);
+//   3. all warps update the trailing lower triangle, A -= X X^T (4 x 4 tiles).
 // Finally the off-diagonal 32 x 32 blocks of L^-1 are assembled block row by
-// block row: Y_pq = -Y_pp sum_{q <= m < p} L_pm Y_mq.
+// block row: Y_pq = -Y_pp sum_{q <= m < p} L_pm Y_mq (4 x 4 tiles).
+// The pivot reciprocal square root comes from rsqrtf; the factor is d * rsqrt(d).
 constexpr int DIAG_THREADS = 256;
 constexpr int SP = 32;           // sub-panel width
 constexpr int LDA = NB + 4;      // shared-memory row stride (floats)
-constexpr size_t DIAG_SMEM = (2 * NB * LDA + SP * LDA + 3 * SP * SP) * sizeof(float);
+constexpr size_t DIAG_SMEM = (2 * NB * LDA + 2 * SP * LDA + 3 * SP * SP + SP) * sizeof(float);
 
 // Lane i holds row i of a 32 x 32 symmetric block (entries k <= i) and ends
-// with row i of its lower Cholesky factor.  The pivot row is broadcast by
-// shuffles, so the 32 elimination steps need no CTA-wide barrier.  The steps
-// are unrolled by template recursion so that every index into `a` is a
-// compile-time constant (the array stays in registers).
+// with row i of its lower Cholesky factor; `rinv` of lane i ends as 1 / L_ii.
+// The steps are unrolled by template recursion so that every index into `a`
+// is a compile-time constant (the array stays in registers).
 template <int J>
 struct CholStep {
-    static __device__ __forceinline__ void run(float (&a)[SP], int lane, int64_t gcol0, DeviceStatus *st) {
+    static __device__ __forceinline__ void run(float (&a)[SP], float &rinv, int lane, int64_t gcol0,
+                                               DeviceStatus *st) {
         const unsigned full = 0xffffffffu;
         const float d = __shfl_sync(full, a[J], J);
         if (lane == 0 && !(d > 0.f)) atomicMin(&st->bad_pivot, (unsigned long long)(gcol0 + J));
-        const float l = sqrtf(d);
-        const float r = 1.f / l;
-        a[J] = (lane > J) ? a[J] * r : (lane == J ? l : a[J]);
+        const float r = rsqrtf(d);
+        if (lane == J) rinv = r;
+        a[J] = (lane > J) ? a[J] * r : (lane == J ? d * r : a[J]);
 #pragma unroll
         for (int k = J + 1; k < SP; ++k) {
             const float lkj = __shfl_sync(full, a[J], k);
             a[k] = (lane >= k) ? fmaf(-a[J], lkj, a[k]) : a[k];
         }
-        CholStep<J + 1>::run(a, lane, gcol0, st);
+        CholStep<J + 1>::run(a, rinv, lane, gcol0, st);
     }
 };
 template <>
 struct CholStep<SP> {
-    static __device__ __forceinline__ void run(float (&)[SP], int, int64_t, DeviceStatus *) {}
+    static __device__ __forceinline__ void run(float (&)[SP], float &, int, int64_t, DeviceStatus *) {}
 };
 
-__device__ __forceinline__ void warp_chol32(float (&a)[SP], int lane, int64_t gcol0, DeviceStatus *st) {
-    CholStep<0>::run(a, lane, gcol0, st);
-}
-
 // Column `lane` of the inverse of the 32 x 32 lower factor stored at L (row
-// stride LDA): y_i = (delta_i,lane - sum_{k<i} L_ik y_k) / L_ii.  L is read
-// with shared-memory broadcasts; the result goes to Y (same stride).
-__device__ __forceinline__ void warp_trinv32(const float *L, float *Y, int lane) {
+// stride LDA), dinv[i] = 1 / L_ii: y_i = (delta_i,lane - sum_{k<i} L_ik y_k) dinv_i.
+// Written transposed: YT[lane][i] = (L^-1)_{i,lane}.
+__device__ __forceinline__ void warp_trinv32(const float *L, const float *dinv, float *YT, int lane) {
     float y[SP];
 #pragma unroll
     for (int i = 0; i < SP; ++i) {
-        float s = (lane == i) ? 1.f : 0.f;
+        float s0 = (lane == i) ? 1.f : 0.f, s1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < i; ++k) s = fmaf(-L[i * LDA + k], y[k], s);
-        y[i] = s / L[i * LDA + i];
-        Y[i * LDA + lane] = y[i];
+        for (int k = 0; k + 1 < i; k += 2) {
+            s0 = fmaf(-L[i * LDA + k], y[k], s0);
+            s1 = fmaf(-L[i * LDA + k + 1], y[k + 1], s1);
+        }
+        if (i & 1) s0 = fmaf(-L[i * LDA + i - 1], y[i - 1], s0);
+        y[i] = (s0 + s1) * dinv[i];
     }
+#pragma unroll
+    for (int i = 0; i < SP; ++i) YT[lane * LDA + i] = y[i];
 }
 
 __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restrict__ F, int64_t cols, int64_t k0,
@@ -135,68 +136,97 @@ __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restr
     float *A = sm;                 // [NB][LDA]: the block, lower triangle, becomes L
     float *Y = A + NB * LDA;       // [NB][LDA]: L^-1, lower triangle
     float *XT = Y + NB * LDA;      // [SP][LDA]: solved sub-panel, transposed (XT[k][i] = X_ik)
-    float *T = XT + SP * LDA;      // [3][SP][SP]: partial sums of the inverse assembly
+    float *YT = XT + SP * LDA;     // [SP][LDA]: current diagonal inverse, transposed
+    float *T = YT + SP * LDA;      // [3][SP][SP]: partial sums of the inverse assembly
+    float *dinv = T + 3 * SP * SP; // [SP]
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
 
-    for (int idx = t; idx < NB * NB; idx += DIAG_THREADS) {
-        const int i = idx / NB, j = idx % NB;
-        float v;
-        if (i < kb && j < kb) v = (j <= i) ? F[(k0 + i) * cols + (k0 + j)] : 0.f;
-        else v = (i == j) ? 1.f : 0.f;
-        A[i * LDA + j] = v;
-        Y[i * LDA + j] = 0.f;
+    // Load: 16 float4 per thread, all issued before any shared-memory store.
+    const bool vec = (cols % 4) == 0 && ((uintptr_t)F % 16) == 0;
+    {
+        float4 v[NB * NB / 4 / DIAG_THREADS];
+#pragma unroll
+        for (int u = 0; u < NB * NB / 4 / DIAG_THREADS; ++u) {
+            const int idx = t + u * DIAG_THREADS;
+            const int i = idx / (NB / 4), j = (idx % (NB / 4)) * 4;
+            const float *src = F + (k0 + i) * cols + (k0 + j);
+            if (vec && i < kb && j + 3 < kb) {
+                v[u] = *reinterpret_cast<const float4 *>(src);
+            } else {
+                float e[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) e[c] = (i < kb && j + c < kb) ? src[c] : 0.f;
+                v[u] = make_float4(e[0], e[1], e[2], e[3]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NB * NB / 4 / DIAG_THREADS; ++u) {
+            const int idx = t + u * DIAG_THREADS;
+            const int i = idx / (NB / 4), j = (idx % (NB / 4)) * 4;
+            float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int jj = j + c;
+                if (i >= kb || jj >= kb) e[c] = (i == jj) ? 1.f : 0.f;
+                else if (jj > i) e[c] = 0.f;
+            }
+            *reinterpret_cast<float4 *>(A + i * LDA + j) = make_float4(e[0], e[1], e[2], e[3]);
+            *reinterpret_cast<float4 *>(Y + i * LDA + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     __syncthreads();
 
     for (int c0 = 0; c0 < NB; c0 += SP) {
         if (warp == 0) {
-            float a[SP];
+            float a[SP], rinv = 0.f;
 #pragma unroll
             for (int k = 0; k < SP; ++k) a[k] = (k <= lane) ? A[(c0 + lane) * LDA + c0 + k] : 0.f;
-            warp_chol32(a, lane, k0 + c0, st);
+            CholStep<0>::run(a, rinv, lane, k0 + c0, st);
 #pragma unroll
             for (int k = 0; k < SP; ++k)
                 if (k <= lane) A[(c0 + lane) * LDA + c0 + k] = a[k];
+            dinv[lane] = rinv;
             __syncwarp();
-            warp_trinv32(A + c0 * LDA + c0, Y + c0 * LDA + c0, lane);
+            warp_trinv32(A + c0 * LDA + c0, dinv, YT, lane);
+            __syncwarp();
+            // Diagonal block of Y from its transposed copy.
+#pragma unroll 4
+            for (int i = 0; i < SP; ++i) Y[(c0 + i) * LDA + c0 + lane] = YT[lane * LDA + i];
         }
         __syncthreads();
         const int r0 = c0 + SP, R = NB - r0;  // rows below the diagonal sub-block
         if (R == 0) break;
-        // X_ic = sum_{k <= c} A_ik Y_ck; TPR threads per row, interleaved columns.
-        const int tpr = DIAG_THREADS / R >= 8 ? 8 : (DIAG_THREADS / R >= 4 ? 4 : 2);
-        const int row = t / tpr, sub = t % tpr;
-        float xo[SP / 2];
-        if (row < R) {
-            float ar[SP];
-            const float *ap = A + (r0 + row) * LDA + c0;
+        // X_ic = sum_{k <= c} A_ik Y_ck (Y_ck = YT[k][c]) in 4 x 4 tiles: rows i0.., columns cc..
+        const int ntile = (R / 4) * (SP / 4);
+        float xo[4][4];
+        int ti0 = 0, tc0 = 0;
+        const bool active = t < ntile;
+        if (active) {
+            ti0 = r0 + (t / (SP / 4)) * 4;
+            tc0 = (t % (SP / 4)) * 4;
 #pragma unroll
-            for (int k = 0; k < SP; k += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(ap + k);
-                ar[k] = v.x; ar[k + 1] = v.y; ar[k + 2] = v.z; ar[k + 3] = v.w;
-            }
+            for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int q = 0; q < SP / 2; ++q) {
-                const int c = sub + q * tpr;
-                float acc = 0.f;
-                if (c < SP) {
-                    const float *yp = Y + (c0 + c) * LDA + c0;
+                for (int b = 0; b < 4; ++b) xo[a][b] = 0.f;
+            for (int k = 0; k < tc0 + 4; ++k) {
+                const float4 yv = *reinterpret_cast<const float4 *>(YT + k * LDA + tc0);
+                const float yb[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
-                    for (int k = 0; k < SP; ++k)
-                        if (k <= c) acc = fmaf(ar[k], yp[k], acc);
+                for (int a = 0; a < 4; ++a) {
+                    const float av = A[(ti0 + a) * LDA + c0 + k];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) xo[a][b] = fmaf(av, yb[b], xo[a][b]);
                 }
-                xo[q] = acc;
             }
         }
         __syncthreads();
-        if (row < R) {
+        if (active) {
 #pragma unroll
-            for (int q = 0; q < SP / 2; ++q) {
-                const int c = sub + q * tpr;
-                if (c < SP) {
-                    A[(r0 + row) * LDA + c0 + c] = xo[q];
-                    XT[c * LDA + r0 + row] = xo[q];
-                }
+            for (int a = 0; a < 4; ++a) {
+                *reinterpret_cast<float4 *>(A + (ti0 + a) * LDA + c0 + tc0) =
+                    make_float4(xo[a][0], xo[a][1], xo[a][2], xo[a][3]);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) XT[(tc0 + b) * LDA + ti0 + a] = xo[a][b];
             }
         }
         __syncthreads();
@@ -228,34 +258,74 @@ __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restr
         __syncthreads();
     }
 
-    // Off-diagonal blocks of Y = L^-1, one block row p at a time.
+    // Off-diagonal blocks of Y = L^-1, one block row p at a time, 4 x 4 tiles:
+    // T_q = sum_{m=q}^{p-1} L_pm Y_mq, then Y_pq = -Y_pp T_q, for q < p.
     for (int p = 1; p < NB / SP; ++p) {
-        // T_q = sum_{m=q}^{p-1} L_pm Y_mq for q < p.
-        for (int idx = t; idx < p * SP * SP; idx += DIAG_THREADS) {
-            const int q = idx / (SP * SP), i = (idx / SP) % SP, c = idx % SP;
-            const float *lp = A + (p * SP + i) * LDA;
-            float acc = 0.f;
-            for (int k = q * SP; k < p * SP; ++k) acc = fmaf(lp[k], Y[k * LDA + q * SP + c], acc);
-            T[idx] = acc;
+        const int ntl = p * (SP / 4) * (SP / 4);
+        for (int tl = t; tl < ntl; tl += DIAG_THREADS) {
+            const int q = tl / 64, i0 = ((tl / 8) % 8) * 4, c0 = (tl % 8) * 4;
+            float acc[4][4] = {};
+            for (int k = q * SP; k < p * SP; ++k) {
+                const float4 yv = *reinterpret_cast<const float4 *>(Y + k * LDA + q * SP + c0);
+                const float yb[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float lv = A[(p * SP + i0 + a) * LDA + k];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(lv, yb[b], acc[a][b]);
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                *reinterpret_cast<float4 *>(T + q * SP * SP + (i0 + a) * SP + c0) =
+                    make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
         }
         __syncthreads();
-        // Y_pq = -Y_pp T_q.
-        for (int idx = t; idx < p * SP * SP; idx += DIAG_THREADS) {
-            const int q = idx / (SP * SP), i = (idx / SP) % SP, c = idx % SP;
-            const float *yp = Y + (p * SP + i) * LDA + p * SP;
+        for (int tl = t; tl < ntl; tl += DIAG_THREADS) {
+            const int q = tl / 64, i0 = ((tl / 8) % 8) * 4, c0 = (tl % 8) * 4;
             const float *tq = T + q * SP * SP;
-            float acc = 0.f;
-            for (int k = 0; k <= i; ++k) acc = fmaf(yp[k], tq[k * SP + c], acc);
-            Y[(p * SP + i) * LDA + q * SP + c] = -acc;
+            float acc[4][4] = {};
+            for (int k = 0; k < i0 + 4; ++k) {
+                const float4 tv = *reinterpret_cast<const float4 *>(tq + k * SP + c0);
+                const float tb[4] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float yv = Y[(p * SP + i0 + a) * LDA + p * SP + k];  // zero for k > i0 + a
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(yv, tb[b], acc[a][b]);
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                *reinterpret_cast<float4 *>(Y + (p * SP + i0 + a) * LDA + q * SP + c0) =
+                    make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
         }
         __syncthreads();
     }
 
-    for (int idx = t; idx < NB * NB; idx += DIAG_THREADS) {
-        const int i = idx / NB, j = idx % NB;
-        const bool in = i < kb && j <= i;
-        if (in) F[(k0 + i) * cols + (k0 + j)] = A[i * LDA + j];
-        Linv[idx] = in ? Y[i * LDA + j] : 0.f;
+    // Store: F gets the lower factor (its part above the diagonal is zero in A),
+    // Linv the inverse; padding rows / columns are not written to F.
+#pragma unroll 4
+    for (int u = 0; u < NB * NB / 4 / DIAG_THREADS; ++u) {
+        const int idx = t + u * DIAG_THREADS;
+        const int i = idx / (NB / 4), j = (idx % (NB / 4)) * 4;
+        const float4 lv = *reinterpret_cast<const float4 *>(A + i * LDA + j);
+        float4 yv = *reinterpret_cast<const float4 *>(Y + i * LDA + j);
+        float *dst = F + (k0 + i) * cols + (k0 + j);
+        if (vec && i < kb && j + 3 < kb) {
+            *reinterpret_cast<float4 *>(dst) = lv;
+        } else if (i < kb) {
+            const float e[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (j + c < kb) dst[c] = e[c];
+        }
+        if (i >= kb) yv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j + 0 >= kb) yv.x = 0.f;
+        if (j + 1 >= kb) yv.y = 0.f;
+        if (j + 2 >= kb) yv.z = 0.f;
+        if (j + 3 >= kb) yv.w = 0.f;
+        *reinterpret_cast<float4 *>(Linv + idx * 4) = yv;
     }
 }
 
