@@ -197,7 +197,7 @@ gq_status eora_compensate(const float *dW, int64_t rows, int64_t cols, const flo
  * is allocated or freed: no cudaMalloc, no cudaFree, no allocating library call.
  *
  *   Size limit: gptq_quantize_layer_workspace_size(rows, cols, block) must be
- *   <= GQ_NOALLOC_SCRATCH_BYTES (e.g. rows = cols = 1024, block = 128 fits);
+ *   <= GQ_NOALLOC_SCRATCH_BYTES (e.g. rows = cols = 768, block = 128 fits);
  *   larger layers are rejected with GQ_EWORKSPACE before anything is enqueued.
  *   All buffers must live on the current CUDA device, and `stream` must belong
  *   to it.  The first call on a device looks up the scratch's device address

@@ -12,11 +12,12 @@ namespace {
 inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline cudaStream_t cs(gq_stream_t s) { return (cudaStream_t)s; }
 
-// Sweep workspace: [Uinv: nblk x block x block][V: cols x cols][D: rows x cols], float32.
+// Sweep workspace (float32, 256-byte aligned regions):
+//   [Uinv: nblk x block x block][VThi: cols x cols][VTlo: cols x cols][D: rows x cols][DL: rows x cols].
 size_t sweep_ws_bytes(int64_t rows, int64_t cols, int block) {
     const int64_t nblk = (cols + block - 1) / block;
-    return align_up((size_t)nblk * block * block * sizeof(float)) + align_up((size_t)cols * cols * sizeof(float)) +
-           align_up((size_t)rows * cols * sizeof(float));
+    return align_up((size_t)nblk * block * block * sizeof(float)) + 2 * align_up((size_t)cols * cols * sizeof(float)) +
+           2 * align_up((size_t)rows * cols * sizeof(float));
 }
 
 gq_status check_sweep_args(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *F, int bits,
@@ -47,27 +48,28 @@ struct SweepCtx {
     int32_t *qzeros;
     uint8_t *codes;
     float *W_hat, *row_err;
-    float *Uinv, *V, *D;
+    float *Uinv, *VThi, *VTlo, *D, *DL;
     cudaStream_t s;
 };
 
 // Blocks [a, b): sweep the left half, apply its deferred update to the right
 // half as one GEMM, sweep the right half.  Same sums as updating after every
-// block, in fewer and larger GEMMs.
+// block, in fewer and larger GEMMs.  The GEMM runs on the tensor cores with
+// float32 accuracy (3xTF32): D[:, right] += ΔW[:, left] V[left, right].
 cudaError_t sweep_range(const SweepCtx &c, int64_t a, int64_t b) {
     const int64_t B = c.block;
     if (b - a == 1) {
         const int64_t c0 = a * B;
         const int bw = (int)((c.cols - c0) < B ? (c.cols - c0) : B);
         return sweep_block_launch(c.W, c.bf16, c.rows, c.cols, c0, bw, c.Uinv + a * B * B, c.F, c.dead, c.bits, c.group,
-                                  c.D, c.qweight, c.scales, c.qzeros, c.codes, c.W_hat, c.row_err, c.s);
+                                  c.D, c.DL, c.qweight, c.scales, c.qzeros, c.codes, c.W_hat, c.row_err, c.s);
     }
     const int64_t m = (a + b) / 2;
     cudaError_t e = sweep_range(c, a, m);
     if (e != cudaSuccess) return e;
     const int64_t k0 = a * B, k1 = m * B, n1 = (b * B < c.cols) ? b * B : c.cols;
-    e = sgemm<float>(c.rows, n1 - k1, k1 - k0, 1.f, c.D + k0, c.cols, false, c.V + k0 * c.cols + k1, c.cols, false, 1.f,
-                     c.D + k1, c.cols, 0, c.s);
+    e = gemm3(c.rows, n1 - k1, k1 - k0, 1.f, c.D + k0, c.DL + k0, c.cols, c.VThi + k1 * c.cols + k0,
+              c.VTlo + k1 * c.cols + k0, c.cols, 1.f, c.D + k1, c.cols, 0, nullptr, nullptr, 0, c.s);
     if (e != cudaSuccess) return e;
     return sweep_range(c, m, b);
 }
@@ -94,9 +96,10 @@ const char *gq_status_string(gq_status s) {
 
 gq_status gq_check_device(gq_stream_t stream) {
     if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return GQ_ECUDA;
-    const unsigned int e = read_and_clear_device_error();
-    if (e == ~0u) return GQ_ECUDA;
-    return e ? GQ_ETIMEOUT : GQ_OK;
+    const unsigned int e1 = read_and_clear_device_error();
+    const unsigned int e2 = gemm_read_and_clear_error();
+    if (e1 == ~0u || e2 == ~0u) return GQ_ECUDA;
+    return (e1 | e2) ? GQ_ETIMEOUT : GQ_OK;
 }
 
 gq_status gptq_hessian_accumulate(float *H, int64_t cols, const void *X, gq_dtype xt, int64_t n, int64_t ldx,
@@ -120,8 +123,7 @@ gq_status gptq_hessian_accumulate(float *H, int64_t cols, const void *X, gq_dtyp
 }
 
 size_t gptq_factor_workspace_size(int64_t cols) {
-    (void)cols;
-    return factor_scratch_bytes();
+    return factor_scratch_bytes(cols);
 }
 
 gq_status gptq_factor(const float *H, int64_t cols, float damp, float *F, uint8_t *dead, void *ws, size_t ws_bytes,
@@ -166,13 +168,15 @@ gq_status gptq_sweep(const void *W, gq_dtype wt, int64_t rows, int64_t cols, con
     c.bits = bits; c.group = group; c.block = block;
     c.qweight = qweight; c.scales = scales; c.qzeros = qzeros; c.codes = codes; c.W_hat = W_hat; c.row_err = row_err;
     c.Uinv = (float *)ws;
-    c.V = (float *)((char *)ws + align_up((size_t)nblk * block * block * sizeof(float)));
-    c.D = (float *)((char *)c.V + align_up((size_t)cols * cols * sizeof(float)));
+    c.VThi = (float *)((char *)ws + align_up((size_t)nblk * block * block * sizeof(float)));
+    c.VTlo = (float *)((char *)c.VThi + align_up((size_t)cols * cols * sizeof(float)));
+    c.D = (float *)((char *)c.VTlo + align_up((size_t)cols * cols * sizeof(float)));
+    c.DL = (float *)((char *)c.D + align_up((size_t)rows * cols * sizeof(float)));
     c.s = s;
     GQ_CUDA_TRY(cudaMemsetAsync(c.D, 0, (size_t)rows * cols * sizeof(float), s));
     if (row_err) GQ_CUDA_TRY(cudaMemsetAsync(row_err, 0, (size_t)rows * sizeof(float), s));
     GQ_CUDA_TRY(block_inverses(F, cols, block, c.Uinv, s));
-    GQ_CUDA_TRY(premultiply(F, cols, block, c.Uinv, c.V, s));
+    GQ_CUDA_TRY(premultiply_t(F, cols, block, c.Uinv, c.VThi, c.VTlo, s));
     GQ_CUDA_TRY(sweep_range(c, 0, nblk));
     return GQ_OK;
 }

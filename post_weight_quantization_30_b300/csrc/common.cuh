@@ -62,28 +62,51 @@ cudaError_t sgemm(int64_t M, int64_t N, int64_t K, float alpha, const TA *A, int
 cudaError_t sgemm_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, bool a_t, const float *B,
                          int64_t ldb, bool b_t, float *C, float *partials, int slices, cudaStream_t s);
 
+// C = beta C + alpha A B^T on the tensor cores with float32 accuracy (3xTF32):
+// A (M x K) and B (N x K), K contiguous, each given as its TF32 split
+// (hi, lo) with x = hi + lo.  tri = 1 skips the output tiles entirely above
+// the diagonal.  Optional Chi / Clo (may be NULL) receive the split of the
+// result (leading dimension ldcs).  Row strides must be multiples of 4
+// elements and operand bases 16-byte aligned (gemm3_supported).
+bool gemm3_supported(const void *p, int64_t ld);
+cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi, const float *Alo, int64_t lda,
+                  const float *Bhi, const float *Blo, int64_t ldb, float beta, float *C, int64_t ldc, int tri,
+                  float *Chi, float *Clo, int64_t ldcs, cudaStream_t s);
+// hi / lo TF32 split of a rows x cols float32 matrix (x = hi + lo exactly).
+cudaError_t split_tf32(const float *src, int64_t rows, int64_t cols, int64_t lds, float *hi, float *lo, int64_t ldd,
+                       cudaStream_t s);
+
 // Hessian accumulation on the tensor cores (bf16 inputs, tcgen05 + TMA).
 cudaError_t hessian_bf16_tc(float *H, int64_t cols, const __nv_bfloat16 *X, int64_t n, int64_t ldx,
                             cudaStream_t s);
 bool hessian_bf16_tc_supported(int64_t cols, const void *X, int64_t ldx);
-// Error bits recorded by bounded device-side waits since the last call (then cleared).
+// Error bits recorded by bounded device-side waits since the last call (then
+// cleared): the Hessian kernel's and the GEMM kernel's flags.  ~0u if the flag
+// could not be read.
 unsigned int read_and_clear_device_error();
+unsigned int gemm_read_and_clear_error();
 
 // Factor pieces.
 cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, uint8_t *dead,
                            DeviceStatus *st, cudaStream_t s);
-// Linv: 128 x 128 float32 scratch.
-cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *Linv, cudaStream_t s);
+// scratch: cholesky_scratch_floats(cols) floats, 16-byte aligned; its first
+// 128 x 128 floats hold the inverse of the last diagonal block on return.
+size_t cholesky_scratch_floats(int64_t cols);
+cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *scratch, cudaStream_t s);
 cudaError_t factor_finalize(float *F, int64_t cols, cudaStream_t s);
-size_t factor_scratch_bytes();
+size_t factor_scratch_bytes(int64_t cols);
 
 // Sweep pieces.
 cudaError_t block_inverses(const float *F, int64_t cols, int block, float *Uinv, cudaStream_t s);
-// V[rows above block b, blk_b] = F[..., blk_b] Uinv_b for every block column b (V may alias F).
-cudaError_t premultiply(const float *F, int64_t cols, int block, const float *Uinv, float *V, cudaStream_t s);
+// VT[blk_b, rows above block b] = (F[..., blk_b] Uinv_b)^T for every block column
+// b, written as its TF32 split (VThi, VTlo; cols x cols each, row-major).
+cudaError_t premultiply_t(const float *F, int64_t cols, int block, const float *Uinv, float *VThi, float *VTlo,
+                          cudaStream_t s);
+// One block of the sweep.  On exit the block's columns of D hold the TF32 hi
+// part of ΔW and those of DL the lo part.
 cudaError_t sweep_block_launch(const void *W, bool w_bf16, int64_t rows, int64_t cols, int64_t c0,
                                int bw, const float *Uinv_blk, const float *F, const uint8_t *dead, int bits, int group,
-                               float *D, int32_t *qweight, float *scales, int32_t *qzeros,
+                               float *D, float *DL, int32_t *qweight, float *scales, int32_t *qzeros,
                                uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s);
 
 // EoRA (eora.cu).  eora_run synchronizes `s` once, after the factorization of

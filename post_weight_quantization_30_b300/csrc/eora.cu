@@ -289,7 +289,7 @@ size_t eora_layout(int64_t rows, int64_t cols, int r, EoraWs *w, char *base) {
     };
     EoraWs t;
     t.st = (DeviceStatus *)take(sizeof(DeviceStatus));
-    t.Linv = (float *)take(128 * 128 * sizeof(float));
+    t.Linv = (float *)take(cholesky_scratch_floats(cols > 128 ? cols : 128) * sizeof(float));
     t.F = (float *)take((size_t)cols * cols * sizeof(float));
     t.dead = (uint8_t *)take((size_t)cols);
     t.M = (float *)take((size_t)rows * cols * sizeof(float));

@@ -358,22 +358,47 @@ cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, u
     return cudaGetLastError();
 }
 
-cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *Linv, cudaStream_t s) {
+// Scratch of cholesky_lower_inplace: [Linv: NB x NB][Lhi, Llo: NB x NB][Phi, Plo: cols x NB].
+size_t cholesky_scratch_floats(int64_t cols) { return (size_t)3 * NB * NB + (size_t)2 * cols * NB; }
+
+// Right-looking blocked Cholesky, panel width NB.  Per panel: the diagonal
+// block and its inverse (one CTA); the panel below, P <- P L_kk^-T; the
+// trailing lower triangle, A22 -= P P^T.  The two products run on the tensor
+// cores with float32 accuracy (3xTF32) when the row stride allows TMA
+// (cols % 4 == 0), else on the float32 SIMT GEMM.
+cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *scratch, cudaStream_t s) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(potrf_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DIAG_SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    float *Linv = scratch;
+    float *Lhi = Linv + NB * NB, *Llo = Lhi + NB * NB;
+    float *Phi = Llo + NB * NB, *Plo = Phi + cols * NB;
+    const bool tc = (cols % 4) == 0;
     for (int64_t k0 = 0; k0 < cols; k0 += NB) {
         const int kb = (int)((cols - k0) < NB ? (cols - k0) : NB);
         potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, s>>>(F, cols, k0, kb, Linv, st);
         const int64_t k1 = k0 + kb;
-        if (k1 < cols) {
-            const int64_t rest = cols - k1;
-            float *P = F + k1 * cols + k0;  // rest x kb panel below the diagonal block
+        if (k1 >= cols) break;
+        const int64_t rest = cols - k1;
+        float *P = F + k1 * cols + k0;  // rest x kb panel below the diagonal block
+        cudaError_t e;
+        if (tc) {
+            // P <- P L^-T, also written split (Phi, Plo; row stride NB) for the update.
+            if ((e = split_tf32(Linv, NB, NB, NB, Lhi, Llo, NB, s)) != cudaSuccess) return e;
+            if ((e = split_tf32(P, rest, kb, cols, Phi, Plo, NB, s)) != cudaSuccess) return e;
+            if ((e = gemm3(rest, kb, kb, 1.f, Phi, Plo, NB, Lhi, Llo, NB, 0.f, P, cols, 0, Phi, Plo, NB, s)) !=
+                cudaSuccess)
+                return e;
+            // A22 -= P P^T (tiles touching the lower triangle).
+            if ((e = gemm3(rest, rest, kb, -1.f, Phi, Plo, NB, Phi, Plo, NB, 1.f, F + k1 * cols + k1, cols, 1, nullptr,
+                           nullptr, 0, s)) != cudaSuccess)
+                return e;
+        } else {
             // P <- P L^-T in place: each 128-row tile reads its rows completely before writing them.
-            cudaError_t e = sgemm<float>(rest, kb, kb, 1.f, P, cols, false, Linv, NB, true, 0.f, P, cols, 0, s);
+            e = sgemm<float>(rest, kb, kb, 1.f, P, cols, false, Linv, NB, true, 0.f, P, cols, 0, s);
             if (e != cudaSuccess) return e;
             e = sgemm<float>(rest, rest, kb, -1.f, P, cols, false, P, cols, true, 1.f, F + k1 * cols + k1, cols,
                              /*tri=*/1, s);
@@ -389,6 +414,8 @@ cudaError_t factor_finalize(float *F, int64_t cols, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-size_t factor_scratch_bytes() { return align_up(sizeof(DeviceStatus)) + align_up(NB * NB * sizeof(float)); }
+size_t factor_scratch_bytes(int64_t cols) {
+    return align_up(sizeof(DeviceStatus)) + align_up(cholesky_scratch_floats(cols) * sizeof(float));
+}
 
 }  // namespace gq

@@ -1,0 +1,368 @@
+// Float32-accurate GEMM on the fifth-generation tensor cores (sm_103a):
+//     C = beta C + alpha A B^T      (A: M x K, B: N x K, both K contiguous)
+// with every operand given as the pair (hi, lo) of a float32 value split into
+// two tensor-float32 parts (x = hi + lo exactly; hi is x rounded to TF32,
+// lo = x - hi).  Each product is formed as lo_A hi_B + hi_A lo_B + hi_A hi_B
+// ("3xTF32"); the dropped lo_A lo_B term is below 2^-22 of |x y|.
+//
+// This is the GEMM of the deferred trailing update of the GPTQ sweep
+// (W[:, later] -= E_blk U[blk, later], applied as an update of the pending
+// deferred sums) and of the blocked Cholesky's trailing updates.
+//
+// Design:
+// * One CTA per 128 x 128 output tile (tiles entirely above the diagonal can
+//   be skipped).  Warp 0 / lane 0 issues TMA loads of the four operand tiles
+//   (32 K-values = one 128-byte swizzle row each), three-stage mbarrier
+//   pipeline, 64 KB per stage.  Warp 1 / lane 0 issues tcgen05.mma
+//   (kind::tf32, M = 128, N = 128, K = 8), three per k-step.
+// * The tensor core accumulates G_KF stages (256 K-values) into one of two
+//   TMEM buffers; four epilogue warps add each partial into float32
+//   registers with round-to-nearest while the next period fills the other
+//   buffer.  Long in-TMEM accumulation is avoided because the tensor core's
+//   own accumulation rounds less accurately than an IEEE add.
+// * Every mbarrier wait is bounded; on expiry the CTA records the error flag
+//   that gq_check_device reports, and exits without writing C.
+#include "tc_common.cuh"
+
+namespace gq {
+
+// Bit 0: a bounded wait of this file's kernels gave up.  (Each translation
+// unit has its own device flags: the library is built without relocatable
+// device code.)
+__device__ unsigned int g_gemm_error = 0;
+
+namespace {
+using namespace tc;
+
+constexpr int GM = 128, GN = 128, GK = 32;
+constexpr int G_STAGES = 3;
+constexpr int TILE_A = GM * GK * 4;                  // 16 KB
+constexpr int TILE_B = GN * GK * 4;                  // 16 KB
+constexpr int G_STAGE = 2 * TILE_A + 2 * TILE_B;     // 64 KB
+constexpr int G_SMEM = G_STAGES * G_STAGE + 1024;
+constexpr uint32_t G_TMEM = GN;                      // columns per accumulator buffer
+constexpr int G_KF = 8;                              // stages per TMEM period
+constexpr int G_NWARPS = 6;                          // TMA, MMA, 4 epilogue warps
+
+// Instruction descriptor, kind::tf32: D f32, A and B TF32 (format 2), both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ float tf32_hi(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+__global__ void __launch_bounds__(G_NWARPS * 32, 1)
+    gemm3_kernel(const __grid_constant__ CUtensorMap ahi, const __grid_constant__ CUtensorMap alo,
+                 const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo, float *C,
+                 int64_t ldc, int M, int N, int K, float alpha, float beta, int tri, float *Chi, float *Clo,
+                 int64_t ldcs) {
+    const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
+    if (tri == 1 && n0 > m0 + GM - 1) return;  // tile entirely above the diagonal
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[G_STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[G_STAGES];
+    __shared__ __align__(8) uint64_t tfull[2];
+    __shared__ __align__(8) uint64_t tempty[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ktiles = (K + GK - 1) / GK;
+    const int periods = (ktiles + G_KF - 1) / G_KF;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G_STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(2 * G_TMEM)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tmem_slot;
+    bool ok = true;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kt = 0; kt < ktiles; ++kt) {
+                const int s = kt % G_STAGES;
+                const uint32_t ph = (uint32_t)(kt / G_STAGES) & 1u;
+                if (!mbar_wait(&empty_bar[s], ph ^ 1u) || *(volatile int *)&abort_flag) {
+                    atomicOr(&g_gemm_error, 1u);
+                    abort_flag = 1;
+                    break;
+                }
+                unsigned char *st = smem + s * G_STAGE;
+                mbar_arrive_expect_tx(&full_bar[s], G_STAGE);
+                const int x = kt * GK;
+                tma_load_2d(st, &ahi, x, m0, &full_bar[s]);
+                tma_load_2d(st + TILE_A, &alo, x, m0, &full_bar[s]);
+                tma_load_2d(st + 2 * TILE_A, &bhi, x, n0, &full_bar[s]);
+                tma_load_2d(st + 2 * TILE_A + TILE_B, &blo, x, n0, &full_bar[s]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_tf32(GM, GN);
+            for (int p = 0; p < periods && ok; ++p) {
+                const int b = p & 1;
+                const uint32_t u = (uint32_t)(p >> 1) & 1u;
+                if (!mbar_wait(&tempty[b], u ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const uint32_t acc = tmem + (uint32_t)(b * G_TMEM);
+                const int k_end = (p + 1) * G_KF < ktiles ? (p + 1) * G_KF : ktiles;
+                for (int kt = p * G_KF; kt < k_end; ++kt) {
+                    const int s = kt % G_STAGES;
+                    const uint32_t ph = (uint32_t)(kt / G_STAGES) & 1u;
+                    if (!mbar_wait(&full_bar[s], ph)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t a_hi = smem_u32(smem + s * G_STAGE);
+                    const uint32_t a_lo = a_hi + TILE_A;
+                    const uint32_t b_hi = a_hi + 2 * TILE_A;
+                    const uint32_t b_lo = b_hi + TILE_B;
+#pragma unroll
+                    for (int kk = 0; kk < GK / 8; ++kk) {
+                        // K-major, 128-byte swizzle: 8-row groups 1024 B apart; a
+                        // k-step of 8 TF32 values advances the start by 32 bytes.
+                        const uint32_t off = kk * 32;
+                        const uint64_t dah = smem_desc(a_hi + off, 16, 1024);
+                        const uint64_t dal = smem_desc(a_lo + off, 16, 1024);
+                        const uint64_t dbh = smem_desc(b_hi + off, 16, 1024);
+                        const uint64_t dbl = smem_desc(b_lo + off, 16, 1024);
+                        const uint32_t first = (kt == p * G_KF && kk == 0) ? 0u : 1u;
+                        mma_tf32(acc, dal, dbh, idesc, first);
+                        mma_tf32(acc, dah, dbl, idesc, 1u);
+                        mma_tf32(acc, dah, dbh, idesc, 1u);
+                    }
+                    mma_commit(&empty_bar[s]);
+                }
+                mma_commit(&tfull[b]);
+            }
+            if (!ok) {
+                atomicOr(&g_gemm_error, 1u);
+                abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // Epilogue warps: TMEM lane quarter = warp % 4; each thread owns one row x 128 columns.
+        const int q = warp & 3;
+        float master[GN];
+#pragma unroll
+        for (int i = 0; i < GN; ++i) master[i] = 0.f;
+        for (int p = 0; p < periods; ++p) {
+            const int b = p & 1;
+            const uint32_t u = (uint32_t)(p >> 1) & 1u;
+            if (!mbar_wait(&tfull[b], u)) {
+                ok = false;
+                break;
+            }
+            __syncwarp();
+            fence_after();
+            const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * G_TMEM);
+#pragma unroll
+            for (int ch = 0; ch < GN / 32; ++ch) {
+                float v[32];
+                tmem_ld32(base + ch * 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) master[ch * 32 + i] += v[i];
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+        }
+        if (!ok) {
+            atomicOr(&g_gemm_error, 1u);
+            abort_flag = 1;
+        }
+        __syncwarp();
+        // Epilogue through shared memory (the pipeline stages are idle now): each
+        // warp writes its 32 rows x 128 columns of partial sums there, then
+        // reads C and writes the result one 512-byte row at a time, coalesced.
+        // Row stride 132 floats keeps the float4 accesses free of bank conflicts.
+        float *stage = reinterpret_cast<float *>(smem) + (size_t)q * 32 * (GN + 4);
+        if (ok && periods > 0) {
+#pragma unroll
+            for (int j = 0; j < GN; j += 4)
+                *reinterpret_cast<float4 *>(stage + lane * (GN + 4) + j) =
+                    make_float4(master[j], master[j + 1], master[j + 2], master[j + 3]);
+        }
+        __syncwarp();
+        const int c = n0 + lane * 4;  // this lane's 4 columns of every row
+        const bool full4 = (c + 3 < N) && (ldc % 4) == 0 && ((uintptr_t)C % 16) == 0 &&
+                           (!Chi || ((ldcs % 4) == 0 && ((uintptr_t)Chi % 16) == 0 && ((uintptr_t)Clo % 16) == 0));
+        if (ok && periods > 0) {
+            for (int rr0 = 0; rr0 < 32; rr0 += 8) {
+                float4 old[8];
+                if (beta != 0.f) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int r = m0 + q * 32 + rr0 + u;
+                        old[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (r < M) {
+                            const float *cp = C + (int64_t)r * ldc + c;
+                            if (full4) old[u] = *reinterpret_cast<const float4 *>(cp);
+                            else {
+                                if (c < N) old[u].x = cp[0];
+                                if (c + 1 < N) old[u].y = cp[1];
+                                if (c + 2 < N) old[u].z = cp[2];
+                                if (c + 3 < N) old[u].w = cp[3];
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int rr = rr0 + u, r = m0 + q * 32 + rr;
+                    if (r >= M || c >= N) continue;
+                    const float4 a = *reinterpret_cast<const float4 *>(stage + rr * (GN + 4) + lane * 4);
+                    float v[4] = {alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w};
+                    if (beta != 0.f) {
+                        v[0] = fmaf(beta, old[u].x, v[0]);
+                        v[1] = fmaf(beta, old[u].y, v[1]);
+                        v[2] = fmaf(beta, old[u].z, v[2]);
+                        v[3] = fmaf(beta, old[u].w, v[3]);
+                    }
+                    float *cp = C + (int64_t)r * ldc + c;
+                    float h[4], l[4];
+                    if (Chi) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            h[e] = tf32_hi(v[e]);
+                            l[e] = v[e] - h[e];
+                        }
+                    }
+                    if (full4) {
+                        *reinterpret_cast<float4 *>(cp) = make_float4(v[0], v[1], v[2], v[3]);
+                        if (Chi) {
+                            *reinterpret_cast<float4 *>(Chi + (int64_t)r * ldcs + c) = make_float4(h[0], h[1], h[2], h[3]);
+                            *reinterpret_cast<float4 *>(Clo + (int64_t)r * ldcs + c) = make_float4(l[0], l[1], l[2], l[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (c + e < N) {
+                                cp[e] = v[e];
+                                if (Chi) {
+                                    Chi[(int64_t)r * ldcs + c + e] = h[e];
+                                    Clo[(int64_t)r * ldcs + c + e] = l[e];
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * G_TMEM) : "memory");
+    }
+}
+
+__global__ void split_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t lds,
+                             float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
+    const int64_t n = rows * cols;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i % cols;
+        const float x = src[r * lds + c];
+        const float h = tf32_hi(x);
+        hi[r * ldd + c] = h;
+        lo[r * ldd + c] = x - h;
+    }
+}
+
+bool make_map(CUtensorMap *map, const float *base, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t gstride[1] = {(cuuint64_t)ld * 4};
+    cuuint32_t box[2] = {(cuuint32_t)GK, (cuuint32_t)box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void *)base, gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+unsigned int gemm_read_and_clear_error() {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(v)) != cudaSuccess) return ~0u;
+    const unsigned int zero = 0;
+    if (v) cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(zero));
+    return v;
+}
+
+bool gemm3_supported(const void *p, int64_t ld) { return ((uintptr_t)p % 16) == 0 && (ld % 4) == 0; }
+
+cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi, const float *Alo, int64_t lda,
+                  const float *Bhi, const float *Blo, int64_t ldb, float beta, float *C, int64_t ldc, int tri,
+                  float *Chi, float *Clo, int64_t ldcs, cudaStream_t s) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    if (K <= 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemm3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap mah, mal, mbh, mbl;
+    if (!make_map(&mah, Ahi, K, M, lda, GM) || !make_map(&mal, Alo, K, M, lda, GM) ||
+        !make_map(&mbh, Bhi, K, N, ldb, GN) || !make_map(&mbl, Blo, K, N, ldb, GN))
+        return cudaErrorInvalidValue;
+    dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
+    gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta,
+                                                    tri, Chi, Clo, ldcs);
+    return cudaGetLastError();
+}
+
+cudaError_t split_tf32(const float *src, int64_t rows, int64_t cols, int64_t lds, float *hi, float *lo, int64_t ldd,
+                       cudaStream_t s) {
+    const int64_t n = rows * cols;
+    if (n <= 0) return cudaSuccess;
+    int64_t g = (n + 255) / 256;
+    if (g > 148 * 16) g = 148 * 16;
+    split_kernel<<<(unsigned)g, 256, 0, s>>>(src, rows, cols, lds, hi, lo, ldd);
+    return cudaGetLastError();
+}
+
+}  // namespace gq

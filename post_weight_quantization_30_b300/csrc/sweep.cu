@@ -5,11 +5,12 @@
 // of block b as updated by every earlier column are
 //     W_blk + ΔW[:, <s] F[<s, blk] Uinv_b,   Uinv_b = F[blk, blk]^-1 = U[blk, blk],
 // with ΔW = W - Ŵ.  V = F blockdiag(Uinv_b) (rows above each diagonal block) is
-// formed once, so the buffer D (rows x cols float32, in the workspace) holds,
-// for a block not yet swept, sum over earlier blocks of ΔW_prev V_prev,blk,
-// accumulated by the deferred trailing GEMMs; once a block is swept its
-// columns of D hold ΔW.  Inside the block the ordinary per-column update runs
-// with Uinv_b.
+// formed once, transposed and split into TF32 parts (VThi + VTlo), the operand
+// layout of the tensor-core GEMM.  The buffer D (rows x cols float32, in the
+// workspace) holds, for a block not yet swept, sum over earlier blocks of
+// ΔW_prev V_prev,blk, accumulated by the deferred trailing GEMMs; once a block
+// is swept its columns of D hold the TF32 hi part of ΔW and those of DL the lo
+// part.  Inside the block the ordinary per-column update runs with Uinv_b.
 //
 // Kernel layout.  One CTA = 32 output rows x one block, 16 warps x 2 rows; 16
 // lanes per row, each owning 8 consecutive block columns in registers.  Per
@@ -89,11 +90,17 @@ __device__ __forceinline__ float rint_div(float w, float s, float inv_s) {
     return rintf(__fdiv_rn(w, s));
 }
 
+__device__ __forceinline__ float tf32_hi(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
 template <int BITS, typename TW>
 __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ W, int64_t rows, int64_t cols,
                                                          int64_t c0, int bw, const float *__restrict__ Uinv,
                                                          const float *__restrict__ F, const uint8_t *__restrict__ dead,
-                                                         int group, float *__restrict__ D,
+                                                         int group, float *__restrict__ D, float *__restrict__ DL,
                                                          int32_t *__restrict__ qweight, float *__restrict__ scales,
                                                          int32_t *__restrict__ qzeros, uint8_t *__restrict__ codes,
                                                          float *__restrict__ W_hat, float *__restrict__ row_err) {
@@ -217,9 +224,18 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
             load8<TW>(W + row * cols + c0 + cl, w0);
 #pragma unroll
             for (int c = 0; c < CPL; ++c) dw[c] = (dmask[c] ? 0.f : w0[c]) - wq[c];
+            // ΔW as its TF32 split: the operand of the deferred-update GEMMs.
+            float dh[CPL];
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) dh[c] = tf32_hi(dw[c]);
             float *dp = D + row * cols + c0 + cl;
-            *reinterpret_cast<float4 *>(dp) = make_float4(dw[0], dw[1], dw[2], dw[3]);
-            *reinterpret_cast<float4 *>(dp + 4) = make_float4(dw[4], dw[5], dw[6], dw[7]);
+            float *lp = DL + row * cols + c0 + cl;
+            *reinterpret_cast<float4 *>(dp) = make_float4(dh[0], dh[1], dh[2], dh[3]);
+            *reinterpret_cast<float4 *>(dp + 4) = make_float4(dh[4], dh[5], dh[6], dh[7]);
+            *reinterpret_cast<float4 *>(lp) =
+                make_float4(dw[0] - dh[0], dw[1] - dh[1], dw[2] - dh[2], dw[3] - dh[3]);
+            *reinterpret_cast<float4 *>(lp + 4) =
+                make_float4(dw[4] - dh[4], dw[5] - dh[5], dw[6] - dh[6], dw[7] - dh[7]);
             if (W_hat) {
                 float *hp = W_hat + row * cols + c0 + cl;
                 *reinterpret_cast<float4 *>(hp) = make_float4(wq[0], wq[1], wq[2], wq[3]);
@@ -252,20 +268,22 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
     }
 }
 
-// V[:, blk] = F[:, blk] Uinv_b for the rows above each diagonal block: the
-// deferred update of block b from the earlier columns is then sum ΔW_prev V_prev,b.
-// One CTA per (128-row tile, block column), 256 threads, 8 x 8 outputs each.
-// A CTA reads its whole input tile before writing the same tile, and tiles are
-// disjoint, so V may alias F.
-__global__ void __launch_bounds__(256) premultiply_kernel(const float *F, int64_t cols, int block,
-                                                          const float *__restrict__ Uinv, float *V) {
-    __shared__ __align__(16) float As[16][128 + 4];
-    __shared__ __align__(16) float Bs[16][128 + 4];
+// VT[s0 + n][m] = sum_k Uinv_b[k][n] F[m][s0 + k] for m < s0: the transpose of
+// V[:, blk_b] = F[:, blk_b] Uinv_b above each diagonal block b, so that the
+// deferred update of block b from the earlier columns is ΔW_prev V_prev,b with
+// V given K-contiguous, and written as its TF32 split.  One CTA per
+// (128-column m-tile, block b), 256 threads, 8 x 8 outputs each; stores run
+// along m (coalesced).
+__global__ void __launch_bounds__(256) premultiply_t_kernel(const float *__restrict__ F, int64_t cols, int block,
+                                                            const float *__restrict__ Uinv, float *__restrict__ VThi,
+                                                            float *__restrict__ VTlo) {
+    __shared__ __align__(16) float As[16][128 + 4];  // As[k][n] = Uinv_b[k][n]
+    __shared__ __align__(16) float Bs[16][128 + 4];  // Bs[k][m] = F[m][s0 + k]
     const int b = blockIdx.y;
     const int64_t s0 = (int64_t)b * block;
     const int bw = (int)((cols - s0) < block ? (cols - s0) : block);
     const int64_t m0 = (int64_t)blockIdx.x * 128;
-    if (m0 >= s0) return;  // only rows above the diagonal block
+    if (m0 >= s0) return;  // only columns left of the diagonal block
     const float *Ub = Uinv + s0 * block;  // bw x bw, row stride bw
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
     float acc[8][8];
@@ -275,11 +293,11 @@ __global__ void __launch_bounds__(256) premultiply_kernel(const float *F, int64_
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
     for (int k0 = 0; k0 < bw; k0 += 16) {
         for (int idx = threadIdx.x; idx < 16 * 128; idx += 256) {
-            const int r = idx / 16, k = idx % 16;  // A: F[m0 + r][s0 + k0 + k]
-            const int64_t gr = m0 + r;
-            As[k][r] = (gr < s0 && k0 + k < bw) ? F[gr * cols + s0 + k0 + k] : 0.f;
-            const int kk = idx / 128, n = idx % 128;  // B: Uinv_b[k0 + kk][n]
-            Bs[kk][n] = (k0 + kk < bw && n < bw) ? Ub[(int64_t)(k0 + kk) * bw + n] : 0.f;
+            const int kk = idx / 128, n = idx % 128;
+            As[kk][n] = (k0 + kk < bw && n < bw) ? Ub[(int64_t)(k0 + kk) * bw + n] : 0.f;
+            const int m = idx / 16, k = idx % 16;
+            const int64_t gm = m0 + m;
+            Bs[k][m] = (gm < s0 && k0 + k < bw) ? F[gm * cols + s0 + k0 + k] : 0.f;
         }
         __syncthreads();
 #pragma unroll
@@ -301,12 +319,16 @@ __global__ void __launch_bounds__(256) premultiply_kernel(const float *F, int64_
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int64_t m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
-        if (m >= s0) continue;
+        const int n = (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+        if (n >= bw) continue;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int n = (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
-            if (n < bw) V[m * cols + s0 + n] = acc[i][j];
+            const int64_t m = m0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+            if (m >= s0) continue;
+            const float v = acc[i][j];
+            const float h = tf32_hi(v);
+            VThi[(s0 + n) * cols + m] = h;
+            VTlo[(s0 + n) * cols + m] = v - h;
         }
     }
 }
@@ -345,7 +367,8 @@ __global__ void __launch_bounds__(128) block_inverse_kernel(const float *__restr
 
 template <int BITS, typename TW>
 cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, int bw, const float *Uinv,
-                         const float *F, const uint8_t *dead, int group, float *D, int32_t *qweight, float *scales,
+                         const float *F, const uint8_t *dead, int group, float *D, float *DL, int32_t *qweight,
+                         float *scales,
                          int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s) {
     const size_t smem = sizeof(SweepSmem);
     static bool attr_set = false;  // per template instance
@@ -355,7 +378,7 @@ cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, in
         attr_set = true;
     }
     sweep_kernel<BITS, TW><<<(unsigned)((rows + ROWS - 1) / ROWS), NTHREADS, smem, s>>>(
-        W, rows, cols, c0, bw, Uinv, F, dead, group, D, qweight, scales, qzeros, codes, W_hat, row_err);
+        W, rows, cols, c0, bw, Uinv, F, dead, group, D, DL, qweight, scales, qzeros, codes, W_hat, row_err);
     return cudaGetLastError();
 }
 
@@ -374,25 +397,26 @@ cudaError_t block_inverses(const float *F, int64_t cols, int block, float *Uinv,
     return cudaGetLastError();
 }
 
-cudaError_t premultiply(const float *F, int64_t cols, int block, const float *Uinv, float *V, cudaStream_t s) {
+cudaError_t premultiply_t(const float *F, int64_t cols, int block, const float *Uinv, float *VThi, float *VTlo,
+                          cudaStream_t s) {
     const int64_t nblk = (cols + block - 1) / block;
     if (nblk < 2) return cudaSuccess;
     dim3 grid((unsigned)(((nblk - 1) * block + 127) / 128), (unsigned)nblk);
-    premultiply_kernel<<<grid, 256, 0, s>>>(F, cols, block, Uinv, V);
+    premultiply_t_kernel<<<grid, 256, 0, s>>>(F, cols, block, Uinv, VThi, VTlo);
     return cudaGetLastError();
 }
 
 cudaError_t sweep_block_launch(const void *W, bool w_bf16, int64_t rows, int64_t cols, int64_t c0, int bw,
                                const float *Uinv_blk, const float *F, const uint8_t *dead, int bits, int group,
-                               float *D, int32_t *qweight, float *scales, int32_t *qzeros, uint8_t *codes,
+                               float *D, float *DL, int32_t *qweight, float *scales, int32_t *qzeros, uint8_t *codes,
                                float *W_hat, float *row_err, cudaStream_t s) {
 #define GQ_SWEEP_CASE(B)                                                                                         \
     if (bits == B) {                                                                                             \
         if (w_bf16)                                                                                              \
             return launch_sweep<B, __nv_bfloat16>((const __nv_bfloat16 *)W, rows, cols, c0, bw, Uinv_blk, F, dead, \
-                                                  group, D, qweight, scales, qzeros, codes, W_hat, row_err, s);   \
-        return launch_sweep<B, float>((const float *)W, rows, cols, c0, bw, Uinv_blk, F, dead, group, D, qweight,  \
-                                      scales, qzeros, codes, W_hat, row_err, s);                                 \
+                                                  group, D, DL, qweight, scales, qzeros, codes, W_hat, row_err, s); \
+        return launch_sweep<B, float>((const float *)W, rows, cols, c0, bw, Uinv_blk, F, dead, group, D, DL,       \
+                                      qweight, scales, qzeros, codes, W_hat, row_err, s);                        \
     }
     GQ_SWEEP_CASE(2)
     GQ_SWEEP_CASE(3)
