@@ -80,49 +80,65 @@ __global__ void reverse_damp_kernel(const float *__restrict__ H, int64_t cols, f
 constexpr int DIAG_THREADS = 256;
 constexpr int SP = 32;           // sub-panel width
 constexpr int LDA = NB + 4;      // shared-memory row stride (floats)
-constexpr size_t DIAG_SMEM = (2 * NB * LDA + 2 * SP * LDA + 3 * SP * SP + SP) * sizeof(float);
+constexpr size_t DIAG_SMEM = (2 * NB * LDA + 2 * SP * LDA + 3 * SP * SP + 3 * SP) * sizeof(float);
 
 // Lane i holds row i of a 32 x 32 symmetric block (entries k <= i) and ends
 // with row i of its lower Cholesky factor; `rinv` of lane i ends as 1 / L_ii.
-// The steps are unrolled by template recursion so that every index into `a`
-// is a compile-time constant (the array stays in registers).
+// Step J: the pivot comes by shuffle from lane J; the new column J of L is
+// written once to a shared-memory buffer (two alternating buffers) and read
+// back by every lane with float4 broadcast loads for the rank-1 update.  The
+// steps are unrolled by template recursion so that every index into `a` is a
+// compile-time constant (the array stays in registers).
 template <int J>
 struct CholStep {
     static __device__ __forceinline__ void run(float (&a)[SP], float &rinv, int lane, int64_t gcol0,
-                                               DeviceStatus *st) {
+                                               DeviceStatus *st, float *colbuf) {
         const unsigned full = 0xffffffffu;
         const float d = __shfl_sync(full, a[J], J);
         if (lane == 0 && !(d > 0.f)) atomicMin(&st->bad_pivot, (unsigned long long)(gcol0 + J));
         const float r = rsqrtf(d);
         if (lane == J) rinv = r;
         a[J] = (lane > J) ? a[J] * r : (lane == J ? d * r : a[J]);
+        if (J + 1 < SP) {
+            float *cb = colbuf + (J & 1) * SP;
+            cb[lane] = a[J];
+            __syncwarp();
 #pragma unroll
-        for (int k = J + 1; k < SP; ++k) {
-            const float lkj = __shfl_sync(full, a[J], k);
-            a[k] = (lane >= k) ? fmaf(-a[J], lkj, a[k]) : a[k];
+            for (int k4 = ((J + 1) / 4) * 4; k4 < SP; k4 += 4) {
+                const float4 c4 = *reinterpret_cast<const float4 *>(cb + k4);
+                const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = k4 + u;
+                    if (k > J) a[k] = (lane >= k) ? fmaf(-a[J], cv[u], a[k]) : a[k];
+                }
+            }
         }
-        CholStep<J + 1>::run(a, rinv, lane, gcol0, st);
+        CholStep<J + 1>::run(a, rinv, lane, gcol0, st, colbuf);
     }
 };
 template <>
 struct CholStep<SP> {
-    static __device__ __forceinline__ void run(float (&)[SP], float &, int, int64_t, DeviceStatus *) {}
+    static __device__ __forceinline__ void run(float (&)[SP], float &, int, int64_t, DeviceStatus *, float *) {}
 };
 
 // Column `lane` of the inverse of the 32 x 32 lower factor stored at L (row
-// stride LDA), dinv[i] = 1 / L_ii: y_i = (delta_i,lane - sum_{k<i} L_ik y_k) dinv_i.
-// Written transposed: YT[lane][i] = (L^-1)_{i,lane}.
+// stride LDA, 16-byte aligned rows), dinv[i] = 1 / L_ii:
+// y_i = (delta_i,lane - sum_{k<i} L_ik y_k) dinv_i, rows of L read as float4
+// broadcasts.  Written transposed: YT[lane][i] = (L^-1)_{i,lane}.
 __device__ __forceinline__ void warp_trinv32(const float *L, const float *dinv, float *YT, int lane) {
     float y[SP];
 #pragma unroll
     for (int i = 0; i < SP; ++i) {
         float s0 = (lane == i) ? 1.f : 0.f, s1 = 0.f;
 #pragma unroll
-        for (int k = 0; k + 1 < i; k += 2) {
-            s0 = fmaf(-L[i * LDA + k], y[k], s0);
-            s1 = fmaf(-L[i * LDA + k + 1], y[k + 1], s1);
+        for (int k4 = 0; k4 < i; k4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(L + i * LDA + k4);
+            if (k4 + 0 < i) s0 = fmaf(-l4.x, y[k4 + 0], s0);
+            if (k4 + 1 < i) s1 = fmaf(-l4.y, y[k4 + 1], s1);
+            if (k4 + 2 < i) s0 = fmaf(-l4.z, y[k4 + 2], s0);
+            if (k4 + 3 < i) s1 = fmaf(-l4.w, y[k4 + 3], s1);
         }
-        if (i & 1) s0 = fmaf(-L[i * LDA + i - 1], y[i - 1], s0);
         y[i] = (s0 + s1) * dinv[i];
     }
 #pragma unroll
@@ -139,6 +155,7 @@ __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restr
     float *YT = XT + SP * LDA;     // [SP][LDA]: current diagonal inverse, transposed
     float *T = YT + SP * LDA;      // [3][SP][SP]: partial sums of the inverse assembly
     float *dinv = T + 3 * SP * SP; // [SP]
+    float *colbuf = dinv + SP;     // [2][SP]: pivot column broadcast of the warp factorization
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
 
     // Load: 16 float4 per thread, all issued before any shared-memory store.
@@ -181,7 +198,7 @@ __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restr
             float a[SP], rinv = 0.f;
 #pragma unroll
             for (int k = 0; k < SP; ++k) a[k] = (k <= lane) ? A[(c0 + lane) * LDA + c0 + k] : 0.f;
-            CholStep<0>::run(a, rinv, lane, k0 + c0, st);
+            CholStep<0>::run(a, rinv, lane, k0 + c0, st, colbuf);
 #pragma unroll
             for (int k = 0; k < SP; ++k)
                 if (k <= lane) A[(c0 + lane) * LDA + c0 + k] = a[k];
