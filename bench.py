@@ -239,7 +239,7 @@ def run_ours(args, rank: int, world: int):
     h_avg_s = statistics.mean(h_ms) / 1e3
     achieved = flops / h_avg_s / 1e12
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    traffic = _read_traffic()
+    traffic = _read_traffic(args.workload)
 
     result = {
         "metric": METRIC,
@@ -277,14 +277,24 @@ def run_ours(args, rank: int, world: int):
     return result
 
 
-def _read_traffic():
-    """DRAM bytes per launch of the Hessian kernel from the committed ncu summary, if current."""
+def _read_traffic(workload: str):
+    """DRAM bytes per launch of the Hessian kernel from the committed ncu summary,
+    if it was taken on this workload and the kernel source is unchanged since."""
+    import hashlib
+
     p = os.path.join(ROOT, "profiles", "hessian_traffic.json")
     try:
         with open(p) as f:
-            return json.load(f).get("dram_bytes_per_launch")
+            rec = json.load(f)
+        src = b"".join(open(os.path.join(ROOT, "post_weight_quantization_30_b300", "csrc", n), "rb").read()
+                       for n in ("hessian_tc.cu", "tc_common.cuh"))
     except (OSError, ValueError):
         return None
+    if hashlib.sha256(src).hexdigest() != rec.get("kernel_source_sha256"):
+        return None
+    if not str(rec.get("workload", "")).startswith(workload):
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 # ----------------------------------------------------------------- oracle (CPU)
