@@ -107,14 +107,13 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def launches_per_step(rows: int, cols: int, block: int) -> int:
-    """Kernels of libgq launched by one step (Hessian + factor + sweep)."""
-    nb_panel = 128
-    panels = -(-cols // nb_panel)
-    factor = 2 + panels + 2 * (panels - 1) + 1  # diag sum, reversal; diagonal block per panel; solve + update but last; finalize
-    nblk = -(-cols // block)
-    sweep = 2 + nblk + (nblk - 1)  # block inverses, premultiply; one sweep per block; one deferred GEMM per split
-    return 1 + factor + sweep
+def describe_inputs(spec) -> str:
+    """The synthetic recipe of the workload, for the JSON line."""
+    x = spec.X
+    dist = {"t": f"Student-t({x.nu:g})", "normal": "N(0,1)", "absnormal_x_normal": "|N(0,1)|*N(0,1)"}[x.dist]
+    out = f" with {x.n_outliers} outlier channels x{x.outlier_scale:g}" if x.n_outliers else ""
+    return (f"synthetic, seeded: X {x.rows}x{x.cols} {x.dtype} {dist}{out}; "
+            f"W {spec.rows}x{spec.cols} {spec.W.dtype} N(0,{spec.W.std:g}^2)")
 
 
 # --------------------------------------------------------------------------- ours
@@ -139,8 +138,20 @@ def run_ours(args, rank: int, world: int):
     R, C, N = spec.rows, spec.cols, spec.n
     H = torch.zeros((C, C), dtype=torch.float32, device=dev)
     ws = torch.empty(gq.lib.gptq_quantize_layer_workspace_size(R, C, spec.block), dtype=torch.uint8, device=dev)
-    out = gq._lib._sweep_outputs(R, C, spec.bits, spec.group, dev, codes=False, W_hat=False, row_err=False)
+    r = spec.eora_rank
+    # Ŵ is an output only when EoRA needs it (the error it compensates is W - Ŵ).
+    out = gq._lib._sweep_outputs(R, C, spec.bits, spec.group, dev, codes=False, W_hat=r > 0, row_err=False)
+    if r:
+        dW = torch.empty((R, C), dtype=torch.float32, device=dev)
+        ews = torch.empty(gq.lib.eora_compensate_workspace_size(R, C, r), dtype=torch.uint8, device=dev)
+        eout = dict(A=torch.empty((r, C), dtype=torch.float32, device=dev),
+                    B=torch.empty((R, r), dtype=torch.float32, device=dev),
+                    sigma=torch.empty(r, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream(dev)
+
+    def eora_part(Wsrc):
+        gq.gptq_weight_error(Wsrc, out["W_hat"], out=dW)
+        gq.eora_compensate(dW, H, r, workspace=ews, out=eout)
 
     def step(ev=None):
         H.zero_()
@@ -150,6 +161,8 @@ def run_ours(args, rank: int, world: int):
         if ev is not None:
             ev[1].record(stream)
         gq.gptq_quantize_layer(W, H, spec.bits, spec.group, spec.block, spec.damp, workspace=ws, out=out)
+        if r:
+            eora_part(W)
 
     for _ in range(args.warmup):
         step()
@@ -164,6 +177,7 @@ def run_ours(args, rank: int, world: int):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
+        launches0 = gq.lib.gq_kernel_launches()
         clocks.mark("start")
         start.record(stream)
         for k in range(args.steps):
@@ -173,6 +187,7 @@ def run_ours(args, rank: int, world: int):
         if world > 1:
             dist.barrier()
         clocks.mark("stop")
+        launches = gq.lib.gq_kernel_launches() - launches0
         time.sleep(0.15)
     ms_total = start.elapsed_time(stop)
     h_ms = [a.elapsed_time(b) for a, b in hev]
@@ -193,6 +208,9 @@ def run_ours(args, rank: int, world: int):
 
     reps = 3
     acc = {"hessian": 0.0, "factor": 0.0, "sweep": 0.0}
+    if r:
+        acc["eora"] = 0.0
+        e.append(torch.cuda.Event(enable_timing=True))
     for _ in range(reps):
         H.zero_()
         e[0].record(stream)
@@ -204,18 +222,27 @@ def run_ours(args, rank: int, world: int):
                                 ctypes.c_void_p(stream.cuda_stream), ctypes.byref(info))
         assert st == 0, st
         e[2].record(stream)
-        gq.gptq_sweep(W, F, dead, spec.bits, spec.group, spec.block, codes=False, W_hat=False, row_err=False,
-                      workspace=sws)
+        so = gq.gptq_sweep(W, F, dead, spec.bits, spec.group, spec.block, codes=False, W_hat=r > 0, row_err=False,
+                           workspace=sws)
         e[3].record(stream)
+        if r:
+            gq.gptq_weight_error(W, so["W_hat"], out=dW)
+            gq.eora_compensate(dW, H, r, workspace=ews, out=eout)
+            e[4].record(stream)
         torch.cuda.synchronize(dev)
         acc["hessian"] += e[0].elapsed_time(e[1])
         acc["factor"] += e[1].elapsed_time(e[2])
         acc["sweep"] += e[2].elapsed_time(e[3])
+        if r:
+            acc["eora"] += e[3].elapsed_time(e[4])
     phase = {k: v / reps for k, v in acc.items()}
 
     # End to end through the public API from pinned host buffers, every step:
     # H2D of X and W, the whole path, D2H of the packed result.
-    res_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items() if v is not None}
+    results = {k: v for k, v in out.items() if v is not None and k != "W_hat"}
+    if r:
+        results.update(eora_A=eout["A"], eora_B=eout["B"])
+    res_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in results.items()}
     h2d = x_host.numel() * 2 + w_host.numel() * 2
     d2h = sum(v.numel() * v.element_size() for v in res_host.values())
     Xd = torch.empty_like(X)
@@ -229,8 +256,10 @@ def run_ours(args, rank: int, world: int):
         H.zero_()
         gq.gptq_hessian_accumulate(H, Xd)
         gq.gptq_quantize_layer(Wd, H, spec.bits, spec.group, spec.block, spec.damp, workspace=ws, out=out)
+        if r:
+            eora_part(Wd)
         for k, v in res_host.items():
-            v.copy_(out[k], non_blocking=True)
+            v.copy_(results[k], non_blocking=True)
         torch.cuda.synchronize(dev)
     e2e_s = (time.perf_counter() - t0) / e2e_steps
 
@@ -252,8 +281,8 @@ def run_ours(args, rank: int, world: int):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16/f32",
-        "data": "synthetic (seeded; Student-t(4) activations with 41 outlier channels x30, N(0,0.02^2) weights)",
+        "dtype": "bf16 x bf16 -> f32 (Hessian); f32 (factor, sweep, 3xTF32 GEMMs" + (", EoRA)" if r else ")"),
+        "data": describe_inputs(spec),
         "config": {
             "workload": args.workload, "rows": R, "cols": C, "tokens": N, "bits": spec.bits, "group": spec.group,
             "block": spec.block, "damp": spec.damp, "x_dtype": spec.X.dtype, "w_dtype": spec.W.dtype,
@@ -268,7 +297,7 @@ def run_ours(args, rank: int, world: int):
             "flops_per_launch": flops, "traffic": traffic,
         },
         "e2e": {"value": round(e2e_s, 6), "unit": "s/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step(R, C, spec.block) * args.steps,
+        "gpu_launches": int(launches),
         "clocks": clocks.summary(),
         "input_generation_s": round(gen_s, 1),
     }

@@ -54,6 +54,10 @@ typedef enum { GQ_F32 = 0, GQ_BF16 = 1 } gq_dtype;
 /* Version of this ABI (bumped on any signature change). */
 int gq_abi_version(void);
 
+/* Number of kernel launches this library has enqueued since it was loaded,
+ * all devices and streams (a monotonic host-side counter; for accounting). */
+unsigned long long gq_kernel_launches(void);
+
 /* Human-readable name of a status code (static string; never NULL). */
 const char *gq_status_string(gq_status s);
 
@@ -150,6 +154,18 @@ gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t 
                               float *scales, int32_t *qzeros, uint8_t *codes, float *W_hat,
                               float *row_err, void *ws, size_t ws_bytes, gq_stream_t stream,
                               int64_t *info);
+
+/*
+ * The compression error that EoRA compensates, dW = W - Ŵ ([EoRA-blog]
+ * "Bucear en el espacio propio en busca de un adaptador").
+ *
+ *   W      rows x cols, type wt (the original weights), read only.
+ *   W_hat  rows x cols float32 (e.g. the W_hat output of gptq_quantize_layer).
+ *   dW     rows x cols float32 output.
+ * Asynchronous.
+ */
+gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *W_hat, float *dW,
+                            gq_stream_t stream);
 
 /*
  * EoRA compensation of the quantization error ([EoRA-blog] "Bucear en el

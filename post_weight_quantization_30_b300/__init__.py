@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     gptq_quantize_layer_noalloc,
     gptq_sweep,
     gptq_unpack,
+    gptq_weight_error,
     gq_check_device,
     lib,
 )

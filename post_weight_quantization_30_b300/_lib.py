@@ -37,6 +37,7 @@ STATUS = {0: "GQ_OK", -1: "GQ_EINVAL", -2: "GQ_ENOTPD", -3: "GQ_EUNSUPPORTED", -
 # name -> (restype, argtypes); the full exported surface of include/gq.h
 SIGNATURES = {
     "gq_abi_version": (_i, []),
+    "gq_kernel_launches": (ctypes.c_ulonglong, []),
     "gq_status_string": (ctypes.c_char_p, [_i]),
     "gq_check_device": (_i, [_p]),
     "gptq_hessian_accumulate": (_i, [_p, _i64, _p, _i, _i64, _i64, _p]),
@@ -49,6 +50,7 @@ SIGNATURES = {
                                  ctypes.POINTER(_i64)]),
     "gptq_quantize_layer_noalloc": (_i, [_p, _i, _i64, _i64, _p, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p,
                                          ctypes.POINTER(_i64)]),
+    "gptq_weight_error": (_i, [_p, _i, _i64, _i64, _p, _p, _p]),
     "eora_compensate_workspace_size": (_sz, [_i64, _i64, _i]),
     "eora_compensate": (_i, [_p, _i64, _i64, _p, _i, _p, _p, _p, _p, _sz, _p, ctypes.POINTER(_i64)]),
     "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
@@ -202,6 +204,17 @@ def gptq_quantize_layer_noalloc(W: torch.Tensor, H: torch.Tensor, bits: int, gro
                                            _ptr(o.get("row_err")), _stream(W.device), ctypes.byref(info)),
            "gptq_quantize_layer_noalloc", info.value)
     return o
+
+
+def gptq_weight_error(W: torch.Tensor, W_hat: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """dW = W - W_hat (float32), the error EoRA compensates."""
+    _need_cuda(W, W_hat)
+    rows, cols = W.shape
+    W = W.contiguous()
+    dW = out if out is not None else torch.empty((rows, cols), dtype=torch.float32, device=W.device)
+    _check(lib.gptq_weight_error(_ptr(W), _dtype_code(W), rows, cols, _ptr(W_hat.contiguous()), _ptr(dW),
+                                 _stream(W.device)), "gptq_weight_error")
+    return dW
 
 
 def eora_compensate(dW: torch.Tensor, H: torch.Tensor, r: int, workspace: torch.Tensor | None = None,

@@ -1,11 +1,18 @@
 // C ABI of libgq (declared in include/gq.h): argument validation, workspace
 // layout and the order of the stream-ordered launches.
+#include <atomic>
 #include <climits>
 #include <cstring>
 
 #include "common.cuh"
 
 using namespace gq;
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void gq::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 
@@ -79,6 +86,8 @@ cudaError_t sweep_range(const SweepCtx &c, int64_t a, int64_t b) {
 extern "C" {
 
 int gq_abi_version(void) { return 1; }
+
+unsigned long long gq_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char *gq_status_string(gq_status s) {
     switch (s) {
@@ -208,6 +217,13 @@ gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t 
     if (st != GQ_OK) return st;
     return gptq_sweep(W, wt, rows, cols, F, dead, bits, group, block, qweight, scales, qzeros, codes, W_hat, row_err, p,
                       sweep_ws_bytes(rows, cols, block), stream);
+}
+
+gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *W_hat, float *dW,
+                            gq_stream_t stream) {
+    if (wt != GQ_F32 && wt != GQ_BF16) return GQ_EUNSUPPORTED;
+    if (!W || !W_hat || !dW || rows <= 0 || cols <= 0) return GQ_EINVAL;
+    return weight_error_launch(W, wt == GQ_BF16, rows * cols, W_hat, dW, cs(stream)) == cudaSuccess ? GQ_OK : GQ_ECUDA;
 }
 
 size_t eora_compensate_workspace_size(int64_t rows, int64_t cols, int r) {

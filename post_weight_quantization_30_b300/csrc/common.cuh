@@ -20,6 +20,9 @@
 
 namespace gq {
 
+// Counts one kernel launch enqueued by the library (host side).
+void count_launch();
+
 // Device status block kept in the workspace.  `bad_pivot` holds the first input
 // column (in original index order) whose Cholesky pivot was not positive, or
 // INT64_MAX when every pivot was fine.
@@ -116,6 +119,9 @@ size_t eora_workspace_bytes(int64_t rows, int64_t cols, int r);
 int eora_subspace_width(int64_t rows, int64_t cols, int r);
 cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H, int r, float *A, float *B,
                      float *sigma, void *ws, cudaStream_t s, unsigned long long *bad_pivot_host);
+
+// dW = W - W_hat, n elements (W float32 or bf16).
+cudaError_t weight_error_launch(const void *W, bool w_bf16, int64_t n, const float *W_hat, float *dW, cudaStream_t s);
 
 cudaError_t pack_launch(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight,
                         cudaStream_t s);

@@ -315,9 +315,11 @@ unsigned grid1d(int64_t n) {
 cudaError_t orthonormalize(const EoraWs &w, int k, int64_t cols, DeviceStatus *qst, cudaStream_t s) {
     for (int pass = 0; pass < 2; ++pass) {
         normalize_rows_kernel<<<k, 256, 0, s>>>(w.ZT, cols);
+        count_launch();
         cudaError_t e = sgemm_splitk(k, k, cols, w.ZT, cols, false, w.ZT, cols, true, w.Gm, w.part, SPLITK, s);
         if (e != cudaSuccess) return e;
         shift_gram_kernel<<<1, 128, 0, s>>>(w.Gm, k);
+        count_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         e = cholesky_lower_inplace(w.Gm, k, qst, w.Linv, s);
         if (e != cudaSuccess) return e;
@@ -349,6 +351,7 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     if ((e = cudaMemsetAsync(qst, 0xFF, sizeof(DeviceStatus), s)) != cudaSuccess) return e;
     if ((e = factor_prepare(H, cols, 0.f, w.F, w.dead, w.st, s)) != cudaSuccess) return e;
     dead_to_pivot_kernel<<<grid1d(cols), 256, 0, s>>>(w.dead, cols, w.st);
+    count_launch();
     if ((e = cholesky_lower_inplace(w.F, cols, w.st, w.Linv, s)) != cudaSuccess) return e;
     if ((e = factor_finalize(w.F, cols, s)) != cudaSuccess) return e;
     if ((e = cudaMemcpyAsync(bad_pivot_host, &w.st->bad_pivot, sizeof(unsigned long long), cudaMemcpyDeviceToHost,
@@ -365,6 +368,7 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
 
     // Block subspace iteration on G, the block kept as rows of ZT (k x cols).
     init_block_kernel<<<grid1d((int64_t)k * cols), 256, 0, s>>>(w.ZT, k, cols);
+    count_launch();
     if ((e = orthonormalize(w, k, cols, qst, s)) != cudaSuccess) return e;
     for (int it = 0; it < EORA_ITERS; ++it) {
         // ZT <- ZT G  (= (G Z)^T, G symmetric)
@@ -390,6 +394,7 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
         attr_set = true;
     }
     jacobi_eig_kernel<<<1, JT, JACOBI_SMEM, s>>>(w.Gm, k, w.lam, w.Wt);
+    count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // V_r^T = W[:, :r]^T Z^T  (r x cols)
     if ((e = sgemm<float>(r, cols, k, 1.f, w.Wt, k, true, w.ZT, cols, false, 0.f, w.VrT, cols, 0, s)) != cudaSuccess)
@@ -398,10 +403,12 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     if ((e = sgemm<float>(rows, r, cols, 1.f, w.M, cols, false, w.VrT, cols, true, 0.f, B, r, 0, s)) != cudaSuccess)
         return e;
     sign_normalize_kernel<<<r, 256, 0, s>>>(B, rows, r);
+    count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // A = Σ^-2 B^T ΔW  (r x cols)
     if ((e = sgemm<float>(r, cols, rows, 1.f, B, r, true, dW, cols, false, 0.f, A, cols, 0, s)) != cudaSuccess) return e;
     finish_kernel<<<r, 256, 0, s>>>(w.lam, r, sigma, A, cols);
+    count_launch();
     return cudaGetLastError();
 }
 

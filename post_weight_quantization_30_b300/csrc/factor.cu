@@ -370,8 +370,10 @@ __global__ void finalize_kernel(float *__restrict__ F, int64_t cols) {
 cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, uint8_t *dead,
                            DeviceStatus *st, cudaStream_t s) {
     diag_sum_kernel<<<1, 1024, 0, s>>>(H, cols, damp, st);
+    count_launch();
     dim3 grid((unsigned)((cols + 255) / 256 < 8 ? (cols + 255) / 256 : 8), (unsigned)cols);
     reverse_damp_kernel<<<grid, 256, 0, s>>>(H, cols, F, dead, st);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -397,6 +399,7 @@ cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, flo
     for (int64_t k0 = 0; k0 < cols; k0 += NB) {
         const int kb = (int)((cols - k0) < NB ? (cols - k0) : NB);
         potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, s>>>(F, cols, k0, kb, Linv, st);
+        count_launch();
         const int64_t k1 = k0 + kb;
         if (k1 >= cols) break;
         const int64_t rest = cols - k1;
@@ -428,6 +431,7 @@ cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, flo
 cudaError_t factor_finalize(float *F, int64_t cols, cudaStream_t s) {
     dim3 grid((unsigned)((cols + 255) / 256 < 8 ? (cols + 255) / 256 : 8), (unsigned)cols);
     finalize_kernel<<<grid, 256, 0, s>>>(F, cols);
+    count_launch();
     return cudaGetLastError();
 }
 

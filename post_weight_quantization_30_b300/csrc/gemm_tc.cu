@@ -352,6 +352,7 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
     gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta,
                                                     tri, Chi, Clo, ldcs);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -362,6 +363,7 @@ cudaError_t split_tf32(const float *src, int64_t rows, int64_t cols, int64_t lds
     int64_t g = (n + 255) / 256;
     if (g > 148 * 16) g = 148 * 16;
     split_kernel<<<(unsigned)g, 256, 0, s>>>(src, rows, cols, lds, hi, lo, ldd);
+    count_launch();
     return cudaGetLastError();
 }
 

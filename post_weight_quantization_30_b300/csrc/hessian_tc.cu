@@ -273,6 +273,7 @@ cudaError_t hessian_bf16_tc(float *H, int64_t cols, const __nv_bfloat16 *X, int6
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
         hessian_tc_kernel<<<tiles, NWARPS * 32, SMEM_BYTES, s>>>(map, H, (int)cols, (int)nc);
+        count_launch();
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -44,12 +44,28 @@ __global__ void unpack_kernel(const int32_t *__restrict__ qweight, int64_t rows,
     }
 }
 
+template <typename TW>
+__global__ void weight_error_kernel(const TW *__restrict__ W, const float *__restrict__ W_hat, int64_t n,
+                                    float *__restrict__ dW) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dW[i] = load_f32(W + i) - W_hat[i];
+}
+
 unsigned grid_for(int64_t total) {
     int64_t g = (total + 255) / 256;
     return (unsigned)(g < 148 * 16 ? (g < 1 ? 1 : g) : 148 * 16);
 }
 
 }  // namespace
+
+cudaError_t weight_error_launch(const void *W, bool w_bf16, int64_t n, const float *W_hat, float *dW, cudaStream_t s) {
+    if (w_bf16)
+        weight_error_kernel<__nv_bfloat16><<<grid_for(n), 256, 0, s>>>((const __nv_bfloat16 *)W, W_hat, n, dW);
+    else
+        weight_error_kernel<float><<<grid_for(n), 256, 0, s>>>((const float *)W, W_hat, n, dW);
+    count_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t pack_launch(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight,
                         cudaStream_t s) {
@@ -58,6 +74,7 @@ cudaError_t pack_launch(const uint8_t *codes, int64_t rows, int64_t cols, int bi
     else if (bits == 3) pack_kernel<3><<<g, 256, 0, s>>>(codes, rows, cols, qweight);
     else if (bits == 4) pack_kernel<4><<<g, 256, 0, s>>>(codes, rows, cols, qweight);
     else return cudaErrorInvalidValue;
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -68,6 +85,7 @@ cudaError_t unpack_launch(const int32_t *qweight, int64_t rows, int64_t cols, in
     else if (bits == 3) unpack_kernel<3><<<g, 256, 0, s>>>(qweight, rows, cols, codes);
     else if (bits == 4) unpack_kernel<4><<<g, 256, 0, s>>>(qweight, rows, cols, codes);
     else return cudaErrorInvalidValue;
+    count_launch();
     return cudaGetLastError();
 }
 

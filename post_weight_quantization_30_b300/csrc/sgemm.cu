@@ -158,6 +158,7 @@ cudaError_t sgemm(int64_t M, int64_t N, int64_t K, float alpha, const TA *A, int
         sgemm_kernel<TA, false, true><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri, K, 0);
     else
         sgemm_kernel<TA, false, false><<<grid, NT, 0, s>>>(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tri, K, 0);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -186,10 +187,12 @@ cudaError_t sgemm_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_
         sgemm_kernel<float, false, true><<<grid, NT, 0, s>>>(M, N, K, 1.f, A, lda, B, ldb, 0.f, partials, N, 0, kslice, cz);
     else
         sgemm_kernel<float, false, false><<<grid, NT, 0, s>>>(M, N, K, 1.f, A, lda, B, ldb, 0.f, partials, N, 0, kslice, cz);
+    count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t n = M * N;
     sum_slices_kernel<<<(unsigned)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184), 256, 0, s>>>(partials, z < 1 ? 1 : z, n, C);
+    count_launch();
     return cudaGetLastError();
 }
 

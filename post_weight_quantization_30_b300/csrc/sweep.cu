@@ -379,6 +379,7 @@ cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, in
     }
     sweep_kernel<BITS, TW><<<(unsigned)((rows + ROWS - 1) / ROWS), NTHREADS, smem, s>>>(
         W, rows, cols, c0, bw, Uinv, F, dead, group, D, DL, qweight, scales, qzeros, codes, W_hat, row_err);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -394,6 +395,7 @@ cudaError_t block_inverses(const float *F, int64_t cols, int block, float *Uinv,
     }
     const int64_t nblk = (cols + block - 1) / block;
     block_inverse_kernel<<<(unsigned)nblk, 128, smem, s>>>(F, cols, block, Uinv);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -403,6 +405,7 @@ cudaError_t premultiply_t(const float *F, int64_t cols, int block, const float *
     if (nblk < 2) return cudaSuccess;
     dim3 grid((unsigned)(((nblk - 1) * block + 127) / 128), (unsigned)nblk);
     premultiply_t_kernel<<<grid, 256, 0, s>>>(F, cols, block, Uinv, VThi, VTlo);
+    count_launch();
     return cudaGetLastError();
 }
 

@@ -137,3 +137,13 @@ def test_not_positive_definite(gq):
     with pytest.raises(gq.GQError) as ei:
         _run(gq, dW, H2, 4)
     assert ei.value.status == -2
+
+
+def test_weight_error_is_exact(gq):
+    rng = np.random.default_rng(7)
+    w = rng.standard_normal((64, 96)).astype(np.float32)
+    wh = (w + rng.standard_normal((64, 96)).astype(np.float32) * 0.01).astype(np.float32)
+    Wb = torch.from_numpy(w).cuda().to(torch.bfloat16)
+    dW = gq.gptq_weight_error(Wb, torch.from_numpy(wh).cuda()).cpu().numpy()
+    expect = Wb.float().cpu().numpy() - wh  # one float32 subtraction per element
+    assert np.array_equal(dW, expect)
