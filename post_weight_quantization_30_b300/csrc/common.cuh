@@ -75,6 +75,17 @@ bool gemm3_supported(const void *p, int64_t ld);
 cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi, const float *Alo, int64_t lda,
                   const float *Bhi, const float *Blo, int64_t ldb, float beta, float *C, int64_t ldc, int tri,
                   float *Chi, float *Clo, int64_t ldcs, cudaStream_t s);
+// C (M x N, row-major, ldc = N) = A B^T as gemm3, with K split into `slices`
+// ranges computed by separate CTAs into `partials` (slices * M * N floats)
+// and summed in a fixed order.
+cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, const float *Alo, int64_t lda,
+                         const float *Bhi, const float *Blo, int64_t ldb, float *C, float *partials, int slices,
+                         cudaStream_t s);
+// C[i] = sum over z < slices of partials[z * n + i] (fixed order).
+cudaError_t sum_slices(const float *partials, int slices, int64_t n, float *C, cudaStream_t s);
+// hi / lo TF32 split of the transpose of a rows x cols float32 matrix (cols x rows out).
+cudaError_t split_transpose_tf32(const float *src, int64_t rows, int64_t cols, int64_t lds, float *hi, float *lo,
+                                 int64_t ldd, cudaStream_t s);
 // hi / lo TF32 split of a rows x cols float32 matrix (x = hi + lo exactly).
 cudaError_t split_tf32(const float *src, int64_t rows, int64_t cols, int64_t lds, float *hi, float *lo, int64_t ldd,
                        cudaStream_t s);

@@ -269,38 +269,64 @@ __global__ void finish_kernel(const float *__restrict__ lam, int r, float *__res
 struct EoraWs {
     DeviceStatus *st;
     float *Linv, *F, *M, *G, *ZT, *ZT2, *Gm, *part, *lam, *Wt, *VrT;
+    // tensor-core path only (null otherwise)
+    float *FThi, *FTlo, *dWhi, *dWlo, *Mthi, *Mtlo, *Ghi, *Glo, *Zhi, *Zlo;
     uint8_t *dead;
 };
 
+constexpr int ZSPLIT = 4;   // K slices of the subspace products on the tensor cores
+constexpr int ASPLIT = 8;   // K slices of A = B^T dW
+
 int eora_k(int64_t rows, int64_t cols, int r) {
+    (void)rows;
     int64_t k = 2 * (int64_t)r;
     if (k > EORA_MAX_K) k = EORA_MAX_K;
     if (k > cols) k = cols;
     return (int)k;
 }
 
+// The tensor-core path needs TMA-compatible row strides for M^T (rows) and H (cols).
+bool eora_tc(int64_t rows, int64_t cols) { return rows % 4 == 0 && cols % 4 == 0; }
+
 size_t eora_layout(int64_t rows, int64_t cols, int r, EoraWs *w, char *base) {
     const int k = eora_k(rows, cols, r);
+    const bool tc = eora_tc(rows, cols);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         char *p = base ? base + off : nullptr;
         off += align_up(bytes);
         return p;
     };
-    EoraWs t;
+    const size_t rc = (size_t)rows * cols * sizeof(float), cc = (size_t)cols * cols * sizeof(float);
+    EoraWs t = {};
     t.st = (DeviceStatus *)take(sizeof(DeviceStatus));
     t.Linv = (float *)take(cholesky_scratch_floats(cols > 128 ? cols : 128) * sizeof(float));
-    t.F = (float *)take((size_t)cols * cols * sizeof(float));
+    t.F = (float *)take(cc);
     t.dead = (uint8_t *)take((size_t)cols);
-    t.M = (float *)take((size_t)rows * cols * sizeof(float));
-    t.G = (float *)take((size_t)cols * cols * sizeof(float));
+    t.M = (float *)take(rc);  // M (rows x cols) on the SIMT path, M^T (cols x rows) on the tensor path
+    t.G = (float *)take(cc);
     t.ZT = (float *)take((size_t)k * cols * sizeof(float));
     t.ZT2 = (float *)take((size_t)k * cols * sizeof(float));
     t.Gm = (float *)take((size_t)k * k * sizeof(float));
-    t.part = (float *)take((size_t)SPLITK * k * k * sizeof(float));
+    size_t part = (size_t)SPLITK * k * k;
+    if ((size_t)ASPLIT * r * cols > part) part = (size_t)ASPLIT * r * cols;
+    if (tc && (size_t)ZSPLIT * k * cols > part) part = (size_t)ZSPLIT * k * cols;
+    t.part = (float *)take(part * sizeof(float));
     t.lam = (float *)take((size_t)k * sizeof(float));
     t.Wt = (float *)take((size_t)k * k * sizeof(float));
     t.VrT = (float *)take((size_t)r * cols * sizeof(float));
+    if (tc) {
+        t.FThi = (float *)take(cc);
+        t.FTlo = (float *)take(cc);
+        t.dWhi = (float *)take(rc);
+        t.dWlo = (float *)take(rc);
+        t.Mthi = (float *)take(rc);
+        t.Mtlo = (float *)take(rc);
+        t.Ghi = (float *)take(cc);
+        t.Glo = (float *)take(cc);
+        t.Zhi = (float *)take((size_t)k * cols * sizeof(float));
+        t.Zlo = (float *)take((size_t)k * cols * sizeof(float));
+    }
     if (w) *w = t;
     return off;
 }
@@ -310,25 +336,27 @@ unsigned grid1d(int64_t n) {
     return (unsigned)(g < 1 ? 1 : (g > 148 * 8 ? 148 * 8 : g));
 }
 
-// Rows of ZT (k x cols) made orthonormal: two passes of shifted Cholesky-QR,
-// ZT <- L^-1 ZT with ZT ZT^T + shift = L L^T.  Result in ZT.
-cudaError_t orthonormalize(const EoraWs &w, int k, int64_t cols, DeviceStatus *qst, cudaStream_t s) {
-    for (int pass = 0; pass < 2; ++pass) {
-        normalize_rows_kernel<<<k, 256, 0, s>>>(w.ZT, cols);
-        count_launch();
-        cudaError_t e = sgemm_splitk(k, k, cols, w.ZT, cols, false, w.ZT, cols, true, w.Gm, w.part, SPLITK, s);
-        if (e != cudaSuccess) return e;
-        shift_gram_kernel<<<1, 128, 0, s>>>(w.Gm, k);
-        count_launch();
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        e = cholesky_lower_inplace(w.Gm, k, qst, w.Linv, s);
-        if (e != cudaSuccess) return e;
-        e = sgemm<float>(k, cols, k, 1.f, w.Linv, 128, false, w.ZT, cols, false, 0.f, w.ZT2, cols, 0, s);
-        if (e != cudaSuccess) return e;
-        e = cudaMemcpyAsync(w.ZT, w.ZT2, (size_t)k * cols * sizeof(float), cudaMemcpyDeviceToDevice, s);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+// One pass of shifted Cholesky-QR on the rows of src (k x cols): rows scaled
+// to unit norm, src src^T + shift = L L^T, dst = L^-1 src.  src is scaled in place.
+cudaError_t cholqr_pass(const EoraWs &w, float *src, float *dst, int k, int64_t cols, DeviceStatus *qst,
+                        cudaStream_t s) {
+    normalize_rows_kernel<<<k, 256, 0, s>>>(src, cols);
+    count_launch();
+    cudaError_t e = sgemm_splitk(k, k, cols, src, cols, false, src, cols, true, w.Gm, w.part, SPLITK, s);
+    if (e != cudaSuccess) return e;
+    shift_gram_kernel<<<1, 128, 0, s>>>(w.Gm, k);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cholesky_lower_inplace(w.Gm, k, qst, w.Linv, s)) != cudaSuccess) return e;
+    return sgemm<float>(k, cols, k, 1.f, w.Linv, 128, false, src, cols, false, 0.f, dst, cols, 0, s);
+}
+
+// Y = Z^T-block times G: rows of ZT (k x cols) multiplied by the symmetric G.
+cudaError_t block_times_g(const EoraWs &w, const float *ZT, float *Y, int k, int64_t cols, bool tc, cudaStream_t s) {
+    if (!tc) return sgemm<float>(k, cols, cols, 1.f, ZT, cols, false, w.G, cols, false, 0.f, Y, cols, 0, s);
+    cudaError_t e = split_tf32(ZT, k, cols, cols, w.Zhi, w.Zlo, cols, s);
+    if (e != cudaSuccess) return e;
+    return gemm3_splitk(k, cols, cols, w.Zhi, w.Zlo, cols, w.Ghi, w.Glo, cols, Y, w.part, ZSPLIT, s);
 }
 
 }  // namespace
@@ -344,6 +372,7 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     const size_t main_bytes = eora_layout(rows, cols, r, &w, (char *)ws);
     DeviceStatus *qst = (DeviceStatus *)((char *)ws + main_bytes);
     const int k = eora_k(rows, cols, r);
+    const bool tc = eora_tc(rows, cols);
     cudaError_t e;
 
     // H = F F^T (no damping); every input must be live.
@@ -360,30 +389,45 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
     if (*bad_pivot_host != ULLONG_MAX) return cudaSuccess;
 
-    // M = ΔW F, G = M^T M (symmetric).
-    if ((e = sgemm<float>(rows, cols, cols, 1.f, dW, cols, false, w.F, cols, false, 0.f, w.M, cols, 0, s)) != cudaSuccess)
+    if (tc) {
+        // M^T = F^T dW^T (cols x rows, also split), G = M^T M (cols x cols, also split).
+        if ((e = split_transpose_tf32(w.F, cols, cols, cols, w.FThi, w.FTlo, cols, s)) != cudaSuccess) return e;
+        if ((e = split_tf32(dW, rows, cols, cols, w.dWhi, w.dWlo, cols, s)) != cudaSuccess) return e;
+        if ((e = gemm3(cols, rows, cols, 1.f, w.FThi, w.FTlo, cols, w.dWhi, w.dWlo, cols, 0.f, w.M, rows, 0, w.Mthi,
+                       w.Mtlo, rows, s)) != cudaSuccess)
+            return e;
+        if ((e = gemm3(cols, cols, rows, 1.f, w.Mthi, w.Mtlo, rows, w.Mthi, w.Mtlo, rows, 0.f, w.G, cols, 0, w.Ghi,
+                       w.Glo, cols, s)) != cudaSuccess)
+            return e;
+    } else {
+        // M = dW F, G = M^T M (symmetric).
+        if ((e = sgemm<float>(rows, cols, cols, 1.f, dW, cols, false, w.F, cols, false, 0.f, w.M, cols, 0, s)) !=
+            cudaSuccess)
+            return e;
+        if ((e = sgemm<float>(cols, cols, rows, 1.f, w.M, cols, true, w.M, cols, false, 0.f, w.G, cols, 2, s)) !=
+            cudaSuccess)
+            return e;
+    }
+
+    // Block subspace iteration on G, the block kept as the rows of ZT (k x cols):
+    // ZT <- orth(ZT G).  One Cholesky-QR pass per product, two at the start and
+    // before the Rayleigh-Ritz step.
+    init_block_kernel<<<grid1d((int64_t)k * cols), 256, 0, s>>>(w.ZT2, k, cols);
+    count_launch();
+    if ((e = cholqr_pass(w, w.ZT2, w.ZT, k, cols, qst, s)) != cudaSuccess) return e;
+    if ((e = cholqr_pass(w, w.ZT, w.ZT2, k, cols, qst, s)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(w.ZT, w.ZT2, (size_t)k * cols * sizeof(float), cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
         return e;
-    if ((e = sgemm<float>(cols, cols, rows, 1.f, w.M, cols, true, w.M, cols, false, 0.f, w.G, cols, 2, s)) != cudaSuccess)
+    for (int it = 0; it < EORA_ITERS; ++it) {
+        if ((e = block_times_g(w, w.ZT, w.ZT2, k, cols, tc, s)) != cudaSuccess) return e;
+        if ((e = cholqr_pass(w, w.ZT2, w.ZT, k, cols, qst, s)) != cudaSuccess) return e;
+    }
+    if ((e = cholqr_pass(w, w.ZT, w.ZT2, k, cols, qst, s)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(w.ZT, w.ZT2, (size_t)k * cols * sizeof(float), cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
         return e;
 
-    // Block subspace iteration on G, the block kept as rows of ZT (k x cols).
-    init_block_kernel<<<grid1d((int64_t)k * cols), 256, 0, s>>>(w.ZT, k, cols);
-    count_launch();
-    if ((e = orthonormalize(w, k, cols, qst, s)) != cudaSuccess) return e;
-    for (int it = 0; it < EORA_ITERS; ++it) {
-        // ZT <- ZT G  (= (G Z)^T, G symmetric)
-        if ((e = sgemm<float>(k, cols, cols, 1.f, w.ZT, cols, false, w.G, cols, false, 0.f, w.ZT2, cols, 0, s)) !=
-            cudaSuccess)
-            return e;
-        if ((e = cudaMemcpyAsync(w.ZT, w.ZT2, (size_t)k * cols * sizeof(float), cudaMemcpyDeviceToDevice, s)) !=
-            cudaSuccess)
-            return e;
-        if ((e = orthonormalize(w, k, cols, qst, s)) != cudaSuccess) return e;
-    }
     // Rayleigh-Ritz: T = Z^T G Z (k x k), eigenpairs by Jacobi.
-    if ((e = sgemm<float>(k, cols, cols, 1.f, w.ZT, cols, false, w.G, cols, false, 0.f, w.ZT2, cols, 0, s)) !=
-        cudaSuccess)
-        return e;
+    if ((e = block_times_g(w, w.ZT, w.ZT2, k, cols, tc, s)) != cudaSuccess) return e;
     if ((e = sgemm_splitk(k, k, cols, w.ZT2, cols, false, w.ZT, cols, true, w.Gm, w.part, SPLITK, s)) != cudaSuccess)
         return e;
     static bool attr_set = false;
@@ -400,13 +444,16 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     if ((e = sgemm<float>(r, cols, k, 1.f, w.Wt, k, true, w.ZT, cols, false, 0.f, w.VrT, cols, 0, s)) != cudaSuccess)
         return e;
     // B = M V_r (rows x r), signs normalised.
-    if ((e = sgemm<float>(rows, r, cols, 1.f, w.M, cols, false, w.VrT, cols, true, 0.f, B, r, 0, s)) != cudaSuccess)
-        return e;
+    if (tc)
+        e = sgemm<float>(rows, r, cols, 1.f, w.M, rows, true, w.VrT, cols, true, 0.f, B, r, 0, s);
+    else
+        e = sgemm<float>(rows, r, cols, 1.f, w.M, cols, false, w.VrT, cols, true, 0.f, B, r, 0, s);
+    if (e != cudaSuccess) return e;
     sign_normalize_kernel<<<r, 256, 0, s>>>(B, rows, r);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // A = Σ^-2 B^T ΔW  (r x cols)
-    if ((e = sgemm<float>(r, cols, rows, 1.f, B, r, true, dW, cols, false, 0.f, A, cols, 0, s)) != cudaSuccess) return e;
+    // A = Σ^-2 B^T dW  (r x cols)
+    if ((e = sgemm_splitk(r, cols, rows, B, r, true, dW, cols, false, A, w.part, ASPLIT, s)) != cudaSuccess) return e;
     finish_kernel<<<r, 256, 0, s>>>(w.lam, r, sigma, A, cols);
     count_launch();
     return cudaGetLastError();

@@ -70,9 +70,15 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
     gemm3_kernel(const __grid_constant__ CUtensorMap ahi, const __grid_constant__ CUtensorMap alo,
                  const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo, float *C,
                  int64_t ldc, int M, int N, int K, float alpha, float beta, int tri, float *Chi, float *Clo,
-                 int64_t ldcs) {
+                 int64_t ldcs, int ktiles_per_z, int64_t c_zstride) {
     const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
     if (tri == 1 && n0 > m0 + GM - 1) return;  // tile entirely above the diagonal
+    // Split K (gridDim.z > 1): slice z covers k-tiles [z * ktiles_per_z, ...) and
+    // writes its partial product to C + z * c_zstride.
+    const int kt_all = (K + GK - 1) / GK;
+    const int kt0 = blockIdx.z * ktiles_per_z;
+    const int kt1 = (kt0 + ktiles_per_z) < kt_all ? (kt0 + ktiles_per_z) : kt_all;
+    C += (int64_t)blockIdx.z * c_zstride;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[G_STAGES];
@@ -84,7 +90,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
 
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ktiles = (K + GK - 1) / GK;
+    const int ktiles = kt1 > kt0 ? kt1 - kt0 : 0;
     const int periods = (ktiles + G_KF - 1) / G_KF;
 
     if (threadIdx.x == 0) {
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
                 }
                 unsigned char *st = smem + s * G_STAGE;
                 mbar_arrive_expect_tx(&full_bar[s], G_STAGE);
-                const int x = kt * GK;
+                const int x = (kt0 + kt) * GK;
                 tma_load_2d(st, &ahi, x, m0, &full_bar[s]);
                 tma_load_2d(st + TILE_A, &alo, x, m0, &full_bar[s]);
                 tma_load_2d(st + 2 * TILE_A, &bhi, x, n0, &full_bar[s]);
@@ -310,6 +316,28 @@ __global__ void split_kernel(const float *__restrict__ src, int64_t rows, int64_
     }
 }
 
+// dst = src^T split: hi[c][r] = tf32(src[r][c]), lo = src - hi.  32 x 32 tiles
+// through shared memory so both the reads and the writes are coalesced.
+__global__ void split_transpose_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t lds,
+                                       float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
+    __shared__ float tile[32][33];
+    const int64_t r0 = (int64_t)blockIdx.y * 32, c0 = (int64_t)blockIdx.x * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int64_t r = r0 + i, c = c0 + threadIdx.x;
+        tile[i][threadIdx.x] = (r < rows && c < cols) ? src[r * lds + c] : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int64_t c = c0 + i, r = r0 + threadIdx.x;
+        if (c < cols && r < rows) {
+            const float x = tile[threadIdx.x][i];
+            const float h = tf32_hi(x);
+            hi[c * ldd + r] = h;
+            lo[c * ldd + r] = x - h;
+        }
+    }
+}
+
 bool make_map(CUtensorMap *map, const float *base, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -350,8 +378,45 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
         !make_map(&mbh, Bhi, K, N, ldb, GN) || !make_map(&mbl, Blo, K, N, ldb, GN))
         return cudaErrorInvalidValue;
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
+    const int kt_all = (int)((K + GK - 1) / GK);
     gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta,
-                                                    tri, Chi, Clo, ldcs);
+                                                    tri, Chi, Clo, ldcs, kt_all, 0);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, const float *Alo, int64_t lda,
+                         const float *Bhi, const float *Blo, int64_t ldb, float *C, float *partials, int slices,
+                         cudaStream_t s) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    if (K <= 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || slices < 1) return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemm3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap mah, mal, mbh, mbl;
+    if (!make_map(&mah, Ahi, K, M, lda, GM) || !make_map(&mal, Alo, K, M, lda, GM) ||
+        !make_map(&mbh, Bhi, K, N, ldb, GN) || !make_map(&mbl, Blo, K, N, ldb, GN))
+        return cudaErrorInvalidValue;
+    const int kt_all = (int)((K + GK - 1) / GK);
+    const int per = (kt_all + slices - 1) / slices;
+    const int z = (kt_all + per - 1) / per;
+    dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM), (unsigned)z);
+    gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, partials, N, (int)M, (int)N, (int)K, 1.f, 0.f,
+                                                    0, nullptr, nullptr, 0, per, M * N);
+    count_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return sum_slices(partials, z, M * N, C, s);
+}
+
+cudaError_t split_transpose_tf32(const float *src, int64_t rows, int64_t cols, int64_t lds, float *hi, float *lo,
+                                 int64_t ldd, cudaStream_t s) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows + 31) / 32));
+    split_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(src, rows, cols, lds, hi, lo, ldd);
     count_launch();
     return cudaGetLastError();
 }

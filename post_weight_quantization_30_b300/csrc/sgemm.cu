@@ -172,6 +172,12 @@ __global__ void sum_slices_kernel(const float *__restrict__ P, int slices, int64
 }
 }  // namespace
 
+cudaError_t sum_slices(const float *partials, int slices, int64_t n, float *C, cudaStream_t s) {
+    sum_slices_kernel<<<(unsigned)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184), 256, 0, s>>>(partials, slices, n, C);
+    count_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t sgemm_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, bool a_t, const float *B,
                          int64_t ldb, bool b_t, float *C, float *partials, int slices, cudaStream_t s) {
     if (M <= 0 || N <= 0) return cudaSuccess;

@@ -147,3 +147,13 @@ def test_weight_error_is_exact(gq):
     dW = gq.gptq_weight_error(Wb, torch.from_numpy(wh).cuda()).cpu().numpy()
     expect = Wb.float().cpu().numpy() - wh  # one float32 subtraction per element
     assert np.array_equal(dW, expect)
+
+
+def test_ragged_shape_uses_simt_path(gq):
+    """rows, cols not multiples of 4: the products run on the float32 SIMT path."""
+    rows, cols, r = 90, 66, 8
+    rng = np.random.default_rng(8)
+    dW = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32).astype(np.float64)
+    H = _h_from_x(400, cols, 9, outliers=1).astype(np.float32)
+    g = _run(gq, dW, H, r)
+    _check_unique_parts(g, dW, H, r)
