@@ -81,6 +81,51 @@ cudaError_t sweep_range(const SweepCtx &c, int64_t a, int64_t b) {
     return sweep_range(c, m, b);
 }
 
+// Dead inputs + damping, blocked Cholesky of the reversed matrix, reversal;
+// one synchronization to read the pivot status.
+gq_status factor_impl(const float *H, int64_t cols, float damp, float *F, uint8_t *dead, void *ws, cudaStream_t s,
+                      int64_t *info, float *Uinv, int block) {
+    DeviceStatus *st = (DeviceStatus *)ws;
+    float *scratch = (float *)((char *)ws + align_up(sizeof(DeviceStatus)));
+    GQ_CUDA_TRY(cudaMemsetAsync(st, 0xFF, sizeof(DeviceStatus), s));
+    GQ_CUDA_TRY(factor_prepare(H, cols, damp, F, dead, st, s));
+    GQ_CUDA_TRY(cholesky_lower_inplace(F, cols, st, scratch, s, Uinv, block));
+    GQ_CUDA_TRY(factor_finalize(F, cols, s));
+    unsigned long long bad = 0;
+    GQ_CUDA_TRY(cudaMemcpyAsync(&bad, &st->bad_pivot, sizeof(bad), cudaMemcpyDeviceToHost, s));
+    GQ_CUDA_TRY(cudaStreamSynchronize(s));
+    if (bad != ULLONG_MAX) {
+        if (info) *info = cols - 1 - (int64_t)bad;
+        return GQ_ENOTPD;
+    }
+    if (info) *info = -1;
+    return GQ_OK;
+}
+
+// The sweep on a checked workspace.  uinv_ready: the block-inverse region at
+// the start of ws already holds F's diagonal-block inverses.
+gq_status sweep_impl(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *F, const uint8_t *dead,
+                     int bits, int group, int block, int32_t *qweight, float *scales, int32_t *qzeros, uint8_t *codes,
+                     float *W_hat, float *row_err, void *ws, cudaStream_t s, bool uinv_ready) {
+    const int64_t nblk = (cols + block - 1) / block;
+    SweepCtx c;
+    c.W = W; c.bf16 = (wt == GQ_BF16); c.rows = rows; c.cols = cols; c.F = F; c.dead = dead;
+    c.bits = bits; c.group = group; c.block = block;
+    c.qweight = qweight; c.scales = scales; c.qzeros = qzeros; c.codes = codes; c.W_hat = W_hat; c.row_err = row_err;
+    c.Uinv = (float *)ws;
+    c.VThi = (float *)((char *)ws + align_up((size_t)nblk * block * block * sizeof(float)));
+    c.VTlo = (float *)((char *)c.VThi + align_up((size_t)cols * cols * sizeof(float)));
+    c.D = (float *)((char *)c.VTlo + align_up((size_t)cols * cols * sizeof(float)));
+    c.DL = (float *)((char *)c.D + align_up((size_t)rows * cols * sizeof(float)));
+    c.s = s;
+    GQ_CUDA_TRY(cudaMemsetAsync(c.D, 0, (size_t)rows * cols * sizeof(float), s));
+    if (row_err) GQ_CUDA_TRY(cudaMemsetAsync(row_err, 0, (size_t)rows * sizeof(float), s));
+    if (!uinv_ready) GQ_CUDA_TRY(block_inverses(F, cols, block, c.Uinv, s));
+    GQ_CUDA_TRY(premultiply_t(F, cols, block, c.Uinv, c.VThi, c.VTlo, s));
+    GQ_CUDA_TRY(sweep_range(c, 0, nblk));
+    return GQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -140,22 +185,7 @@ gq_status gptq_factor(const float *H, int64_t cols, float damp, float *F, uint8_
     if (cols <= 0 || !H || !F) return GQ_EINVAL;
     if (!(damp >= 0.f)) return GQ_EINVAL;
     if (!ws || !aligned(ws, kAlign) || ws_bytes < gptq_factor_workspace_size(cols)) return GQ_EWORKSPACE;
-    cudaStream_t s = cs(stream);
-    DeviceStatus *st = (DeviceStatus *)ws;
-    float *Linv = (float *)((char *)ws + align_up(sizeof(DeviceStatus)));
-    GQ_CUDA_TRY(cudaMemsetAsync(st, 0xFF, sizeof(DeviceStatus), s));
-    GQ_CUDA_TRY(factor_prepare(H, cols, damp, F, dead, st, s));
-    GQ_CUDA_TRY(cholesky_lower_inplace(F, cols, st, Linv, s));
-    GQ_CUDA_TRY(factor_finalize(F, cols, s));
-    unsigned long long bad = 0;
-    GQ_CUDA_TRY(cudaMemcpyAsync(&bad, &st->bad_pivot, sizeof(bad), cudaMemcpyDeviceToHost, s));
-    GQ_CUDA_TRY(cudaStreamSynchronize(s));
-    if (bad != ULLONG_MAX) {
-        if (info) *info = cols - 1 - (int64_t)bad;
-        return GQ_ENOTPD;
-    }
-    if (info) *info = -1;
-    return GQ_OK;
+    return factor_impl(H, cols, damp, F, dead, ws, cs(stream), info, nullptr, 0);
 }
 
 size_t gptq_sweep_workspace_size(int64_t rows, int64_t cols, int block) {
@@ -170,24 +200,8 @@ gq_status gptq_sweep(const void *W, gq_dtype wt, int64_t rows, int64_t cols, con
                                     row_err);
     if (st != GQ_OK) return st;
     if (!ws || !aligned(ws, kAlign) || ws_bytes < sweep_ws_bytes(rows, cols, block)) return GQ_EWORKSPACE;
-    cudaStream_t s = cs(stream);
-    const int64_t nblk = (cols + block - 1) / block;
-    SweepCtx c;
-    c.W = W; c.bf16 = (wt == GQ_BF16); c.rows = rows; c.cols = cols; c.F = F; c.dead = dead;
-    c.bits = bits; c.group = group; c.block = block;
-    c.qweight = qweight; c.scales = scales; c.qzeros = qzeros; c.codes = codes; c.W_hat = W_hat; c.row_err = row_err;
-    c.Uinv = (float *)ws;
-    c.VThi = (float *)((char *)ws + align_up((size_t)nblk * block * block * sizeof(float)));
-    c.VTlo = (float *)((char *)c.VThi + align_up((size_t)cols * cols * sizeof(float)));
-    c.D = (float *)((char *)c.VTlo + align_up((size_t)cols * cols * sizeof(float)));
-    c.DL = (float *)((char *)c.D + align_up((size_t)rows * cols * sizeof(float)));
-    c.s = s;
-    GQ_CUDA_TRY(cudaMemsetAsync(c.D, 0, (size_t)rows * cols * sizeof(float), s));
-    if (row_err) GQ_CUDA_TRY(cudaMemsetAsync(row_err, 0, (size_t)rows * sizeof(float), s));
-    GQ_CUDA_TRY(block_inverses(F, cols, block, c.Uinv, s));
-    GQ_CUDA_TRY(premultiply_t(F, cols, block, c.Uinv, c.VThi, c.VTlo, s));
-    GQ_CUDA_TRY(sweep_range(c, 0, nblk));
-    return GQ_OK;
+    return sweep_impl(W, wt, rows, cols, F, dead, bits, group, block, qweight, scales, qzeros, codes, W_hat, row_err,
+                      ws, cs(stream), false);
 }
 
 size_t gptq_quantize_layer_workspace_size(int64_t rows, int64_t cols, int block) {
@@ -213,10 +227,13 @@ gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t 
     p += align_up((size_t)cols);
     void *fws = p;
     p += gptq_factor_workspace_size(cols);
-    st = gptq_factor(H, cols, damp, F, dead, fws, gptq_factor_workspace_size(cols), stream, info);
+    // The sweep workspace starts with its block-inverse region, which the
+    // factorization fills directly when its panels coincide with the blocks.
+    const bool uinv = factor_emits_uinv(cols, block);
+    st = factor_impl(H, cols, damp, F, dead, fws, cs(stream), info, uinv ? (float *)p : nullptr, block);
     if (st != GQ_OK) return st;
-    return gptq_sweep(W, wt, rows, cols, F, dead, bits, group, block, qweight, scales, qzeros, codes, W_hat, row_err, p,
-                      sweep_ws_bytes(rows, cols, block), stream);
+    return sweep_impl(W, wt, rows, cols, F, dead, bits, group, block, qweight, scales, qzeros, codes, W_hat, row_err, p,
+                      cs(stream), uinv);
 }
 
 gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *W_hat, float *dW,

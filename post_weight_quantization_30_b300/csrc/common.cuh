@@ -101,12 +101,18 @@ unsigned int read_and_clear_device_error();
 unsigned int gemm_read_and_clear_error();
 
 // Factor pieces.
+// True when cholesky_lower_inplace can emit the sweep's block inverses.
+inline bool factor_emits_uinv(int64_t cols, int block) { return block == 128 && cols % 128 == 0; }
 cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, uint8_t *dead,
                            DeviceStatus *st, cudaStream_t s);
 // scratch: cholesky_scratch_floats(cols) floats, 16-byte aligned; its first
 // 128 x 128 floats hold the inverse of the last diagonal block on return.
 size_t cholesky_scratch_floats(int64_t cols);
-cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *scratch, cudaStream_t s);
+// Uinv (may be NULL): if non-NULL, block == 128 and cols % 128 == 0, receives the
+// inverses of the diagonal blocks of F = J L J in sweep order (nblk x 128 x 128),
+// (factor_emits_uinv tells when).
+cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *scratch, cudaStream_t s,
+                                   float *Uinv = nullptr, int block = 0);
 cudaError_t factor_finalize(float *F, int64_t cols, cudaStream_t s);
 size_t factor_scratch_bytes(int64_t cols);
 

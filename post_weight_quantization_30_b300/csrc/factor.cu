@@ -22,6 +22,12 @@ namespace {
 
 constexpr int NB = 128;  // panel width
 
+__device__ __forceinline__ float tf32_round(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
 __global__ void diag_sum_kernel(const float *__restrict__ H, int64_t cols, float damp, DeviceStatus *st) {
     __shared__ double red[32];
     double acc = 0.0;
@@ -98,7 +104,10 @@ struct CholStep {
         if (lane == 0 && !(d > 0.f)) atomicMin(&st->bad_pivot, (unsigned long long)(gcol0 + J));
         const float r = rsqrtf(d);
         if (lane == J) rinv = r;
-        a[J] = (lane > J) ? a[J] * r : (lane == J ? d * r : a[J]);
+        // Lane J holds d, so d r = sqrt(d) there; below the diagonal a[J] r = L_iJ.
+        // Entries above a lane's diagonal (k > lane) are never read, so every lane
+        // updates all of its entries without a per-entry predicate.
+        a[J] *= r;
         if (J + 1 < SP) {
             float *cb = colbuf + (J & 1) * SP;
             cb[lane] = a[J];
@@ -110,7 +119,7 @@ struct CholStep {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int k = k4 + u;
-                    if (k > J) a[k] = (lane >= k) ? fmaf(-a[J], cv[u], a[k]) : a[k];
+                    if (k > J) a[k] = fmaf(-a[J], cv[u], a[k]);
                 }
             }
         }
@@ -145,9 +154,13 @@ __device__ __forceinline__ void warp_trinv32(const float *L, const float *dinv, 
     for (int i = 0; i < SP; ++i) YT[lane * LDA + i] = y[i];
 }
 
+// Optional outputs (may be NULL): Lhi / Llo, the TF32 split of Linv (NB x NB);
+// Urev, the index-reversed inverse Urev[i][j] = Linv[kb-1-i][kb-1-j] (kb x kb,
+// row stride kb): the inverse of the matching diagonal block of F = J L J.
 __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restrict__ F, int64_t cols, int64_t k0,
                                                                   int kb, float *__restrict__ Linv,
-                                                                  DeviceStatus *st) {
+                                                                  DeviceStatus *st, float *__restrict__ Lhi,
+                                                                  float *__restrict__ Llo, float *__restrict__ Urev) {
     extern __shared__ __align__(16) float sm[];
     float *A = sm;                 // [NB][LDA]: the block, lower triangle, becomes L
     float *Y = A + NB * LDA;       // [NB][LDA]: L^-1, lower triangle
@@ -343,6 +356,19 @@ __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restr
         if (j + 2 >= kb) yv.z = 0.f;
         if (j + 3 >= kb) yv.w = 0.f;
         *reinterpret_cast<float4 *>(Linv + idx * 4) = yv;
+        if (Lhi) {
+            const float h[4] = {tf32_round(yv.x), tf32_round(yv.y), tf32_round(yv.z), tf32_round(yv.w)};
+            *reinterpret_cast<float4 *>(Lhi + idx * 4) = make_float4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<float4 *>(Llo + idx * 4) =
+                make_float4(yv.x - h[0], yv.y - h[1], yv.z - h[2], yv.w - h[3]);
+        }
+    }
+    if (Urev) {
+        for (int idx = t; idx < kb * kb; idx += DIAG_THREADS) {
+            const int i = idx / kb, j = idx % kb;
+            const int ri = kb - 1 - i, rj = kb - 1 - j;
+            Urev[idx] = (rj <= ri) ? Y[ri * LDA + rj] : 0.f;
+        }
     }
 }
 
@@ -385,7 +411,8 @@ size_t cholesky_scratch_floats(int64_t cols) { return (size_t)3 * NB * NB + (siz
 // trailing lower triangle, A22 -= P P^T.  The two products run on the tensor
 // cores with float32 accuracy (3xTF32) when the row stride allows TMA
 // (cols % 4 == 0), else on the float32 SIMT GEMM.
-cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *scratch, cudaStream_t s) {
+cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *scratch, cudaStream_t s,
+                                   float *Uinv, int block) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(potrf_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DIAG_SMEM);
@@ -396,18 +423,24 @@ cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, flo
     float *Lhi = Linv + NB * NB, *Llo = Lhi + NB * NB;
     float *Phi = Llo + NB * NB, *Plo = Phi + cols * NB;
     const bool tc = (cols % 4) == 0;
+    // Diagonal-block inverses for the sweep come out of the factorization when
+    // its panels coincide with the sweep's blocks (reversed order).
+    const bool urev = Uinv && block == NB && (cols % NB) == 0;
+    const int64_t npanel = (cols + NB - 1) / NB;
     for (int64_t k0 = 0; k0 < cols; k0 += NB) {
         const int kb = (int)((cols - k0) < NB ? (cols - k0) : NB);
-        potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, s>>>(F, cols, k0, kb, Linv, st);
-        count_launch();
         const int64_t k1 = k0 + kb;
-        if (k1 >= cols) break;
+        const bool more = k1 < cols;
+        float *ur = urev ? Uinv + (npanel - 1 - k0 / NB) * NB * NB : nullptr;
+        potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, s>>>(F, cols, k0, kb, Linv, st, (tc && more) ? Lhi : nullptr,
+                                                             Llo, ur);
+        count_launch();
+        if (!more) break;
         const int64_t rest = cols - k1;
         float *P = F + k1 * cols + k0;  // rest x kb panel below the diagonal block
         cudaError_t e;
         if (tc) {
             // P <- P L^-T, also written split (Phi, Plo; row stride NB) for the update.
-            if ((e = split_tf32(Linv, NB, NB, NB, Lhi, Llo, NB, s)) != cudaSuccess) return e;
             if ((e = split_tf32(P, rest, kb, cols, Phi, Plo, NB, s)) != cudaSuccess) return e;
             if ((e = gemm3(rest, kb, kb, 1.f, Phi, Plo, NB, Lhi, Llo, NB, 0.f, P, cols, 0, Phi, Plo, NB, s)) !=
                 cudaSuccess)
