@@ -403,14 +403,75 @@ cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, u
     return cudaGetLastError();
 }
 
-// Scratch of cholesky_lower_inplace: [Linv: NB x NB][Lhi, Llo: NB x NB][Phi, Plo: cols x NB].
-size_t cholesky_scratch_floats(int64_t cols) { return (size_t)3 * NB * NB + (size_t)2 * cols * NB; }
+// Scratch of cholesky_lower_inplace: [Linv: NB x NB][Lhi, Llo: NB x NB][Phi, Plo: cols x NB]
+// and, for the recursive path, [LThi, LTlo: cols x cols], the TF32 split of the
+// solved panels (row stride cols).
+constexpr int64_t REC_MIN = 1024;  // columns from which the recursive path is used
+size_t cholesky_scratch_floats(int64_t cols) {
+    size_t n = (size_t)3 * NB * NB + (size_t)2 * cols * NB;
+    if (cols >= REC_MIN && cols % 4 == 0) n += (size_t)2 * cols * cols;
+    return n;
+}
 
-// Right-looking blocked Cholesky, panel width NB.  Per panel: the diagonal
-// block and its inverse (one CTA); the panel below, P <- P L_kk^-T; the
-// trailing lower triangle, A22 -= P P^T.  The two products run on the tensor
-// cores with float32 accuracy (3xTF32) when the row stride allows TMA
-// (cols % 4 == 0), else on the float32 SIMT GEMM.
+namespace {
+
+struct CholCtx {
+    float *F;
+    int64_t cols;
+    DeviceStatus *st;
+    float *Linv, *Lhi, *Llo, *Phi, *Plo, *LThi, *LTlo;
+    float *Uinv;  // sweep block inverses (reversed), or null
+    cudaStream_t s;
+};
+
+// One panel: diagonal block (factor + inverse), then the rows below solved,
+// P <- P L^-T, written to F and, split, to (LThi, LTlo) or (Phi, Plo).
+cudaError_t chol_panel(const CholCtx &c, int64_t k0, bool rec) {
+    const int64_t cols = c.cols;
+    const int kb = (int)((cols - k0) < NB ? (cols - k0) : NB);
+    const int64_t k1 = k0 + kb;
+    const bool more = k1 < cols;
+    const int64_t npanel = (cols + NB - 1) / NB;
+    float *ur = c.Uinv ? c.Uinv + (npanel - 1 - k0 / NB) * NB * NB : nullptr;
+    potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, c.s>>>(c.F, cols, k0, kb, c.Linv, c.st, more ? c.Lhi : nullptr,
+                                                           c.Llo, ur);
+    count_launch();
+    if (!more) return cudaGetLastError();
+    const int64_t rest = cols - k1;
+    float *P = c.F + k1 * cols + k0;
+    cudaError_t e = split_tf32(P, rest, kb, cols, c.Phi, c.Plo, NB, c.s);
+    if (e != cudaSuccess) return e;
+    if (rec)
+        return gemm3(rest, kb, kb, 1.f, c.Phi, c.Plo, NB, c.Lhi, c.Llo, NB, 0.f, P, cols, 0, c.LThi + k1 * cols + k0,
+                     c.LTlo + k1 * cols + k0, cols, c.s);
+    return gemm3(rest, kb, kb, 1.f, c.Phi, c.Plo, NB, c.Lhi, c.Llo, NB, 0.f, P, cols, 0, c.Phi, c.Plo, NB, c.s);
+}
+
+// Panels [a, b).  On entry the columns of these panels (rows from the first of
+// them down) carry every update from the columns left of panel a.  The left
+// half is factored, its whole contribution to the right half is applied as
+// one GEMM (K = the left half's width), then the right half is factored.
+cudaError_t chol_rec(const CholCtx &c, int64_t a, int64_t b) {
+    if (b - a == 1) return chol_panel(c, a * NB, true);
+    const int64_t m = (a + b) / 2;
+    cudaError_t e = chol_rec(c, a, m);
+    if (e != cudaSuccess) return e;
+    const int64_t c0 = a * NB, cm = m * NB, c1 = (b * NB < c.cols) ? b * NB : c.cols;
+    e = gemm3(c.cols - cm, c1 - cm, cm - c0, -1.f, c.LThi + cm * c.cols + c0, c.LTlo + cm * c.cols + c0, c.cols,
+              c.LThi + cm * c.cols + c0, c.LTlo + cm * c.cols + c0, c.cols, 1.f, c.F + cm * c.cols + cm, c.cols, 1,
+              nullptr, nullptr, 0, c.s);
+    if (e != cudaSuccess) return e;
+    return chol_rec(c, m, b);
+}
+
+}  // namespace
+
+// Blocked Cholesky, panel width NB.  Per panel: the diagonal block and its
+// inverse (one CTA) and the panel below, P <- P L_kk^-T.  The trailing updates
+// A22 -= P P^T run on the tensor cores with float32 accuracy (3xTF32) when the
+// row stride allows TMA (cols % 4 == 0): for cols >= REC_MIN in the recursive
+// order above (few large GEMMs), else right-looking after every panel.
+// Without TMA (cols % 4 != 0) both products run on the float32 SIMT GEMM.
 cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, float *scratch, cudaStream_t s,
                                    float *Uinv, int block) {
     static bool attr_set = false;
@@ -419,39 +480,49 @@ cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, flo
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    float *Linv = scratch;
-    float *Lhi = Linv + NB * NB, *Llo = Lhi + NB * NB;
-    float *Phi = Llo + NB * NB, *Plo = Phi + cols * NB;
-    const bool tc = (cols % 4) == 0;
+    CholCtx c;
+    c.F = F;
+    c.cols = cols;
+    c.st = st;
+    c.Linv = scratch;
+    c.Lhi = c.Linv + NB * NB;
+    c.Llo = c.Lhi + NB * NB;
+    c.Phi = c.Llo + NB * NB;
+    c.Plo = c.Phi + cols * NB;
+    c.LThi = c.Plo + cols * NB;
+    c.LTlo = c.LThi + cols * cols;
     // Diagonal-block inverses for the sweep come out of the factorization when
     // its panels coincide with the sweep's blocks (reversed order).
-    const bool urev = Uinv && block == NB && (cols % NB) == 0;
+    c.Uinv = (Uinv && block == NB && (cols % NB) == 0) ? Uinv : nullptr;
+    c.s = s;
+    const bool tc = (cols % 4) == 0;
     const int64_t npanel = (cols + NB - 1) / NB;
+    if (tc && cols >= REC_MIN) {
+        cudaError_t e = chol_rec(c, 0, npanel);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     for (int64_t k0 = 0; k0 < cols; k0 += NB) {
         const int kb = (int)((cols - k0) < NB ? (cols - k0) : NB);
         const int64_t k1 = k0 + kb;
-        const bool more = k1 < cols;
-        float *ur = urev ? Uinv + (npanel - 1 - k0 / NB) * NB * NB : nullptr;
-        potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, s>>>(F, cols, k0, kb, Linv, st, (tc && more) ? Lhi : nullptr,
-                                                             Llo, ur);
-        count_launch();
-        if (!more) break;
-        const int64_t rest = cols - k1;
-        float *P = F + k1 * cols + k0;  // rest x kb panel below the diagonal block
         cudaError_t e;
         if (tc) {
-            // P <- P L^-T, also written split (Phi, Plo; row stride NB) for the update.
-            if ((e = split_tf32(P, rest, kb, cols, Phi, Plo, NB, s)) != cudaSuccess) return e;
-            if ((e = gemm3(rest, kb, kb, 1.f, Phi, Plo, NB, Lhi, Llo, NB, 0.f, P, cols, 0, Phi, Plo, NB, s)) !=
-                cudaSuccess)
-                return e;
+            if ((e = chol_panel(c, k0, false)) != cudaSuccess) return e;
+            if (k1 >= cols) break;
             // A22 -= P P^T (tiles touching the lower triangle).
-            if ((e = gemm3(rest, rest, kb, -1.f, Phi, Plo, NB, Phi, Plo, NB, 1.f, F + k1 * cols + k1, cols, 1, nullptr,
-                           nullptr, 0, s)) != cudaSuccess)
+            const int64_t rest = cols - k1;
+            if ((e = gemm3(rest, rest, kb, -1.f, c.Phi, c.Plo, NB, c.Phi, c.Plo, NB, 1.f, F + k1 * cols + k1, cols, 1,
+                           nullptr, nullptr, 0, s)) != cudaSuccess)
                 return e;
         } else {
+            float *ur = c.Uinv ? c.Uinv + (npanel - 1 - k0 / NB) * NB * NB : nullptr;
+            potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, s>>>(F, cols, k0, kb, c.Linv, st, nullptr, nullptr, ur);
+            count_launch();
+            if (k1 >= cols) break;
+            const int64_t rest = cols - k1;
+            float *P = F + k1 * cols + k0;  // rest x kb panel below the diagonal block
             // P <- P L^-T in place: each 128-row tile reads its rows completely before writing them.
-            e = sgemm<float>(rest, kb, kb, 1.f, P, cols, false, Linv, NB, true, 0.f, P, cols, 0, s);
+            e = sgemm<float>(rest, kb, kb, 1.f, P, cols, false, c.Linv, NB, true, 0.f, P, cols, 0, s);
             if (e != cudaSuccess) return e;
             e = sgemm<float>(rest, rest, kb, -1.f, P, cols, false, P, cols, true, 1.f, F + k1 * cols + k1, cols,
                              /*tri=*/1, s);

@@ -44,6 +44,7 @@ constexpr uint32_t TMEM_COLS = 256;
 // buffer.  Long in-TMEM accumulation is avoided because each accumulate step
 // of the tensor core loses about half an ulp of the running sum.
 constexpr int KF = 4;
+constexpr int GROUP = 16;  // tile-rows per scheduling group
 constexpr int NWARPS = 10;
 constexpr int EPI_WARPS = 8;
 
@@ -60,15 +61,31 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // Tile of this CTA among the tiles that touch the upper triangle, row-major.
+    // Tile of this CTA among the tiles that touch the upper triangle (bj >=
+    // bjmin(bi) = bi TM / TN), in groups of GROUP tile-rows; within a group
+    // by column, then row.  CTAs that run at the same time then share a
+    // compact set of features of X, which keeps the X stripes they stream in
+    // L2 instead of re-reading all of X from HBM in every wave.
     const int nbi = (cols + TM - 1) / TM, nbj = (cols + TN - 1) / TN;
-    int t = blockIdx.x, bi = 0;
-    for (; bi < nbi; ++bi) {
-        const int cnt = nbj - (bi * TM) / TN;
+    int t = blockIdx.x, g0 = 0;
+    for (; g0 < nbi; g0 += GROUP) {
+        const int g1 = (g0 + GROUP) < nbi ? (g0 + GROUP) : nbi;
+        int cnt = 0;
+        for (int i = g0; i < g1; ++i) cnt += nbj - (i * TM) / TN;
         if (t < cnt) break;
         t -= cnt;
     }
-    const int bj = (bi * TM) / TN + t;
+    const int g1 = (g0 + GROUP) < nbi ? (g0 + GROUP) : nbi;
+    int bi = g0, bj = (g0 * TM) / TN;
+    for (; bj < nbj; ++bj) {
+        int valid = 0;  // rows of the group that reach column bj: a prefix
+        while (g0 + valid < g1 && ((g0 + valid) * TM) / TN <= bj) ++valid;
+        if (t < valid) {
+            bi = g0 + t;
+            break;
+        }
+        t -= valid;
+    }
     const int r0 = bi * TM, c0 = bj * TN;
     const int ktiles = (n + TK - 1) / TK;
     const int periods = (ktiles + KF - 1) / KF;

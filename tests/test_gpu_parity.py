@@ -81,7 +81,7 @@ def test_hessian_strided_input(gq):
 
 
 # ------------------------------------------------------------------- factor ---
-@pytest.mark.parametrize("cols", [256, 200, 1000])
+@pytest.mark.parametrize("cols", [256, 200, 1000, 1056, 1280])  # >= 1024: recursive order, 1056: ragged panel
 def test_factor_parity(gq, cols):
     spec = custom_layer("f", 32, cols, 4 * cols, dtype="f32", n_outliers=2, key=(12, cols)).X
     _, x64 = host_arrays(spec)
@@ -112,6 +112,7 @@ SWEEP_CASES = [
     (128, 320, 2, 64, 128, 2000),   # ragged last block (64 columns)
     (32, 128, 4, 32, 64, 1024),
     (160, 640, 2, 64, 64, 4096),
+    (64, 1152, 4, 128, 128, 4096),  # 9 blocks: recursive factor order, block inverses from the factor
 ]
 
 
