@@ -120,7 +120,7 @@ gq_status gptq_factor(const float *H, int64_t cols, float damp, float *F, uint8_
  * blocks is deferred and applied as GEMMs.  Decisions are float32 with IEEE
  * division and round-half-to-even.
  *
- *   W        rows x cols, type wt, read only (never modified).
+ *   W        rows x cols, type wt, read only (never modified), 16-byte aligned.
  *   F, dead  from gptq_factor (dead may be NULL = no dead inputs).
  *   bits     2, 3 or 4.  group % 32 == 0, cols % group == 0, block % group == 0,
  *            block <= 128, rows % 32 == 0, cols % 32 == 0.
@@ -128,10 +128,10 @@ gq_status gptq_factor(const float *H, int64_t cols, float damp, float *F, uint8_
  * packed axis, code k at bits [k*b, k*b+b) of the stream, cut into 32-bit words):
  *   qweight  [cols*bits/32][rows] int32: the codes of each output row packed
  *            along the input axis.
- *   scales   [cols/group][rows] float32.
+ *   scales   [cols/group][rows] float32, 16-byte aligned.
  *   qzeros   [cols/group][rows*bits/32] int32: zero points packed along rows.
- *   codes    rows x cols uint8, may be NULL.
- *   W_hat    rows x cols float32 dequantized weights, may be NULL.
+ *   codes    rows x cols uint8, may be NULL (4-byte aligned).
+ *   W_hat    rows x cols float32 dequantized weights, may be NULL (16-byte aligned).
  *   row_err  rows float32, may be NULL: sum over columns of e_j^2 with
  *            e_j = (w_j - ŵ_j) / U_jj, which equals ΔW_r H_d ΔW_r^T.
  *   ws       >= gptq_sweep_workspace_size(rows, cols, block) bytes.

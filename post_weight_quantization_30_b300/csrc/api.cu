@@ -36,7 +36,7 @@ gq_status check_sweep_args(const void *W, gq_dtype wt, int64_t rows, int64_t col
     if (rows <= 0 || cols <= 0 || rows % 32 || cols % 32) return GQ_EINVAL;
     if (group <= 0 || group % 32 || cols % group) return GQ_EINVAL;
     if (block <= 0 || block > 128 || block % group) return GQ_EINVAL;
-    if (!aligned(W, wt == GQ_F32 ? 16 : 8) || !aligned(scales, 16) || !aligned(qweight, 4) || !aligned(qzeros, 4))
+    if (!aligned(W, 16) || !aligned(scales, 16) || !aligned(qweight, 4) || !aligned(qzeros, 4))
         return GQ_EINVAL;
     if ((codes && !aligned(codes, 4)) || (W_hat && !aligned(W_hat, 16)) || (row_err && !aligned(row_err, 4)))
         return GQ_EINVAL;

@@ -12,33 +12,40 @@
 // is swept its columns of D hold the TF32 hi part of ΔW and those of DL the lo
 // part.  Inside the block the ordinary per-column update runs with Uinv_b.
 //
-// Kernel layout.  One CTA = 32 output rows x one block, 16 warps x 2 rows; 16
-// lanes per row, each owning 8 consecutive block columns in registers.  Per
-// column j the owning lane of each row quantizes (round-half-even; the code
-// decision equals the one from IEEE division w / s, see rint_div), the scaled
-// error e_j = (w_j - ŵ_j) F_jj (= (w_j - ŵ_j) / U_jj) is broadcast within the
-// row's 16 lanes by a shuffle, and every lane updates its columns with row j of
-// Uinv_b (shared memory, broadcast to all warps).  Group min/max are shuffle
-// butterflies.  The epilogue writes ΔW back to D, the optional codes / Ŵ / row
-// errors, the scales, and packs codes and zero points into 32-bit words
-// (coalesced word-rows of 32 output rows).
+// Kernel layout.  One CTA = 32 output rows x one block; lane = row, warp =
+// one 32-column segment of the block (4 warps).  A warp sweeps its segment's
+// columns one after the other: every lane quantizes its row's weight
+// (round-half-even; the code decision equals the one from IEEE division
+// w / s, see rint_div), forms the scaled error e_j = (w_j - ŵ_j) F_jj
+// (= (w_j - ŵ_j) / U_jj) and updates the rest of the segment in registers
+// with row j of Uinv_b (shared memory, read as broadcasts).  The segment's
+// errors then go through shared memory and the warps of later segments apply
+// them as one rank-32 update.  A group's min / max spans whole segments and is
+// reduced through shared memory as well.  The epilogue writes ΔW (split) back
+// to D / DL, the optional codes / Ŵ / row errors, the scales, and packs codes
+// and zero points into 32-bit words (coalesced word-rows of 32 output rows).
 #include "common.cuh"
 
 namespace gq {
 namespace {
 
-constexpr int ROWS = 32;                   // rows per CTA
-constexpr int LPR = 16;                    // lanes per row
-constexpr int CPL = 8;                     // block columns per lane
-constexpr int RPW = 32 / LPR;              // rows per warp (2)
-constexpr int NTHREADS = ROWS / RPW * 32;  // 512
-constexpr int MAXB = LPR * CPL;            // max block width (128)
+constexpr int ROWS = 32;                   // rows per CTA: one per lane
+constexpr int SEG = 32;                    // block columns per segment: one warp each
+constexpr int MAXB = 128;                  // max block width
+constexpr int NSEG = MAXB / SEG;           // segments (warps) per CTA
+constexpr int NTHREADS = NSEG * 32;        // 128
 constexpr int MAXG = MAXB / 32;            // max groups per block (group >= 32)
+constexpr int ELD = SEG + 1;               // row stride of the error staging (conflict-free column reads)
 
 struct SweepSmem {
-    float U[MAXB][MAXB];            // Uinv_b, upper triangle (lower part zero)
+    float U[MAXB][MAXB];            // Uinv_b, upper triangle (lower part zero); read as broadcasts
     float fdiag[MAXB];              // F_jj = 1 / U_jj
-    uint8_t codes[ROWS][MAXB + 8];  // staging for the qweight packing (8-byte aligned rows)
+    float E[NSEG][ROWS][ELD];       // scaled errors of each segment, per row
+    float gmin[NSEG][ROWS];         // group min / max contributions of each segment
+    float gmax[NSEG][ROWS];
+    float gs[ROWS], ginv[ROWS], gz[ROWS];  // grid of the current group, per row
+    float err[NSEG][ROWS];          // per-segment sums of e_j^2
+    uint8_t codes[ROWS][MAXB + 16]; // codes of the block (rows 16-byte aligned, for the packing epilogue)
     uint8_t zeros[MAXG][ROWS];      // staging for the qzeros packing
     float scales[MAXG][ROWS];       // staging for coalesced scale stores
 };
@@ -77,6 +84,17 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, flo
     }
 }
 
+template <typename TW>
+__device__ __forceinline__ void load32(const TW *p, float (&o)[SEG]) {
+#pragma unroll
+    for (int c = 0; c < SEG; c += 8) {
+        float t[8];
+        load8<TW>(p + c, t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[c + i] = t[i];
+    }
+}
+
 // rint(w / s) with w / s rounded as IEEE division does, without dividing in the
 // common case.  r = w * RN(1/s) differs from the exact quotient t by at most
 // 2^-23 |t| and the IEEE quotient differs from t by at most 2^-24 |t|, so both
@@ -108,144 +126,186 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
     SweepSmem &sm = *reinterpret_cast<SweepSmem *>(smem_raw);
     constexpr float maxq = (float)((1 << BITS) - 1);
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane / LPR, l16 = lane % LPR;  // row within the warp, lane within the row
-    const int rl = warp * RPW + sub;               // row within the CTA
+    const int seg = threadIdx.x >> 5, r = threadIdx.x & 31;  // warp = segment, lane = row
     const int64_t row0 = (int64_t)blockIdx.x * ROWS;
-    const int64_t row = row0 + rl;
-    const int cl = l16 * CPL;                      // first block column of this lane
-    const bool lane_on = cl < bw;
-    const unsigned src_base = (unsigned)(sub * LPR);
+    const int64_t row = row0 + r;
+    const bool row_on = row < rows;
+    const int nseg = bw / SEG;
+    const int cl = seg * SEG;  // first block column of this warp
+    const bool seg_on = seg < nseg;
+    const int gseg = group / SEG;  // segments per group
 
+    // Uinv_b into shared memory with asynchronous 16-byte copies, all in flight
+    // at once (the block's rows and columns beyond bw are zero-filled).
     for (int idx = threadIdx.x; idx < MAXB * MAXB / 4; idx += NTHREADS) {
         const int i = idx / (MAXB / 4), j4 = (idx % (MAXB / 4)) * 4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < bw && j4 < bw) v = *reinterpret_cast<const float4 *>(Uinv + (int64_t)i * bw + j4);
-        *reinterpret_cast<float4 *>(&sm.U[i][j4]) = v;
-    }
-    for (int i = threadIdx.x; i < MAXB; i += NTHREADS) sm.fdiag[i] = (i < bw) ? F[(c0 + i) * cols + c0 + i] : 1.f;
-
-    // Weights of the block as updated by every earlier block: W + D.  Dead inputs are zero.
-    float w[CPL];
-    bool dmask[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-        w[c] = 0.f;
-        dmask[c] = false;
-    }
-    if (lane_on && row < rows) {
-        float t[CPL];
-        load8<TW>(W + row * cols + c0 + cl, w);
-        load8<float>(D + row * cols + c0 + cl, t);
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            if (dead) dmask[c] = dead[c0 + cl + c] != 0;
-            w[c] = (dmask[c] ? 0.f : w[c]) + t[c];
+        float *dst = &sm.U[i][j4];
+        if (i < bw && j4 < bw) {
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                         "l"(Uinv + (int64_t)i * bw + j4)
+                         : "memory");
+        } else {
+            *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    for (int i = threadIdx.x; i < MAXB; i += NTHREADS) sm.fdiag[i] = (i < bw) ? F[(c0 + i) * cols + c0 + i] : 1.f;
+
+    // This warp's segment of the row: the original weights w0 (dead inputs
+    // zero) and the weights as updated by every earlier block, w = w0 + D.
+    float w[SEG], w0[SEG];
+    uint32_t dmask = 0;
+#pragma unroll
+    for (int c = 0; c < SEG; ++c) {
+        w[c] = 0.f;
+        w0[c] = 0.f;
+    }
+    if (seg_on && row_on) {
+        float t[SEG];
+        load32<TW>(W + row * cols + c0 + cl, w0);
+        load32<float>(D + row * cols + c0 + cl, t);
+        if (dead) {
+#pragma unroll
+            for (int c = 0; c < SEG; ++c) dmask |= (dead[c0 + cl + c] != 0 ? 1u : 0u) << c;
+        }
+#pragma unroll
+        for (int c = 0; c < SEG; ++c) {
+            w0[c] = ((dmask >> c) & 1u) ? 0.f : w0[c];
+            w[c] = w0[c] + t[c];
+        }
+    }
+    float e2 = 0.f;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
 
-    float s = 1.f, inv_s = 1.f, z = 0.f, e2 = 0.f;
-    float wq[CPL];
-    uint32_t qlo = 0u, qhi = 0u;
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) wq[c] = 0.f;
-
-    for (int o = 0; o < bw / CPL; ++o) {
-#pragma unroll
-        for (int ci = 0; ci < CPL; ++ci) {
-            const int j = o * CPL + ci;
-            if (ci == 0 && (j % group) == 0) {
-                // Group parameters from the current weights of columns [j, j + group).
+    for (int s = 0; s < nseg; ++s) {
+        if (s % gseg == 0) {
+            // A group starts at segment s: min / max over its segments s .. s + gseg - 1,
+            // whose weights carry every update from the columns before it.
+            if (seg >= s && seg < s + gseg) {
                 float lo = 3.402823466e38f, hi = -3.402823466e38f;
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) {
-                    const int col = cl + c;
-                    if (col >= j && col < j + group && col < bw) {
-                        lo = fminf(lo, w[c]);
-                        hi = fmaxf(hi, w[c]);
-                    }
+                for (int c = 0; c < SEG; ++c) {
+                    lo = fminf(lo, w[c]);
+                    hi = fmaxf(hi, w[c]);
                 }
-#pragma unroll
-                for (int off = LPR / 2; off > 0; off >>= 1) {
-                    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-                    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+                sm.gmin[seg][r] = lo;
+                sm.gmax[seg][r] = hi;
+            }
+            __syncthreads();
+            if (seg == s) {
+                float lo = sm.gmin[s][r], hi = sm.gmax[s][r];
+                for (int k = 1; k < gseg; ++k) {
+                    lo = fminf(lo, sm.gmin[s + k][r]);
+                    hi = fmaxf(hi, sm.gmax[s + k][r]);
                 }
                 float xmin = fminf(lo, 0.f), xmax = fmaxf(hi, 0.f);
                 if (xmin == 0.f && xmax == 0.f) {
                     xmin = -1.f;
                     xmax = 1.f;
                 }
-                s = __fdiv_rn(xmax - xmin, maxq);
-                inv_s = __fdiv_rn(1.f, s);
-                z = rintf(__fdiv_rn(-xmin, s));
-                if (l16 == 0) {
-                    sm.zeros[j / group][rl] = (uint8_t)z;
-                    sm.scales[j / group][rl] = s;
+                const float sc = __fdiv_rn(xmax - xmin, maxq);
+                sm.gs[r] = sc;
+                sm.ginv[r] = __fdiv_rn(1.f, sc);
+                sm.gz[r] = rintf(__fdiv_rn(-xmin, sc));
+                sm.zeros[(s * SEG) / group][r] = (uint8_t)sm.gz[r];
+                sm.scales[(s * SEG) / group][r] = sc;
+            }
+        }
+        if (seg == s) {
+            // The segment's 32 columns, one after the other; every lane (row) quantizes
+            // its own weight, and the error updates the rest of the segment in registers.
+            const float sc = sm.gs[r], inv_s = sm.ginv[r], z = sm.gz[r];
+            float wq[SEG], ebuf[SEG];
+            uint32_t cw[SEG / 4];
+#pragma unroll
+            for (int k = 0; k < SEG / 4; ++k) cw[k] = 0u;
+#pragma unroll
+            for (int ci = 0; ci < SEG; ++ci) {
+                const int j = cl + ci;
+                const float wv = w[ci];
+                const float q = fminf(fmaxf(rint_div(wv, sc, inv_s) + z, 0.f), maxq);
+                const float dq = sc * (q - z);
+                wq[ci] = dq;
+                cw[ci / 4] |= ((uint32_t)q) << (8 * (ci % 4));
+                const float e = (wv - dq) * sm.fdiag[j];
+                ebuf[ci] = e;
+                e2 = fmaf(e, e, e2);
+                // Uinv_b is upper triangular: only the later columns of the segment move here.
+#pragma unroll
+                for (int c4 = ((ci + 1) / 4) * 4; c4 < SEG; c4 += 4) {
+                    const float4 u = *reinterpret_cast<const float4 *>(&sm.U[j][cl + c4]);
+                    if (c4 + 0 > ci) w[c4 + 0] = fmaf(-e, u.x, w[c4 + 0]);
+                    if (c4 + 1 > ci) w[c4 + 1] = fmaf(-e, u.y, w[c4 + 1]);
+                    if (c4 + 2 > ci) w[c4 + 2] = fmaf(-e, u.z, w[c4 + 2]);
+                    if (c4 + 3 > ci) w[c4 + 3] = fmaf(-e, u.w, w[c4 + 3]);
                 }
             }
-            float e = 0.f;
-            if (l16 == o) {
-                const float wv = w[ci];
-                const float q = fminf(fmaxf(rint_div(wv, s, inv_s) + z, 0.f), maxq);
-                const float dq = s * (q - z);
-                wq[ci] = dq;
-                if (ci < 4)
-                    qlo |= ((uint32_t)q) << (8 * ci);
-                else
-                    qhi |= ((uint32_t)q) << (8 * (ci - 4));
-                e = (wv - dq) * sm.fdiag[j];
-                e2 = fmaf(e, e, e2);
+#pragma unroll
+            for (int ci = 0; ci < SEG; ++ci) sm.E[s][r][ci] = ebuf[ci];
+            *reinterpret_cast<uint4 *>(&sm.codes[r][cl]) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            *reinterpret_cast<uint4 *>(&sm.codes[r][cl + 16]) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            if (row_on) {
+                float *dp = D + row * cols + c0 + cl;
+                float *lp = DL + row * cols + c0 + cl;
+#pragma unroll
+                for (int c = 0; c < SEG; c += 4) {
+                    // ΔW as its TF32 split: the operand of the deferred-update GEMMs.
+                    float dw[4], dh[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        dw[u] = w0[c + u] - wq[c + u];
+                        dh[u] = tf32_hi(dw[u]);
+                    }
+                    *reinterpret_cast<float4 *>(dp + c) = make_float4(dh[0], dh[1], dh[2], dh[3]);
+                    *reinterpret_cast<float4 *>(lp + c) =
+                        make_float4(dw[0] - dh[0], dw[1] - dh[1], dw[2] - dh[2], dw[3] - dh[3]);
+                    if (W_hat)
+                        *reinterpret_cast<float4 *>(W_hat + row * cols + c0 + cl + c) =
+                            make_float4(wq[c], wq[c + 1], wq[c + 2], wq[c + 3]);
+                }
             }
-            const float eb = __shfl_sync(0xffffffffu, e, src_base + (unsigned)o);
-            const float4 u0 = *reinterpret_cast<const float4 *>(&sm.U[j][cl]);
-            const float4 u1 = *reinterpret_cast<const float4 *>(&sm.U[j][cl + 4]);
-            // Uinv_b is upper triangular: columns < j get zero updates; column j
-            // itself is already quantized and its working value is unused.
-            w[0] = fmaf(-eb, u0.x, w[0]);
-            w[1] = fmaf(-eb, u0.y, w[1]);
-            w[2] = fmaf(-eb, u0.z, w[2]);
-            w[3] = fmaf(-eb, u0.w, w[3]);
-            w[4] = fmaf(-eb, u1.x, w[4]);
-            w[5] = fmaf(-eb, u1.y, w[5]);
-            w[6] = fmaf(-eb, u1.z, w[6]);
-            w[7] = fmaf(-eb, u1.w, w[7]);
         }
+        __syncthreads();
+        if (seg > s && seg_on) {
+            // Rank-32 update of this warp's segment by segment s: w -= E_s U[seg s, this segment].
+#pragma unroll 4
+            for (int i = 0; i < SEG; ++i) {
+                const float ei = sm.E[s][r][i];
+                const float *ur = &sm.U[s * SEG + i][cl];
+#pragma unroll
+                for (int c4 = 0; c4 < SEG; c4 += 4) {
+                    const float4 u = *reinterpret_cast<const float4 *>(ur + c4);
+                    w[c4 + 0] = fmaf(-ei, u.x, w[c4 + 0]);
+                    w[c4 + 1] = fmaf(-ei, u.y, w[c4 + 1]);
+                    w[c4 + 2] = fmaf(-ei, u.z, w[c4 + 2]);
+                    w[c4 + 3] = fmaf(-ei, u.w, w[c4 + 3]);
+                }
+            }
+        }
+        __syncthreads();
     }
 
-    // Epilogue.
-    float err = e2;
+    // Epilogue: row errors, codes, scales, packed words.
+    sm.err[seg][r] = e2;
+    __syncthreads();
+    if (seg == 0 && row_on && row_err) {
+        float t = 0.f;
+        for (int k = 0; k < nseg; ++k) t += sm.err[k][r];
+        row_err[row] += t;
+    }
+    if (codes && row_on && seg_on) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(&sm.codes[r][cl]);
+        uint8_t *dst = codes + row * cols + c0 + cl;
+        if (((uintptr_t)dst & 15) == 0) {
+            reinterpret_cast<uint4 *>(dst)[0] = src[0];
+            reinterpret_cast<uint4 *>(dst)[1] = src[1];
+        } else {  // the library only requires 4-byte alignment of codes
+            const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src);
 #pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1) err += __shfl_xor_sync(0xffffffffu, err, off);
-    if (row < rows) {
-        if (l16 == 0 && row_err) row_err[row] += err;
-        if (lane_on) {
-            float w0[CPL], dw[CPL];
-            load8<TW>(W + row * cols + c0 + cl, w0);
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) dw[c] = (dmask[c] ? 0.f : w0[c]) - wq[c];
-            // ΔW as its TF32 split: the operand of the deferred-update GEMMs.
-            float dh[CPL];
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) dh[c] = tf32_hi(dw[c]);
-            float *dp = D + row * cols + c0 + cl;
-            float *lp = DL + row * cols + c0 + cl;
-            *reinterpret_cast<float4 *>(dp) = make_float4(dh[0], dh[1], dh[2], dh[3]);
-            *reinterpret_cast<float4 *>(dp + 4) = make_float4(dh[4], dh[5], dh[6], dh[7]);
-            *reinterpret_cast<float4 *>(lp) =
-                make_float4(dw[0] - dh[0], dw[1] - dh[1], dw[2] - dh[2], dw[3] - dh[3]);
-            *reinterpret_cast<float4 *>(lp + 4) =
-                make_float4(dw[4] - dh[4], dw[5] - dh[5], dw[6] - dh[6], dw[7] - dh[7]);
-            if (W_hat) {
-                float *hp = W_hat + row * cols + c0 + cl;
-                *reinterpret_cast<float4 *>(hp) = make_float4(wq[0], wq[1], wq[2], wq[3]);
-                *reinterpret_cast<float4 *>(hp + 4) = make_float4(wq[4], wq[5], wq[6], wq[7]);
-            }
-            if (codes) *reinterpret_cast<uint2 *>(codes + row * cols + c0 + cl) = make_uint2(qlo, qhi);
-            *reinterpret_cast<uint2 *>(&sm.codes[rl][cl]) = make_uint2(qlo, qhi);
+            for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t *>(dst)[i] = s32[i];
         }
     }
-    __syncthreads();
 
     // scales [cols/group][rows]: 32 consecutive rows per group.
     const int ng = bw / group;
