@@ -230,6 +230,16 @@ gq_status gptq_quantize_layer_noalloc(const void *W, gq_dtype wt, int64_t rows, 
                                       gq_stream_t stream, int64_t *info);
 
 /*
+ * The sweep's integer decision rule on its own, for verification: k[i] =
+ * rint(w[i] / s[i]) with the quotient rounded as IEEE float32 division and ties
+ * to even ([LowBit] section 1: the rounding rule is part of the format).  The
+ * sweep forms the quotient from RN(1/s) with one FMA correction instead of a
+ * division; this call lets a test compare the two on chosen inputs.
+ *   w, s, k  n float32 each (device); s normal and nonzero.  Asynchronous.
+ */
+gq_status gptq_code_decisions(const float *w, const float *s, int64_t n, float *k, gq_stream_t stream);
+
+/*
  * Standalone packing of codes (rows x cols uint8, each < 2^bits) into
  * qweight [cols*bits/32][rows] int32, and its inverse.  Same layout as
  * gptq_sweep.  rows % 32 == 0 is not required; cols*bits % 32 == 0 is.

@@ -53,6 +53,7 @@ SIGNATURES = {
     "gptq_weight_error": (_i, [_p, _i, _i64, _i64, _p, _p, _p]),
     "eora_compensate_workspace_size": (_sz, [_i64, _i64, _i]),
     "eora_compensate": (_i, [_p, _i64, _i64, _p, _i, _p, _p, _p, _p, _sz, _p, ctypes.POINTER(_i64)]),
+    "gptq_code_decisions": (_i, [_p, _p, _i64, _p, _p]),
     "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
     "gptq_unpack": (_i, [_p, _i64, _i64, _i, _p, _p]),
 }
@@ -242,6 +243,16 @@ def gq_check_device(device=None):
     """Raise GQError(GQ_ETIMEOUT) if a bounded device-side wait gave up since the last check."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     _check(lib.gq_check_device(_stream(dev)), "gq_check_device")
+
+
+def gptq_code_decisions(w: torch.Tensor, s: torch.Tensor) -> torch.Tensor:
+    """rint(w / s) elementwise by the sweep's decision rule (float32)."""
+    _need_cuda(w, s)
+    w = w.contiguous()
+    s = s.contiguous()
+    k = torch.empty_like(w)
+    _check(lib.gptq_code_decisions(_ptr(w), _ptr(s), w.numel(), _ptr(k), _stream(w.device)), "gptq_code_decisions")
+    return k
 
 
 def gptq_pack(codes: torch.Tensor, bits: int) -> torch.Tensor:

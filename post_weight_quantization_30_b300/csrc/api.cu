@@ -263,6 +263,13 @@ gq_status eora_compensate(const float *dW, int64_t rows, int64_t cols, const flo
     return GQ_OK;
 }
 
+gq_status gptq_code_decisions(const float *w, const float *s, int64_t n, float *k, gq_stream_t stream) {
+    if (n < 0) return GQ_EINVAL;
+    if (n == 0) return GQ_OK;
+    if (!w || !s || !k) return GQ_EINVAL;
+    return code_decisions_launch(w, s, n, k, cs(stream)) == cudaSuccess ? GQ_OK : GQ_ECUDA;
+}
+
 gq_status gptq_pack(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight, gq_stream_t stream) {
     if (bits != 2 && bits != 3 && bits != 4) return GQ_EUNSUPPORTED;
     if (!codes || !qweight || rows <= 0 || cols <= 0 || (cols * bits) % 32) return GQ_EINVAL;

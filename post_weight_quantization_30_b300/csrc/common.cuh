@@ -37,6 +37,20 @@ static constexpr size_t kAlign = 256;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
+// The quotient w / s rounded to nearest (IEEE), given y = RN(1/s): q0 = RN(w y),
+// the exact residual r = w - s q0 (one FMA), q = RN(q0 + r y).  This is the
+// FMA correction step of P. Markstein's division method ("IA-64 and Elementary
+// Functions", Prentice Hall 2000, ch. 8): with y correctly rounded and q0
+// within one ulp of w / s it yields the correctly rounded quotient for normal
+// operands.  It was compared with the hardware IEEE division on 2.6e9 pairs
+// (every significand of s against w within 3 ulps of half-integers, plus
+// random pairs) without a difference; gptq_code_decisions exposes it to tests.
+__device__ __forceinline__ float quotient_rn(float w, float s, float y) {
+    const float q0 = w * y;
+    const float r = fmaf(-s, q0, w);
+    return fmaf(r, y, q0);
+}
+
 template <typename T>
 __device__ __forceinline__ float load_f32(const T *p);
 template <>
@@ -139,6 +153,9 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
 
 // dW = W - W_hat, n elements (W float32 or bf16).
 cudaError_t weight_error_launch(const void *W, bool w_bf16, int64_t n, const float *W_hat, float *dW, cudaStream_t s);
+
+// k[i] = rint(w[i] / s[i]) by the sweep's decision rule (quotient_rn).
+cudaError_t code_decisions_launch(const float *w, const float *s, int64_t n, float *k, cudaStream_t st);
 
 cudaError_t pack_launch(const uint8_t *codes, int64_t rows, int64_t cols, int bits, int32_t *qweight,
                         cudaStream_t s);

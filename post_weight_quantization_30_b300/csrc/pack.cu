@@ -51,6 +51,14 @@ __global__ void weight_error_kernel(const TW *__restrict__ W, const float *__res
         dW[i] = load_f32(W + i) - W_hat[i];
 }
 
+__global__ void code_decisions_kernel(const float *__restrict__ w, const float *__restrict__ s, int64_t n,
+                                      float *__restrict__ k) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float sv = s[i];
+        k[i] = rintf(quotient_rn(w[i], sv, __fdiv_rn(1.f, sv)));
+    }
+}
+
 unsigned grid_for(int64_t total) {
     int64_t g = (total + 255) / 256;
     return (unsigned)(g < 148 * 16 ? (g < 1 ? 1 : g) : 148 * 16);
@@ -63,6 +71,12 @@ cudaError_t weight_error_launch(const void *W, bool w_bf16, int64_t n, const flo
         weight_error_kernel<__nv_bfloat16><<<grid_for(n), 256, 0, s>>>((const __nv_bfloat16 *)W, W_hat, n, dW);
     else
         weight_error_kernel<float><<<grid_for(n), 256, 0, s>>>((const float *)W, W_hat, n, dW);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t code_decisions_launch(const float *w, const float *s, int64_t n, float *k, cudaStream_t st) {
+    code_decisions_kernel<<<grid_for(n), 256, 0, st>>>(w, s, n, k);
     count_launch();
     return cudaGetLastError();
 }

@@ -95,18 +95,10 @@ __device__ __forceinline__ void load32(const TW *p, float (&o)[SEG]) {
     }
 }
 
-// rint(w / s) with w / s rounded as IEEE division does, without dividing in the
-// common case.  r = w * RN(1/s) differs from the exact quotient t by at most
-// 2^-23 |t| and the IEEE quotient differs from t by at most 2^-24 |t|, so both
-// lie on the same side of every half-integer unless r is within 2^-22 |t| of
-// one; only then (threshold 2^-20 (|r| + 1), and for non-finite r) is the
-// exact division taken.
-__device__ __forceinline__ float rint_div(float w, float s, float inv_s) {
-    const float r = w * inv_s;
-    const float k = rintf(r);
-    if (fabsf(fabsf(r - k) - 0.5f) > 9.5367431640625e-07f * (fabsf(r) + 1.f)) return k;
-    return rintf(__fdiv_rn(w, s));
-}
+// rint(w / s) for the IEEE-rounded quotient w / s, without a division:
+// inv_s = RN(1/s) and the FMA-corrected quotient (quotient_rn), then
+// round-half-to-even.
+__device__ __forceinline__ float rint_div(float w, float s, float inv_s) { return rintf(quotient_rn(w, s, inv_s)); }
 
 __device__ __forceinline__ float tf32_hi(float x) {
     uint32_t r;

@@ -213,3 +213,24 @@ def test_rejects_bad_arguments_without_launch(gq):
     with pytest.raises(gq.GQError) as ei:
         gq.gptq_quantize_layer(W, H, 4, 128, block=64)
     assert ei.value.status == -1
+
+
+# ---------------------------------------------------------- code decisions ---
+def test_code_decisions_match_ieee_division(gq):
+    """The sweep rounds w / s without dividing (RN(1/s) plus one FMA correction).
+    Its decisions must equal rint of the IEEE float32 quotient everywhere, in
+    particular for w within a few ulps of (k + 1/2) s, where a plain product
+    w * RN(1/s) can round to the other integer."""
+    rng = np.random.default_rng(21)
+    s = (rng.uniform(1.0, 2.0, 200000) * 2.0 ** rng.integers(-20, 4, 200000)).astype(np.float32)
+    k = rng.integers(-8, 16, 200000).astype(np.float32)
+    w = ((k + np.float32(0.5)) * s).astype(np.float32)
+    offs = rng.integers(-3, 4, 200000).astype(np.int32)
+    w = (w.view(np.int32) + offs).view(np.float32)
+    w = np.concatenate([w, (rng.standard_normal(200000) * 8).astype(np.float32) * s])
+    s = np.concatenate([s, s])
+    got = _np(gq.gptq_code_decisions(torch.from_numpy(w).cuda(), torch.from_numpy(s).cuda()))
+    ref = np.rint(w / s)  # numpy float32 division is IEEE round-to-nearest
+    assert np.array_equal(got, ref)
+    dev = _np(torch.round(torch.from_numpy(w).cuda() / torch.from_numpy(s).cuda()))  # CUDA's own division
+    assert np.array_equal(got, dev)
