@@ -86,9 +86,11 @@ cudaError_t sgemm_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_
 // result (leading dimension ldcs).  Row strides must be multiples of 4
 // elements and operand bases 16-byte aligned (gemm3_supported).
 bool gemm3_supported(const void *p, int64_t ld);
+// split_row0 / split_ncols restrict the split output to rows >= split_row0 and
+// columns < split_ncols of C, written at row r - split_row0 (-1: all columns).
 cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi, const float *Alo, int64_t lda,
                   const float *Bhi, const float *Blo, int64_t ldb, float beta, float *C, int64_t ldc, int tri,
-                  float *Chi, float *Clo, int64_t ldcs, cudaStream_t s);
+                  float *Chi, float *Clo, int64_t ldcs, cudaStream_t s, int split_row0 = 0, int split_ncols = -1);
 // C (M x N, row-major, ldc = N) = A B^T as gemm3, with K split into `slices`
 // ranges computed by separate CTAs into `partials` (slices * M * N floats)
 // and summed in a fixed order.

@@ -426,7 +426,7 @@ struct CholCtx {
 
 // One panel: diagonal block (factor + inverse), then the rows below solved,
 // P <- P L^-T, written to F and, split, to (LThi, LTlo) or (Phi, Plo).
-cudaError_t chol_panel(const CholCtx &c, int64_t k0, bool rec) {
+cudaError_t chol_panel(const CholCtx &c, int64_t k0, bool rec, bool p_split_ready = false) {
     const int64_t cols = c.cols;
     const int kb = (int)((cols - k0) < NB ? (cols - k0) : NB);
     const int64_t k1 = k0 + kb;
@@ -439,8 +439,8 @@ cudaError_t chol_panel(const CholCtx &c, int64_t k0, bool rec) {
     if (!more) return cudaGetLastError();
     const int64_t rest = cols - k1;
     float *P = c.F + k1 * cols + k0;
-    cudaError_t e = split_tf32(P, rest, kb, cols, c.Phi, c.Plo, NB, c.s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
+    if (!p_split_ready && (e = split_tf32(P, rest, kb, cols, c.Phi, c.Plo, NB, c.s)) != cudaSuccess) return e;
     if (rec)
         return gemm3(rest, kb, kb, 1.f, c.Phi, c.Plo, NB, c.Lhi, c.Llo, NB, 0.f, P, cols, 0, c.LThi + k1 * cols + k0,
                      c.LTlo + k1 * cols + k0, cols, c.s);
@@ -451,17 +451,23 @@ cudaError_t chol_panel(const CholCtx &c, int64_t k0, bool rec) {
 // them down) carry every update from the columns left of panel a.  The left
 // half is factored, its whole contribution to the right half is applied as
 // one GEMM (K = the left half's width), then the right half is factored.
-cudaError_t chol_rec(const CholCtx &c, int64_t a, int64_t b) {
-    if (b - a == 1) return chol_panel(c, a * NB, true);
+// p_split_ready: the split of panel a's rows below its diagonal block is
+// already in (Phi, Plo), written by the GEMM that last updated the panel.
+cudaError_t chol_rec(const CholCtx &c, int64_t a, int64_t b, bool p_split_ready) {
+    if (b - a == 1) return chol_panel(c, a * NB, true, p_split_ready);
     const int64_t m = (a + b) / 2;
-    cudaError_t e = chol_rec(c, a, m);
+    cudaError_t e = chol_rec(c, a, m, p_split_ready);
     if (e != cudaSuccess) return e;
     const int64_t c0 = a * NB, cm = m * NB, c1 = (b * NB < c.cols) ? b * NB : c.cols;
+    // The update of panels [m, b) is the last one panel m receives (the next
+    // launch factors it), so its epilogue also emits the split of panel m's rows
+    // below the diagonal block: C rows >= NB, columns < NB.
+    const bool emit = cm + NB < c.cols;
     e = gemm3(c.cols - cm, c1 - cm, cm - c0, -1.f, c.LThi + cm * c.cols + c0, c.LTlo + cm * c.cols + c0, c.cols,
               c.LThi + cm * c.cols + c0, c.LTlo + cm * c.cols + c0, c.cols, 1.f, c.F + cm * c.cols + cm, c.cols, 1,
-              nullptr, nullptr, 0, c.s);
+              emit ? c.Phi : nullptr, emit ? c.Plo : nullptr, NB, c.s, NB, NB);
     if (e != cudaSuccess) return e;
-    return chol_rec(c, m, b);
+    return chol_rec(c, m, b, emit);
 }
 
 }  // namespace
@@ -498,7 +504,7 @@ cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, flo
     const bool tc = (cols % 4) == 0;
     const int64_t npanel = (cols + NB - 1) / NB;
     if (tc && cols >= REC_MIN) {
-        cudaError_t e = chol_rec(c, 0, npanel);
+        cudaError_t e = chol_rec(c, 0, npanel, false);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

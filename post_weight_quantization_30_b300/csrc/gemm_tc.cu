@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
     gemm3_kernel(const __grid_constant__ CUtensorMap ahi, const __grid_constant__ CUtensorMap alo,
                  const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo, float *C,
                  int64_t ldc, int M, int N, int K, float alpha, float beta, int tri, float *Chi, float *Clo,
-                 int64_t ldcs, int ktiles_per_z, int64_t c_zstride) {
+                 int64_t ldcs, int ktiles_per_z, int64_t c_zstride, int split_row0, int split_ncols) {
     const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
     if (tri == 1 && n0 > m0 + GM - 1) return;  // tile entirely above the diagonal
     // Split K (gridDim.z > 1): slice z covers k-tiles [z * ktiles_per_z, ...) and
@@ -268,27 +268,31 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
                     }
                     float *cp = C + (int64_t)r * ldc + c;
                     float h[4], l[4];
-                    if (Chi) {
+                    // The split of the result goes to Chi / Clo for rows >= split_row0 and
+                    // columns < split_ncols, at row r - split_row0.
+                    const bool sp = Chi && r >= split_row0 && c < split_ncols;
+                    const int64_t so = (int64_t)(r - split_row0) * ldcs + c;
+                    if (sp) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             h[e] = tf32_hi(v[e]);
                             l[e] = v[e] - h[e];
                         }
                     }
-                    if (full4) {
+                    if (full4 && (!sp || c + 3 < split_ncols)) {
                         *reinterpret_cast<float4 *>(cp) = make_float4(v[0], v[1], v[2], v[3]);
-                        if (Chi) {
-                            *reinterpret_cast<float4 *>(Chi + (int64_t)r * ldcs + c) = make_float4(h[0], h[1], h[2], h[3]);
-                            *reinterpret_cast<float4 *>(Clo + (int64_t)r * ldcs + c) = make_float4(l[0], l[1], l[2], l[3]);
+                        if (sp) {
+                            *reinterpret_cast<float4 *>(Chi + so) = make_float4(h[0], h[1], h[2], h[3]);
+                            *reinterpret_cast<float4 *>(Clo + so) = make_float4(l[0], l[1], l[2], l[3]);
                         }
                     } else {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             if (c + e < N) {
                                 cp[e] = v[e];
-                                if (Chi) {
-                                    Chi[(int64_t)r * ldcs + c + e] = h[e];
-                                    Clo[(int64_t)r * ldcs + c + e] = l[e];
+                                if (sp && c + e < split_ncols) {
+                                    Chi[so + e] = h[e];
+                                    Clo[so + e] = l[e];
                                 }
                             }
                         }
@@ -364,7 +368,8 @@ bool gemm3_supported(const void *p, int64_t ld) { return ((uintptr_t)p % 16) == 
 
 cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi, const float *Alo, int64_t lda,
                   const float *Bhi, const float *Blo, int64_t ldb, float beta, float *C, int64_t ldc, int tri,
-                  float *Chi, float *Clo, int64_t ldcs, cudaStream_t s) {
+                  float *Chi, float *Clo, int64_t ldcs, cudaStream_t s, int split_row0, int split_ncols) {
+    if (split_ncols < 0) split_ncols = (int)N;
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (K <= 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return cudaErrorInvalidValue;
     static bool attr_set = false;
@@ -380,7 +385,7 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
     const int kt_all = (int)((K + GK - 1) / GK);
     gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta,
-                                                    tri, Chi, Clo, ldcs, kt_all, 0);
+                                                    tri, Chi, Clo, ldcs, kt_all, 0, split_row0, split_ncols);
     count_launch();
     return cudaGetLastError();
 }
@@ -405,7 +410,7 @@ cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, cons
     const int z = (kt_all + per - 1) / per;
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM), (unsigned)z);
     gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, partials, N, (int)M, (int)N, (int)K, 1.f, 0.f,
-                                                    0, nullptr, nullptr, 0, per, M * N);
+                                                    0, nullptr, nullptr, 0, per, M * N, 0, 0);
     count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

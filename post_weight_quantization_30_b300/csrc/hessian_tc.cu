@@ -15,8 +15,9 @@
 //   tcgen05.mma (kind::f16, bf16 x bf16 -> f32, M = 128, N = 256, K = 16) into a
 //   256-column TMEM accumulator; tcgen05.commit releases shared-memory stages
 //   and finally signals the epilogue.
-// * Epilogue: the four warps read their 32 TMEM lanes (one output row each)
-//   with tcgen05.ld and add 2 * acc into H.
+// * Epilogue: eight warps read their TMEM lanes (one output row each, half of
+//   the columns) with tcgen05.ld after every 512 tokens, add the partial sums
+//   into float32 registers and finally add 2 * sum into H.
 // * Every wait on an mbarrier is bounded (clock64 budget); on expiry the CTA
 //   records an error flag, drains what it issued, frees TMEM and returns.
 #include "tc_common.cuh"
@@ -38,12 +39,12 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 constexpr uint32_t TMEM_COLS = 256;
 
 // Warp roles: 0 = TMA producer, 1 = MMA issuer, 2..9 = accumulator warps.
-// The tensor-core accumulator is summed over KF k-tiles (256 tokens) at a
+// The tensor-core accumulator is summed over KF k-tiles (512 tokens) at a
 // time in one of two TMEM buffers; the accumulator warps add each partial
 // sum into float32 registers (round-to-nearest) while the MMAs fill the other
 // buffer.  Long in-TMEM accumulation is avoided because each accumulate step
 // of the tensor core loses about half an ulp of the running sum.
-constexpr int KF = 4;
+constexpr int KF = 8;
 constexpr int GROUP = 16;  // tile-rows per scheduling group
 constexpr int NWARPS = 10;
 constexpr int EPI_WARPS = 8;

@@ -74,6 +74,7 @@ def test_full_size_layer(gq, name):
         og.hessian(bf16_bits_to_f32(xa[r0:r0 + 8192]).astype(np.float64), H0)
     del xa
     rel = np.linalg.norm(Hg - H0) / np.linalg.norm(H0)
+    print(f"{name}: H relative Frobenius error {rel:.3e}")
     assert rel <= 1e-5, rel
 
     # Oracle factor and sweep of sampled rows.

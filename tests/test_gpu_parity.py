@@ -234,3 +234,52 @@ def test_code_decisions_match_ieee_division(gq):
     assert np.array_equal(got, ref)
     dev = _np(torch.round(torch.from_numpy(w).cuda() / torch.from_numpy(s).cuda()))  # CUDA's own division
     assert np.array_equal(got, dev)
+
+
+# --------------------------------------------------------- degenerate cases ---
+def test_zero_rows_and_zero_groups(gq):
+    """An all-zero row (every group falls back to the [-1, 1] grid, z = rint(maxq / 2)
+    rounded half to even) and rows whose first group is zero."""
+    rows, cols, bits, group = 64, 256, 4, 128
+    spec, wa, w64, xa, x64 = _layer_inputs(rows, cols, 2048, bits, group, 128, (16,))
+    w32 = w64.astype(np.float32)
+    w32[5, :] = 0.0
+    w32[17, :group] = 0.0
+    w32[40, :] = 0.0
+    H = torch.zeros((cols, cols), dtype=torch.float32, device="cuda")
+    gq.gptq_hessian_accumulate(H, to_device(xa, spec.X.dtype))
+    H0 = og.hessian(x64)
+    ref = og.quantize_layer(w32.astype(np.float64), H0, bits, group, 0.01)
+    out = gq.gptq_quantize_layer(torch.from_numpy(w32).cuda(), H, bits, group, 128, 0.01)
+    codes = _np(out["codes"])
+    assert np.array_equal(codes[[5, 40]], ref["codes"][[5, 40]])
+    # grid [-1, 1]: s = RN(2 / 15) lies just above 2/15, so -xmin / s = 7.4999995 and z = 7
+    z = np.rint(np.float32(1.0) / (np.float32(2.0) / np.float32(15.0)))
+    assert z == 7 and np.all(codes[5] == z) and np.all(_np(out["W_hat"])[5] == 0)
+    _check_against_oracle(gq, out, ref, w32.astype(np.float64), H0, bits, group, rows, cols)
+
+
+@pytest.mark.parametrize("bits,group", [(2, 64), (3, 128), (4, 32)])
+def test_diagonal_hessian_is_round_to_nearest(gq, bits, group):
+    """With a diagonal H no error propagates: GPTQ is group-wise round-to-nearest, exactly."""
+    rows, cols = 96, 384
+    rng = np.random.default_rng(bits)
+    w = (rng.standard_normal((rows, cols)) * 0.02).astype(np.float32)
+    d = rng.uniform(0.5, 2.0, cols).astype(np.float32)
+    H = torch.from_numpy(np.diag(d)).cuda()
+    out = gq.gptq_quantize_layer(torch.from_numpy(w).cuda(), H, bits, group, 128, 0.01)
+    ref = og.rtn(w.astype(np.float64), bits, group)
+    assert np.array_equal(_np(out["codes"]), ref["codes"])
+    assert np.array_equal(_np(out["W_hat"]), ref["W_hat"])
+    assert np.array_equal(opk.unpack_qzeros(_np(out["qzeros"]), bits, rows), ref["zeros"])
+
+
+def test_single_block_layer(gq):
+    rows, cols, bits, group, block = 32, 64, 2, 32, 64
+    spec, wa, w64, xa, x64 = _layer_inputs(rows, cols, 512, bits, group, block, (17,))
+    H = torch.zeros((cols, cols), dtype=torch.float32, device="cuda")
+    gq.gptq_hessian_accumulate(H, to_device(xa, spec.X.dtype))
+    H0 = og.hessian(x64)
+    ref = og.quantize_layer(w64, H0, bits, group, 0.01)
+    out = gq.gptq_quantize_layer(to_device(wa, spec.W.dtype), H, bits, group, block, 0.01)
+    _check_against_oracle(gq, out, ref, w64, H0, bits, group, rows, cols)
