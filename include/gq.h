@@ -189,7 +189,7 @@ gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t co
  *          projected error ΔW', in descending order.
  *   ws     >= eora_compensate_workspace_size(rows, cols, r) bytes.
  * Computed in float32 with a block subspace iteration of width min(2r, cols)
- * (40 iterations) and a Rayleigh-Ritz step.  When σ_r and σ_{r+1} are close,
+ * (30 iterations) and a Rayleigh-Ritz step.  When σ_r and σ_{r+1} are close,
  * the rank-r subspace is not unique and B A may differ from another exact
  * solution by directions of nearly equal σ; the compensated loss and σ do not.
  * Synchronizes `stream` once (after the factorization of H).

@@ -30,7 +30,7 @@ namespace gq {
 namespace {
 
 constexpr int EORA_MAX_K = 128;   // subspace width limit (r <= 64)
-constexpr int EORA_ITERS = 40;    // subspace iterations
+constexpr int EORA_ITERS = 30;    // subspace iterations
 constexpr int SPLITK = 64;        // K slices of the thin Gram products
 
 // Marks a dead input (zero diagonal of H) as a failed pivot: EoRA needs a
@@ -113,9 +113,18 @@ __global__ void __launch_bounds__(JT) jacobi_eig_kernel(const float *__restrict_
     }
     for (int i = t; i < kk; i += JT) pos[i] = i;
     for (int i = t; i < np; i += JT) sn[i] = 0.f;
+    __shared__ float tol;
+    __syncthreads();
+    if (t == 0) {
+        // Off-diagonal entries below 1e-7 of the largest diagonal entry are at the
+        // float32 rounding level of T: they move no eigenvalue by more than that.
+        float m = 0.f;
+        for (int i = 0; i < k; ++i) m = fmaxf(m, fabsf(T[i * JLD + i]));
+        tol = 1e-7f * m;
+    }
     __syncthreads();
 
-    for (int sweep = 0; sweep < 30; ++sweep) {
+    for (int sweep = 0; sweep < 15; ++sweep) {
         if (t == 0) rotated = 0;
         __syncthreads();
         for (int round = 0; round < kk - 1; ++round) {
@@ -132,9 +141,8 @@ __global__ void __launch_bounds__(JT) jacobi_eig_kernel(const float *__restrict_
                 if (q < k) {
                     const float apq = T[p * JLD + q];
                     const float app = T[p * JLD + p], aqq = T[q * JLD + q];
-                    // Rotate unless a_pq is negligible beside both diagonal entries.
-                    const float g = 100.f * fabsf(apq);
-                    if (!(fabsf(app) + g == fabsf(app) && fabsf(aqq) + g == fabsf(aqq))) {
+                    // Rotate unless a_pq is at the rounding level of T.
+                    if (fabsf(apq) > tol) {
                         const float tau = (aqq - app) / (2.f * apq);
                         const float tt = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
                         c = 1.f / sqrtf(1.f + tt * tt);
@@ -270,7 +278,7 @@ struct EoraWs {
     DeviceStatus *st;
     float *Linv, *F, *M, *G, *ZT, *ZT2, *Gm, *part, *lam, *Wt, *VrT;
     // tensor-core path only (null otherwise)
-    float *FThi, *FTlo, *dWhi, *dWlo, *Mthi, *Mtlo, *Ghi, *Glo, *Zhi, *Zlo;
+    float *FThi, *FTlo, *dWhi, *dWlo, *Mhi, *Mlo, *Mthi, *Mtlo, *Ghi, *Glo, *Zhi, *Zlo;
     uint8_t *dead;
 };
 
@@ -303,7 +311,7 @@ size_t eora_layout(int64_t rows, int64_t cols, int r, EoraWs *w, char *base) {
     t.Linv = (float *)take(cholesky_scratch_floats(cols > 128 ? cols : 128) * sizeof(float));
     t.F = (float *)take(cc);
     t.dead = (uint8_t *)take((size_t)cols);
-    t.M = (float *)take(rc);  // M (rows x cols) on the SIMT path, M^T (cols x rows) on the tensor path
+    t.M = (float *)take(rc);  // M = dW F (rows x cols)
     t.G = (float *)take(cc);
     t.ZT = (float *)take((size_t)k * cols * sizeof(float));
     t.ZT2 = (float *)take((size_t)k * cols * sizeof(float));
@@ -320,6 +328,8 @@ size_t eora_layout(int64_t rows, int64_t cols, int r, EoraWs *w, char *base) {
         t.FTlo = (float *)take(cc);
         t.dWhi = (float *)take(rc);
         t.dWlo = (float *)take(rc);
+        t.Mhi = (float *)take(rc);
+        t.Mlo = (float *)take(rc);
         t.Mthi = (float *)take(rc);
         t.Mtlo = (float *)take(rc);
         t.Ghi = (float *)take(cc);
@@ -390,12 +400,13 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     if (*bad_pivot_host != ULLONG_MAX) return cudaSuccess;
 
     if (tc) {
-        // M^T = F^T dW^T (cols x rows, also split), G = M^T M (cols x cols, also split).
+        // M = dW F (rows x cols, also split), its transpose split, G = M^T M (cols x cols, also split).
         if ((e = split_transpose_tf32(w.F, cols, cols, cols, w.FThi, w.FTlo, cols, s)) != cudaSuccess) return e;
         if ((e = split_tf32(dW, rows, cols, cols, w.dWhi, w.dWlo, cols, s)) != cudaSuccess) return e;
-        if ((e = gemm3(cols, rows, cols, 1.f, w.FThi, w.FTlo, cols, w.dWhi, w.dWlo, cols, 0.f, w.M, rows, 0, w.Mthi,
-                       w.Mtlo, rows, s)) != cudaSuccess)
+        if ((e = gemm3(rows, cols, cols, 1.f, w.dWhi, w.dWlo, cols, w.FThi, w.FTlo, cols, 0.f, w.M, cols, 0, w.Mhi,
+                       w.Mlo, cols, s)) != cudaSuccess)
             return e;
+        if ((e = split_transpose_tf32(w.M, rows, cols, cols, w.Mthi, w.Mtlo, rows, s)) != cudaSuccess) return e;
         if ((e = gemm3(cols, cols, rows, 1.f, w.Mthi, w.Mtlo, rows, w.Mthi, w.Mtlo, rows, 0.f, w.G, cols, 0, w.Ghi,
                        w.Glo, cols, s)) != cudaSuccess)
             return e;
@@ -444,10 +455,12 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     if ((e = sgemm<float>(r, cols, k, 1.f, w.Wt, k, true, w.ZT, cols, false, 0.f, w.VrT, cols, 0, s)) != cudaSuccess)
         return e;
     // B = M V_r (rows x r), signs normalised.
-    if (tc)
-        e = sgemm<float>(rows, r, cols, 1.f, w.M, rows, true, w.VrT, cols, true, 0.f, B, r, 0, s);
-    else
+    if (tc) {
+        if ((e = split_tf32(w.VrT, r, cols, cols, w.Zhi, w.Zlo, cols, s)) != cudaSuccess) return e;
+        e = gemm3(rows, r, cols, 1.f, w.Mhi, w.Mlo, cols, w.Zhi, w.Zlo, cols, 0.f, B, r, 0, nullptr, nullptr, 0, s);
+    } else {
         e = sgemm<float>(rows, r, cols, 1.f, w.M, cols, false, w.VrT, cols, true, 0.f, B, r, 0, s);
+    }
     if (e != cudaSuccess) return e;
     sign_normalize_kernel<<<r, 256, 0, s>>>(B, rows, r);
     count_launch();
