@@ -1,5 +1,6 @@
 /*
- * gq.h -- GPTQ layer quantization and EoRA compensation on one NVIDIA B300 (sm_103a).
+ * gq.h -- GPTQ layer quantization, EoRA compensation and GPTQ-intrinsic LoRA on one
+ * NVIDIA B300 (sm_103a).
  *
  * C ABI of libgq.so.  Every pointer argument is a CUDA DEVICE pointer unless its
  * comment says "host".  The caller owns every buffer; the library never
@@ -25,6 +26,8 @@
  *                sections 1 (format) and 2 (input covariance).
  *   [EoRA-blog]  "Aumento de la precisión de LLM de 2 bits con EoRA", 7minutos.es,
  *                "Bucear en el espacio propio en busca de un adaptador".
+ *   [GPTQ-LoRA]  "Resumen Técnico: GPTQ-intrinsic LoRA", gist.science,
+ *                "Metodología", item 2 "Algoritmo GPTQ-intrinsic LoRA".
  */
 #ifndef GQ_H
 #define GQ_H
@@ -197,6 +200,63 @@ gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t co
 size_t eora_compensate_workspace_size(int64_t rows, int64_t cols, int r);
 gq_status eora_compensate(const float *dW, int64_t rows, int64_t cols, const float *H, int r, float *A, float *B,
                           float *sigma, void *ws, size_t ws_bytes, gq_stream_t stream, int64_t *info);
+
+/*
+ * The GPTQ-intrinsic LoRA basis ([GPTQ-LoRA] "Hessiano Aumentado"): L = V_r,
+ * the r leading right singular vectors of the calibration matrix X, i.e. the r
+ * leading eigenvectors of H = 2 X^T X.
+ *
+ *   H      cols x cols float32 (both triangles, symmetric positive
+ *          semi-definite), read only.
+ *   r      1 <= r <= min(64, cols).
+ *   Lt     r x cols float32 output: row i is the i-th basis vector (L^T in the
+ *          page's notation, which is also the adapter's A).  Rows are
+ *          orthonormal; the largest-magnitude entry of each row is positive.
+ *   lam    r float32 output, may be NULL: the Ritz values (eigenvalues of H,
+ *          = 2 sigma_i(X)^2), descending.
+ *   ws     >= gptq_lora_basis_workspace_size(cols, r) bytes.
+ * Computed in float32 with a block subspace iteration of width min(2r, 128,
+ * cols) (30 iterations) and a Rayleigh-Ritz step.  Where the eigenvalues
+ * around the r-th are close the leading subspace is not unique; the Ritz
+ * values and the captured sum tr(L^T H L) are.  Asynchronous.
+ */
+size_t gptq_lora_basis_workspace_size(int64_t cols, int r);
+gq_status gptq_lora_basis(const float *H, int64_t cols, int r, float *Lt, float *lam, void *ws, size_t ws_bytes,
+                          gq_stream_t stream);
+
+/*
+ * GPTQ-intrinsic LoRA of one layer ([GPTQ-LoRA] "Algoritmo GPTQ-intrinsic
+ * LoRA"): W ≈ Q + R L^T with Q on the GPTQ grid and a rank-r correction whose
+ * right factor is the given basis.
+ *
+ * Defined by the page's augmented problem: calibration X~ = [X, X L], Hessian
+ * H~ = [[H, H L], [L^T H, L^T H L]] damped like GPTQ's (dead inputs, then
+ * H~ + damp * mean(diag H~) * I over all cols + r diagonal entries), and the
+ * GPTQ sweep over W~ = [W, 0] in which the first cols columns are quantized and
+ * the last r, never quantized, absorb the quantization error; their final
+ * values are R.  The library computes the same result by block elimination:
+ * GPTQ on the Schur complement S = H_d - H L (L^T H L + delta I)^-1 L^T H (the
+ * quantized block of the inverse of H~ is S^-1, so the codes are the augmented
+ * sweep's), then R = (W - Ŵ) H L (L^T H L + delta I)^-1, the values the sweep
+ * leaves in the free columns (the optimum of the augmented quadratic given Q).
+ *
+ *   W, wt, rows, cols, H, bits, group, block, qweight, scales, qzeros, codes,
+ *   row_err   as for gptq_quantize_layer (row_err = sum_j e_j^2 over the
+ *             quantized columns of the augmented sweep).
+ *   Lt        r x cols float32 (rows orthonormal, e.g. from gptq_lora_basis), read only.
+ *   r         1 <= r <= min(64, cols).
+ *   damp      > 0 (H~ is singular: without damping it has no Cholesky factor).
+ *   W_hat     rows x cols float32 output, required (R is formed from it), 16-byte aligned.
+ *   R         rows x r float32 output: the adapter's B; its A is Lt.
+ *   ws        >= gptq_intrinsic_lora_workspace_size(rows, cols, r, block) bytes.
+ * Synchronizes `stream` once.  GQ_ENOTPD with *info = the failing column of
+ * the augmented matrix: < cols for S, cols + i for row i of L^T H L + delta I.
+ */
+size_t gptq_intrinsic_lora_workspace_size(int64_t rows, int64_t cols, int r, int block);
+gq_status gptq_intrinsic_lora(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *H,
+                              const float *Lt, int r, int bits, int group, int block, float damp, int32_t *qweight,
+                              float *scales, int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err,
+                              float *R, void *ws, size_t ws_bytes, gq_stream_t stream, int64_t *info);
 
 /*
  * gptq_quantize_layer without a caller-provided workspace, for callers that

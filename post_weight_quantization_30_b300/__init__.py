@@ -1,4 +1,4 @@
-"""GPTQ layer quantization (+ EoRA compensation) native to NVIDIA B300 (sm_103a).
+"""GPTQ layer quantization (+ EoRA compensation, GPTQ-intrinsic LoRA) native to NVIDIA B300 (sm_103a).
 
 The compute path is libgq.so (CUDA kernels behind a C ABI, include/gq.h); this
 package is its thin Python binding.  Importing it loads the library and fails
@@ -12,6 +12,8 @@ from ._lib import (  # noqa: F401
     gptq_code_decisions,
     gptq_factor,
     gptq_hessian_accumulate,
+    gptq_intrinsic_lora,
+    gptq_lora_basis,
     gptq_pack,
     gptq_quantize_layer,
     gptq_quantize_layer_noalloc,

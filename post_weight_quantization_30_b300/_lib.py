@@ -53,6 +53,11 @@ SIGNATURES = {
     "gptq_weight_error": (_i, [_p, _i, _i64, _i64, _p, _p, _p]),
     "eora_compensate_workspace_size": (_sz, [_i64, _i64, _i]),
     "eora_compensate": (_i, [_p, _i64, _i64, _p, _i, _p, _p, _p, _p, _sz, _p, ctypes.POINTER(_i64)]),
+    "gptq_lora_basis_workspace_size": (_sz, [_i64, _i]),
+    "gptq_lora_basis": (_i, [_p, _i64, _i, _p, _p, _p, _sz, _p]),
+    "gptq_intrinsic_lora_workspace_size": (_sz, [_i64, _i64, _i, _i]),
+    "gptq_intrinsic_lora": (_i, [_p, _i, _i64, _i64, _p, _p, _i, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p, _p,
+                                 _sz, _p, ctypes.POINTER(_i64)]),
     "gptq_code_decisions": (_i, [_p, _p, _i64, _p, _p]),
     "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
     "gptq_unpack": (_i, [_p, _i64, _i64, _i, _p, _p]),
@@ -236,6 +241,47 @@ def eora_compensate(dW: torch.Tensor, H: torch.Tensor, r: int, workspace: torch.
     _check(lib.eora_compensate(_ptr(dW), rows, cols, _ptr(H.contiguous()), r, _ptr(o["A"]), _ptr(o["B"]),
                                _ptr(o.get("sigma")), _ptr(ws), ws.numel(), _stream(dW.device), ctypes.byref(info)),
            "eora_compensate", info.value)
+    return o
+
+
+def gptq_lora_basis(H: torch.Tensor, r: int, workspace: torch.Tensor | None = None, out: dict | None = None):
+    """The GPTQ-intrinsic LoRA basis: dict(Lt = the r leading eigenvectors of H as rows, lam = their Ritz values)."""
+    _need_cuda(H)
+    cols = H.shape[0]
+    if H.dtype != torch.float32:
+        raise ValueError("H must be float32")
+    o = out if out is not None else dict(Lt=torch.empty((r, cols), dtype=torch.float32, device=H.device),
+                                         lam=torch.empty(r, dtype=torch.float32, device=H.device))
+    ws_bytes = lib.gptq_lora_basis_workspace_size(cols, r)
+    ws = workspace if workspace is not None else _workspace(ws_bytes, H.device)
+    _check(lib.gptq_lora_basis(_ptr(H.contiguous()), cols, r, _ptr(o["Lt"]), _ptr(o.get("lam")), _ptr(ws),
+                               ws.numel(), _stream(H.device)), "gptq_lora_basis")
+    return o
+
+
+def gptq_intrinsic_lora(W: torch.Tensor, H: torch.Tensor, Lt: torch.Tensor, bits: int, group: int, block: int = 128,
+                        damp: float = 0.01, codes: bool = True, row_err: bool = True,
+                        workspace: torch.Tensor | None = None, out: dict | None = None):
+    """GPTQ-intrinsic LoRA: W ≈ Ŵ + R Lt.  Returns the gptq_quantize_layer outputs plus R (rows x r)."""
+    _need_cuda(W, H, Lt)
+    rows, cols = W.shape
+    r = Lt.shape[0]
+    W = W.contiguous()
+    if H.dtype != torch.float32 or Lt.dtype != torch.float32:
+        raise ValueError("H and Lt must be float32")
+    if out is not None:
+        o = out
+    else:
+        o = _sweep_outputs(rows, cols, bits, group, W.device, codes, True, row_err)
+        o["R"] = torch.empty((rows, r), dtype=torch.float32, device=W.device)
+    ws_bytes = lib.gptq_intrinsic_lora_workspace_size(rows, cols, r, block)
+    ws = workspace if workspace is not None else _workspace(ws_bytes, W.device)
+    info = _i64(-1)
+    _check(lib.gptq_intrinsic_lora(_ptr(W), _dtype_code(W), rows, cols, _ptr(H.contiguous()), _ptr(Lt.contiguous()),
+                                   r, bits, group, block, float(damp), _ptr(o["qweight"]), _ptr(o["scales"]),
+                                   _ptr(o["qzeros"]), _ptr(o.get("codes")), _ptr(o["W_hat"]), _ptr(o.get("row_err")),
+                                   _ptr(o["R"]), _ptr(ws), ws.numel(), _stream(W.device), ctypes.byref(info)),
+           "gptq_intrinsic_lora", info.value)
     return o
 
 

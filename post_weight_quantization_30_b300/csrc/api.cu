@@ -2,6 +2,7 @@
 // layout and the order of the stream-ordered launches.
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstring>
 
 #include "common.cuh"
@@ -41,6 +42,22 @@ gq_status check_sweep_args(const void *W, gq_dtype wt, int64_t rows, int64_t col
     if ((codes && !aligned(codes, 4)) || (W_hat && !aligned(W_hat, 16)) || (row_err && !aligned(row_err, 4)))
         return GQ_EINVAL;
     return GQ_OK;
+}
+
+// The float32 regions of the sweep workspace.
+struct SweepRegions {
+    float *Uinv, *VThi, *VTlo, *D, *DL;
+};
+
+SweepRegions sweep_regions(void *ws, int64_t rows, int64_t cols, int block) {
+    const int64_t nblk = (cols + block - 1) / block;
+    SweepRegions g;
+    g.Uinv = (float *)ws;
+    g.VThi = (float *)((char *)ws + align_up((size_t)nblk * block * block * sizeof(float)));
+    g.VTlo = (float *)((char *)g.VThi + align_up((size_t)cols * cols * sizeof(float)));
+    g.D = (float *)((char *)g.VTlo + align_up((size_t)cols * cols * sizeof(float)));
+    g.DL = (float *)((char *)g.D + align_up((size_t)rows * cols * sizeof(float)));
+    return g;
 }
 
 struct SweepCtx {
@@ -112,17 +129,128 @@ gq_status sweep_impl(const void *W, gq_dtype wt, int64_t rows, int64_t cols, con
     c.W = W; c.bf16 = (wt == GQ_BF16); c.rows = rows; c.cols = cols; c.F = F; c.dead = dead;
     c.bits = bits; c.group = group; c.block = block;
     c.qweight = qweight; c.scales = scales; c.qzeros = qzeros; c.codes = codes; c.W_hat = W_hat; c.row_err = row_err;
-    c.Uinv = (float *)ws;
-    c.VThi = (float *)((char *)ws + align_up((size_t)nblk * block * block * sizeof(float)));
-    c.VTlo = (float *)((char *)c.VThi + align_up((size_t)cols * cols * sizeof(float)));
-    c.D = (float *)((char *)c.VTlo + align_up((size_t)cols * cols * sizeof(float)));
-    c.DL = (float *)((char *)c.D + align_up((size_t)rows * cols * sizeof(float)));
+    const SweepRegions g = sweep_regions(ws, rows, cols, block);
+    c.Uinv = g.Uinv; c.VThi = g.VThi; c.VTlo = g.VTlo; c.D = g.D; c.DL = g.DL;
     c.s = s;
     GQ_CUDA_TRY(cudaMemsetAsync(c.D, 0, (size_t)rows * cols * sizeof(float), s));
     if (row_err) GQ_CUDA_TRY(cudaMemsetAsync(row_err, 0, (size_t)rows * sizeof(float), s));
     if (!uinv_ready) GQ_CUDA_TRY(block_inverses(F, cols, block, c.Uinv, s));
     GQ_CUDA_TRY(premultiply_t(F, cols, block, c.Uinv, c.VThi, c.VTlo, s));
     GQ_CUDA_TRY(sweep_range(c, 0, nblk));
+    return GQ_OK;
+}
+
+// GPTQ-intrinsic LoRA workspace (float32 unless noted, 256-byte aligned regions):
+//   [cst][deadH: cols bytes][deadS: cols bytes][Lthi, Ltlo, Pt, Yt, Ythi, Ytlo: r x cols each]
+//   [Ppart: psplit x r x cols][C: r x r][Cpart: 64 x r x r][Kinv][Yhi, Ylo: cols x r4 each]
+//   [Rtmp: rows x r][Rpart: rsplit x rows x r][F: cols x cols][factor scratch][sweep workspace]
+// The split of H and then S live in the sweep workspace's VThi / VTlo regions, which
+// the sweep itself only fills after the factorization of S has read them.
+struct LoraLayout {
+    DeviceStatus *cst;
+    uint8_t *deadH, *deadS;
+    float *Lthi, *Ltlo, *Pt, *Yt, *Ythi, *Ytlo, *Ppart, *C, *Cpart, *Kinv, *Yhi, *Ylo, *Rtmp, *Rpart, *F;
+    void *fws, *sws;
+};
+
+constexpr int LORA_CSPLIT = 64;  // K slices of C = L^T P
+
+// K slices that bring a GEMM of `tiles` 128 x 128 output tiles to about one CTA per SM.
+int splits_for(int64_t tiles) {
+    int64_t z = (148 + tiles - 1) / tiles;
+    if (z < 1) z = 1;
+    if (z > 8) z = 8;
+    return (int)z;
+}
+
+inline int64_t r4_of(int r) { return (r + 3) / 4 * 4; }
+
+size_t lora_layout(int64_t rows, int64_t cols, int r, int block, LoraLayout *w, char *base) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *p = base ? base + off : nullptr;
+        off += align_up(bytes);
+        return p;
+    };
+    const size_t rc = (size_t)r * cols * sizeof(float);
+    const int ps = splits_for((cols + 127) / 128), rs = splits_for((rows + 127) / 128);
+    LoraLayout t = {};
+    t.cst = (DeviceStatus *)take(sizeof(DeviceStatus));
+    t.deadH = (uint8_t *)take((size_t)cols);
+    t.deadS = (uint8_t *)take((size_t)cols);
+    t.Lthi = (float *)take(rc);
+    t.Ltlo = (float *)take(rc);
+    t.Pt = (float *)take(rc);
+    t.Yt = (float *)take(rc);
+    t.Ythi = (float *)take(rc);
+    t.Ytlo = (float *)take(rc);
+    t.Ppart = (float *)take((size_t)ps * rc);
+    t.C = (float *)take((size_t)r * r * sizeof(float));
+    t.Cpart = (float *)take((size_t)LORA_CSPLIT * r * r * sizeof(float));
+    t.Kinv = (float *)take(cholesky_scratch_floats(128) * sizeof(float));
+    t.Yhi = (float *)take((size_t)cols * r4_of(r) * sizeof(float));
+    t.Ylo = (float *)take((size_t)cols * r4_of(r) * sizeof(float));
+    t.Rtmp = (float *)take((size_t)rows * r * sizeof(float));
+    t.Rpart = (float *)take((size_t)rs * rows * r * sizeof(float));
+    t.F = (float *)take((size_t)cols * cols * sizeof(float));
+    t.fws = take(factor_scratch_bytes(cols));
+    t.sws = take(sweep_ws_bytes(rows, cols, block));
+    if (w) *w = t;
+    return off;
+}
+
+// C = A B^T on the tensor cores (3xTF32), split over K when the output has few tiles.
+cudaError_t gemm3_nt(int64_t M, int64_t N, int64_t K, const float *Ahi, const float *Alo, int64_t lda,
+                     const float *Bhi, const float *Blo, int64_t ldb, float *C, float *part, int slices,
+                     cudaStream_t s) {
+    if (slices <= 1)
+        return gemm3(M, N, K, 1.f, Ahi, Alo, lda, Bhi, Blo, ldb, 0.f, C, N, 0, nullptr, nullptr, 0, s);
+    return gemm3_splitk(M, N, K, Ahi, Alo, lda, Bhi, Blo, ldb, C, part, slices, s);
+}
+
+gq_status intrinsic_impl(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *H, const float *Lt,
+                         int r, int bits, int group, int block, float damp, int32_t *qweight, float *scales,
+                         int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err, float *R, void *ws,
+                         cudaStream_t s, int64_t *info) {
+    LoraLayout w;
+    lora_layout(rows, cols, r, block, &w, (char *)ws);
+    const SweepRegions g = sweep_regions(w.sws, rows, cols, block);
+    const int ps = splits_for((cols + 127) / 128), rs = splits_for((rows + 127) / 128);
+    const int64_t r4 = r4_of(r);
+    float *S = g.VThi;
+    GQ_CUDA_TRY(cudaMemsetAsync(w.cst, 0xFF, sizeof(DeviceStatus), s));
+    // P^T = L^T H (H symmetric), C = L^T P.
+    GQ_CUDA_TRY(split_tf32(Lt, r, cols, cols, w.Lthi, w.Ltlo, cols, s));
+    GQ_CUDA_TRY(split_tf32(H, cols, cols, cols, g.VThi, g.VTlo, cols, s));
+    GQ_CUDA_TRY(gemm3_nt(r, cols, cols, w.Lthi, w.Ltlo, cols, g.VThi, g.VTlo, cols, w.Pt, w.Ppart, ps, s));
+    GQ_CUDA_TRY(sgemm_splitk(r, r, cols, Lt, cols, false, w.Pt, cols, true, w.C, w.Cpart, LORA_CSPLIT, s));
+    // delta over the augmented diagonal; C_d = C + delta I = K K^T; Y^T = K^-1 P^T.
+    GQ_CUDA_TRY(lora_damp_launch(H, cols, w.C, r, damp, w.deadH, w.cst, s));
+    GQ_CUDA_TRY(cholesky_lower_inplace(w.C, r, w.cst, w.Kinv, s));
+    GQ_CUDA_TRY(sgemm<float>(r, cols, r, 1.f, w.Kinv, 128, false, w.Pt, cols, false, 0.f, w.Yt, cols, 0, s));
+    GQ_CUDA_TRY(split_tf32(w.Yt, r, cols, cols, w.Ythi, w.Ytlo, cols, s));
+    GQ_CUDA_TRY(split_transpose_tf32(w.Yt, r, cols, cols, w.Yhi, w.Ylo, r4, s));
+    // S = H_d - Y Y^T.
+    GQ_CUDA_TRY(schur_init_launch(H, cols, w.cst, S, s));
+    GQ_CUDA_TRY(gemm3(cols, cols, r, -1.f, w.Yhi, w.Ylo, r4, w.Yhi, w.Ylo, r4, 1.f, S, cols, 0, nullptr, nullptr, 0,
+                      s));
+    unsigned long long bad_c = 0;
+    GQ_CUDA_TRY(cudaMemcpyAsync(&bad_c, &w.cst->bad_pivot, sizeof(bad_c), cudaMemcpyDeviceToHost, s));
+    // GPTQ on S: the factorization synchronizes the stream, after which bad_c is valid.
+    const bool uinv = factor_emits_uinv(cols, block);
+    gq_status st = factor_impl(S, cols, 0.f, w.F, w.deadS, w.fws, s, info, uinv ? g.Uinv : nullptr, block);
+    if (bad_c != ULLONG_MAX) {
+        if (info) *info = cols + (int64_t)bad_c;
+        return GQ_ENOTPD;
+    }
+    if (st != GQ_OK) return st;
+    st = sweep_impl(W, wt, rows, cols, w.F, w.deadH, bits, group, block, qweight, scales, qzeros, codes, W_hat,
+                    row_err, w.sws, s, uinv);
+    if (st != GQ_OK) return st;
+    // R = (W - Ŵ) Y K^-1.
+    GQ_CUDA_TRY(dw_split_launch(W, wt == GQ_BF16, W_hat, w.deadH, rows, cols, g.D, g.DL, s));
+    GQ_CUDA_TRY(gemm3_nt(rows, r, cols, g.D, g.DL, cols, w.Ythi, w.Ytlo, cols, w.Rtmp, w.Rpart, rs, s));
+    GQ_CUDA_TRY(sgemm<float>(rows, r, r, 1.f, w.Rtmp, r, false, w.Kinv, 128, false, 0.f, R, r, 0, s));
     return GQ_OK;
 }
 
@@ -234,6 +362,41 @@ gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t 
     if (st != GQ_OK) return st;
     return sweep_impl(W, wt, rows, cols, F, dead, bits, group, block, qweight, scales, qzeros, codes, W_hat, row_err, p,
                       cs(stream), uinv);
+}
+
+size_t gptq_lora_basis_workspace_size(int64_t cols, int r) {
+    if (cols <= 0 || r <= 0) return 0;
+    return lora_basis_workspace_bytes(cols, r);
+}
+
+gq_status gptq_lora_basis(const float *H, int64_t cols, int r, float *Lt, float *lam, void *ws, size_t ws_bytes,
+                          gq_stream_t stream) {
+    if (!H || !Lt || cols <= 0) return GQ_EINVAL;
+    if (r <= 0 || r > 64 || r > cols) return GQ_EINVAL;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < lora_basis_workspace_bytes(cols, r)) return GQ_EWORKSPACE;
+    return lora_basis_run(H, cols, r, Lt, lam, ws, cs(stream)) == cudaSuccess ? GQ_OK : GQ_ECUDA;
+}
+
+size_t gptq_intrinsic_lora_workspace_size(int64_t rows, int64_t cols, int r, int block) {
+    if (rows <= 0 || cols <= 0 || r <= 0 || block <= 0) return 0;
+    return lora_layout(rows, cols, r, block, nullptr, nullptr);
+}
+
+gq_status gptq_intrinsic_lora(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *H,
+                              const float *Lt, int r, int bits, int group, int block, float damp, int32_t *qweight,
+                              float *scales, int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err,
+                              float *R, void *ws, size_t ws_bytes, gq_stream_t stream, int64_t *info) {
+    if (!H || !Lt || !R || !W_hat) return GQ_EINVAL;
+    gq_status st = check_sweep_args(W, wt, rows, cols, H, bits, group, block, qweight, scales, qzeros, codes, W_hat,
+                                    row_err);
+    if (st != GQ_OK) return st;
+    if (r <= 0 || r > 64 || r > cols) return GQ_EINVAL;
+    if (!(damp > 0.f) || !(damp < INFINITY)) return GQ_EINVAL;
+    if (!aligned(R, 4) || !aligned(Lt, 4)) return GQ_EINVAL;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < gptq_intrinsic_lora_workspace_size(rows, cols, r, block))
+        return GQ_EWORKSPACE;
+    return intrinsic_impl(W, wt, rows, cols, H, Lt, r, bits, group, block, damp, qweight, scales, qzeros, codes,
+                          W_hat, row_err, R, ws, cs(stream), info);
 }
 
 gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *W_hat, float *dW,

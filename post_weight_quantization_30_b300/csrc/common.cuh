@@ -51,6 +51,14 @@ __device__ __forceinline__ float quotient_rn(float w, float s, float y) {
     return fmaf(r, y, q0);
 }
 
+// The TF32 value nearest to x (ties away from zero); x - tf32_hi(x) is exact
+// in float32, which is the split the 3xTF32 products use.
+__device__ __forceinline__ float tf32_hi(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
 template <typename T>
 __device__ __forceinline__ float load_f32(const T *p);
 template <>
@@ -145,6 +153,30 @@ cudaError_t sweep_block_launch(const void *W, bool w_bf16, int64_t rows, int64_t
                                float *D, float *DL, int32_t *qweight, float *scales, int32_t *qzeros,
                                uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s);
 
+// Leading eigenpairs of a symmetric positive semi-definite G (subspace.cu).
+constexpr int kSubspaceMaxK = 128;
+struct SubspaceBufs {
+    const float *G;               // cols x cols (SIMT path)
+    const float *Ghi, *Glo;       // its TF32 split (tensor-core path)
+    float *ZT, *ZT2;              // k x cols each
+    float *Zhi, *Zlo;             // k x cols each (tensor-core path)
+    float *Gm, *Wt;               // k x k each
+    float *lam;                   // k
+    float *part;                  // subspace_part_floats(k, cols, tc)
+    float *Linv;                  // cholesky_scratch_floats(128)
+    DeviceStatus *qst;            // status of the Cholesky-QR factorizations
+};
+// k = min(2 r, 128, cols) vectors for r wanted eigenpairs.
+int subspace_width(int64_t cols, int r);
+size_t subspace_part_floats(int k, int64_t cols, bool tc);
+// On return the rows of ZT are orthonormal, lam holds the k Ritz values in
+// descending order and column i of Wt (k x k, row-major) the coefficients of
+// Ritz vector i in those rows.
+cudaError_t subspace_ritz(const SubspaceBufs &w, int k, int64_t cols, bool tc, cudaStream_t s);
+// nvec vectors of length n, entry e of vector v at X[v * vs + e * es]: each
+// negated unless its largest-magnitude entry (first on ties) is positive.
+cudaError_t sign_normalize(float *X, int nvec, int64_t n, int64_t es, int64_t vs, cudaStream_t s);
+
 // EoRA (eora.cu).  eora_run synchronizes `s` once, after the factorization of
 // H, and reports a non-positive pivot through *bad_pivot_host (ULLONG_MAX = none,
 // else the pivot index in reversed order); nothing after that is launched then.
@@ -152,6 +184,20 @@ size_t eora_workspace_bytes(int64_t rows, int64_t cols, int r);
 int eora_subspace_width(int64_t rows, int64_t cols, int r);
 cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H, int r, float *A, float *B,
                      float *sigma, void *ws, cudaStream_t s, unsigned long long *bad_pivot_host);
+
+// GPTQ-intrinsic LoRA (lora.cu).
+size_t lora_basis_workspace_bytes(int64_t cols, int r);
+// Lt (r x cols) = the r leading eigenvectors of H as rows; lam (may be NULL) their Ritz values.
+cudaError_t lora_basis_run(const float *H, int64_t cols, int r, float *Lt, float *lam, void *ws, cudaStream_t s);
+// dead[i] = (H_ii == 0); delta = damp * mean of the augmented diagonal (fix(H_ii), fix(C_ii)) into
+// st->delta; C_ii <- fix(C_ii) + delta (C: r x r, ld r).
+cudaError_t lora_damp_launch(const float *H, int64_t cols, float *C, int r, float damp, uint8_t *dead,
+                             DeviceStatus *st, cudaStream_t s);
+// S = H with diagonal fix(H_ii) + st->delta.
+cudaError_t schur_init_launch(const float *H, int64_t cols, const DeviceStatus *st, float *S, cudaStream_t s);
+// TF32 split of W - W_hat (dead inputs' weights taken as 0), rows x cols, ld cols.
+cudaError_t dw_split_launch(const void *W, bool w_bf16, const float *W_hat, const uint8_t *dead, int64_t rows,
+                            int64_t cols, float *hi, float *lo, cudaStream_t s);
 
 // dW = W - W_hat, n elements (W float32 or bf16).
 cudaError_t weight_error_launch(const void *W, bool w_bf16, int64_t n, const float *W_hat, float *dW, cudaStream_t s);

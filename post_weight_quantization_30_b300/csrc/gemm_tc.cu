@@ -60,12 +60,6 @@ __device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64
         : "memory");
 }
 
-__device__ __forceinline__ float tf32_hi(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
 __global__ void __launch_bounds__(G_NWARPS * 32, 1)
     gemm3_kernel(const __grid_constant__ CUtensorMap ahi, const __grid_constant__ CUtensorMap alo,
                  const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo, float *C,

@@ -85,3 +85,32 @@ def test_eora_host_side_validation(gq):
     assert f(None, 64, 64, p(256), 4, p(256), p(256), None, p(256), 1 << 30, None, None) == -1     # null dW
     assert f(p(256), 64, 64, p(256), 4, p(256), p(256), None, p(256), 16, None, None) == -7        # workspace
     assert gq.lib.eora_compensate_workspace_size(5120, 5120, 64) >= 3 * 5120 * 5120 * 4
+
+
+def test_intrinsic_lora_host_side_validation(gq):
+    p = ctypes.c_void_p
+    b = gq.lib.gptq_lora_basis
+    assert b(p(256), 64, 0, p(256), None, p(256), 1 << 30, None) == -1    # r = 0
+    assert b(p(256), 256, 65, p(256), None, p(256), 1 << 30, None) == -1  # r > 64
+    assert b(p(256), 16, 32, p(256), None, p(256), 1 << 30, None) == -1   # r > cols
+    assert b(None, 64, 4, p(256), None, p(256), 1 << 30, None) == -1      # null H
+    assert b(p(256), 64, 4, p(256), None, p(256), 16, None) == -7         # workspace
+    assert b(p(256), 64, 4, p(256), None, p(260), 1 << 30, None) == -7    # unaligned workspace
+
+    f = gq.lib.gptq_intrinsic_lora
+    ws = gq.lib.gptq_intrinsic_lora_workspace_size(256, 256, 16, 128)
+    assert ws >= gq.lib.gptq_quantize_layer_workspace_size(256, 256, 128)
+
+    def call(r=16, damp=0.01, W_hat=p(256), R=p(256), Lt=p(256), bits=4, ws_bytes=ws):
+        return f(p(256), 0, 256, 256, p(256), Lt, r, bits, 128, 128, damp, p(256), p(256), p(256), None, W_hat, None,
+                 R, p(256), ws_bytes, None, None)
+
+    assert call(r=0) == -1
+    assert call(r=65) == -1
+    assert call(damp=0.0) == -1           # the augmented Hessian needs damping
+    assert call(damp=float("nan")) == -1
+    assert call(W_hat=None) == -1         # R is formed from W_hat
+    assert call(R=None) == -1
+    assert call(Lt=None) == -1
+    assert call(bits=5) == -3
+    assert call(ws_bytes=ws - 1) == -7
