@@ -2,7 +2,9 @@
 
 One step = one pass of the whole path over one synthetic layer:
     H = 0; gptq_hessian_accumulate(H, X); gptq_quantize_layer(W, H, ...)
-with X and W resident in HBM.  X (2.15 GB for the default workload) is larger
+(+ gptq_weight_error and eora_compensate on the EoRA workloads; on the
+GPTQ-intrinsic LoRA workloads gptq_lora_basis and gptq_intrinsic_lora in place
+of gptq_quantize_layer) with X and W resident in HBM.  X (2.15 GB for the default workload) is larger
 than the 126 MB L2, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
@@ -177,8 +179,16 @@ def run_ours(args, rank: int, world: int):
     H = torch.zeros((C, C), dtype=torch.float32, device=dev)
     ws = torch.empty(gq.lib.gptq_quantize_layer_workspace_size(R, C, spec.block), dtype=torch.uint8, device=dev)
     r = spec.eora_rank
-    # Ŵ is an output only when EoRA needs it (the error it compensates is W - Ŵ).
-    out = gq._lib._sweep_outputs(R, C, spec.bits, spec.group, dev, codes=False, W_hat=r > 0, row_err=False)
+    rl = spec.lora_rank
+    # Ŵ is an output only when EoRA or the intrinsic LoRA needs it (the error they compensate is W - Ŵ).
+    out = gq._lib._sweep_outputs(R, C, spec.bits, spec.group, dev, codes=False, W_hat=(r or rl) > 0, row_err=False)
+    if rl:
+        ws = torch.empty(gq.lib.gptq_intrinsic_lora_workspace_size(R, C, rl, spec.block), dtype=torch.uint8,
+                         device=dev)
+        bws = torch.empty(gq.lib.gptq_lora_basis_workspace_size(C, rl), dtype=torch.uint8, device=dev)
+        bout = dict(Lt=torch.empty((rl, C), dtype=torch.float32, device=dev),
+                    lam=torch.empty(rl, dtype=torch.float32, device=dev))
+        out["R"] = torch.empty((R, rl), dtype=torch.float32, device=dev)
     if r:
         dW = torch.empty((R, C), dtype=torch.float32, device=dev)
         ews = torch.empty(gq.lib.eora_compensate_workspace_size(R, C, r), dtype=torch.uint8, device=dev)
@@ -191,6 +201,16 @@ def run_ours(args, rank: int, world: int):
         gq.gptq_weight_error(Wsrc, out["W_hat"], out=dW)
         gq.eora_compensate(dW, H, r, workspace=ews, out=eout)
 
+    def quantize(Wsrc):
+        if rl:
+            gq.gptq_lora_basis(H, rl, workspace=bws, out=bout)
+            gq.gptq_intrinsic_lora(Wsrc, H, bout["Lt"], spec.bits, spec.group, spec.block, spec.damp, workspace=ws,
+                                   out=out)
+            return
+        gq.gptq_quantize_layer(Wsrc, H, spec.bits, spec.group, spec.block, spec.damp, workspace=ws, out=out)
+        if r:
+            eora_part(Wsrc)
+
     def step(ev=None):
         H.zero_()
         if ev is not None:
@@ -198,9 +218,7 @@ def run_ours(args, rank: int, world: int):
         gq.gptq_hessian_accumulate(H, X)
         if ev is not None:
             ev[1].record(stream)
-        gq.gptq_quantize_layer(W, H, spec.bits, spec.group, spec.block, spec.damp, workspace=ws, out=out)
-        if r:
-            eora_part(W)
+        quantize(W)
 
     for _ in range(args.warmup):
         step()
@@ -243,10 +261,29 @@ def run_ours(args, rank: int, world: int):
 
     reps = 3
     acc = {"hessian": 0.0, "factor": 0.0, "sweep": 0.0}
+    if rl:
+        acc = {"hessian": 0.0, "basis": 0.0, "intrinsic_lora": 0.0}
+        for _ in range(reps):
+            H.zero_()
+            e[0].record(stream)
+            gq.gptq_hessian_accumulate(H, X)
+            e[1].record(stream)
+            gq.gptq_lora_basis(H, rl, workspace=bws, out=bout)
+            e[2].record(stream)
+            gq.gptq_intrinsic_lora(W, H, bout["Lt"], spec.bits, spec.group, spec.block, spec.damp, workspace=ws,
+                                   out=out)
+            e[3].record(stream)
+            torch.cuda.synchronize(dev)
+            acc["hessian"] += e[0].elapsed_time(e[1])
+            acc["basis"] += e[1].elapsed_time(e[2])
+            acc["intrinsic_lora"] += e[2].elapsed_time(e[3])
+        reps_done = True
+    else:
+        reps_done = False
     if r:
         acc["eora"] = 0.0
         e.append(torch.cuda.Event(enable_timing=True))
-    for _ in range(reps):
+    for _ in range(0 if reps_done else reps):
         H.zero_()
         e[0].record(stream)
         gq.gptq_hessian_accumulate(H, X)
@@ -275,6 +312,8 @@ def run_ours(args, rank: int, world: int):
     # End to end through the public API from pinned host buffers, every step:
     # H2D of X and W, the whole path, D2H of the packed result.
     results = {k: v for k, v in out.items() if v is not None and k != "W_hat"}
+    if rl:
+        results.update(lora_Lt=bout["Lt"])
     if r:
         results.update(eora_A=eout["A"], eora_B=eout["B"])
     res_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in results.items()}
@@ -290,9 +329,7 @@ def run_ours(args, rank: int, world: int):
         to_dev(w_host, Wd)
         H.zero_()
         gq.gptq_hessian_accumulate(H, Xd)
-        gq.gptq_quantize_layer(Wd, H, spec.bits, spec.group, spec.block, spec.damp, workspace=ws, out=out)
-        if r:
-            eora_part(Wd)
+        quantize(Wd)
         for k, v in res_host.items():
             v.copy_(results[k], non_blocking=True)
         torch.cuda.synchronize(dev)
@@ -321,7 +358,8 @@ def run_ours(args, rank: int, world: int):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 x bf16 -> f32 (Hessian); f32 (factor, sweep, 3xTF32 GEMMs" + (", EoRA)" if r else ")"),
+        "dtype": "bf16 x bf16 -> f32 (Hessian); f32 (factor, sweep, 3xTF32 GEMMs" +
+                 (", EoRA)" if r else ", intrinsic LoRA)" if rl else ")"),
         "data": describe_inputs(spec),
         "config": {
             "workload": args.workload, "rows": R, "cols": C, "tokens": N, "bits": spec.bits, "group": spec.group,
@@ -386,18 +424,34 @@ def cpu_baseline(spec, budget_s: float = 20.0) -> dict:
     t0 = time.perf_counter()
     H = og.hessian(x.astype(np.float64)) * (spec.n / n_s)
     t1 = time.perf_counter()
-    Hd, dead = og.prepare_hessian(H, spec.damp)
-    U = og.inverse_cholesky_upper(Hd)
-    t2 = time.perf_counter()
-    res = og.sweep(w, U, spec.bits, spec.group, dead=dead)
+    if spec.lora_rank:
+        # GPTQ-intrinsic LoRA: basis by a full eigendecomposition, augmented Hessian, partial sweep.
+        from oracle import intrinsic_lora as il
+
+        L, _ = il.top_right_singular_vectors(H, spec.lora_rank)
+        Hd, dead = og.prepare_hessian(il.augmented_hessian(H, L), spec.damp)
+        U = og.inverse_cholesky_upper(Hd)
+        t2 = time.perf_counter()
+        res = il.sweep_partial(np.hstack([w, np.zeros((r_s, spec.lora_rank))]), U, spec.bits, spec.group, spec.cols,
+                               dead=dead)
+    else:
+        Hd, dead = og.prepare_hessian(H, spec.damp)
+        U = og.inverse_cholesky_upper(Hd)
+        t2 = time.perf_counter()
+        res = og.sweep(w, U, spec.bits, spec.group, dead=dead)
     t3 = time.perf_counter()
     opk.pack_qweight(res["codes"], spec.bits)
     t4 = time.perf_counter()
     per_layer = (t1 - t0) * (spec.n / n_s) + (t2 - t1) + (t3 - t2) * (spec.rows / r_s) + (t4 - t3) * (spec.rows / r_s)
     return {
         "value": round(per_layer, 3), "unit": "s/layer", "cores": cores, "kind": "oracle",
-        "sample": f"H on {n_s} of {spec.n} tokens (x{spec.n / n_s:g}); full float64 inverse + Cholesky of "
-                  f"{spec.cols}x{spec.cols}; eager sweep + pack on {r_s} of {spec.rows} rows (x{spec.rows / r_s:g})",
+        "sample": f"H on {n_s} of {spec.n} tokens (x{spec.n / n_s:g}); " +
+                  (f"full float64 eigendecomposition for the rank-{spec.lora_rank} basis, inverse + Cholesky of the "
+                   f"augmented {spec.cols + spec.lora_rank}x{spec.cols + spec.lora_rank} Hessian; "
+                   if spec.lora_rank else
+                   f"full float64 inverse + Cholesky of {spec.cols}x{spec.cols}; ") +
+                  f"eager sweep + pack on {r_s} of {spec.rows} rows (x{spec.rows / r_s:g})" +
+                  ("; EoRA not included" if spec.eora_rank else ""),
         "sample_s": round(t4 - t0, 2),
         "phases_s": {"hessian": round((t1 - t0) * spec.n / n_s, 3), "factor": round(t2 - t1, 3),
                      "sweep": round((t3 - t2) * spec.rows / r_s, 3), "pack": round((t4 - t3) * spec.rows / r_s, 3)},

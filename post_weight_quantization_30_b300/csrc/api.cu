@@ -155,9 +155,10 @@ struct LoraLayout {
 
 constexpr int LORA_CSPLIT = 64;  // K slices of C = L^T P
 
-// K slices that bring a GEMM of `tiles` 128 x 128 output tiles to about one CTA per SM.
+// K slices that bring a GEMM of `tiles` 128 x 128 output tiles close to one CTA
+// per SM without a second wave.
 int splits_for(int64_t tiles) {
-    int64_t z = (148 + tiles - 1) / tiles;
+    int64_t z = 148 / tiles;
     if (z < 1) z = 1;
     if (z > 8) z = 8;
     return (int)z;

@@ -101,10 +101,11 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
                   float *Chi, float *Clo, int64_t ldcs, cudaStream_t s, int split_row0 = 0, int split_ncols = -1);
 // C (M x N, row-major, ldc = N) = A B^T as gemm3, with K split into `slices`
 // ranges computed by separate CTAs into `partials` (slices * M * N floats)
-// and summed in a fixed order.
+// and summed in a fixed order.  one_term: hi x hi only (TF32 accuracy, lo
+// operands not read).
 cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, const float *Alo, int64_t lda,
                          const float *Bhi, const float *Blo, int64_t ldb, float *C, float *partials, int slices,
-                         cudaStream_t s);
+                         cudaStream_t s, bool one_term = false);
 // C[i] = sum over z < slices of partials[z * n + i] (fixed order).
 cudaError_t sum_slices(const float *partials, int slices, int64_t n, float *C, cudaStream_t s);
 // hi / lo TF32 split of the transpose of a rows x cols float32 matrix (cols x rows out).

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
     gemm3_kernel(const __grid_constant__ CUtensorMap ahi, const __grid_constant__ CUtensorMap alo,
                  const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo, float *C,
                  int64_t ldc, int M, int N, int K, float alpha, float beta, int tri, float *Chi, float *Clo,
-                 int64_t ldcs, int ktiles_per_z, int64_t c_zstride, int split_row0, int split_ncols) {
+                 int64_t ldcs, int ktiles_per_z, int64_t c_zstride, int split_row0, int split_ncols, int one_term) {
     const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
     if (tri == 1 && n0 > m0 + GM - 1) return;  // tile entirely above the diagonal
     // Split K (gridDim.z > 1): slice z covers k-tiles [z * ktiles_per_z, ...) and
@@ -123,12 +123,14 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
                     break;
                 }
                 unsigned char *st = smem + s * G_STAGE;
-                mbar_arrive_expect_tx(&full_bar[s], G_STAGE);
+                mbar_arrive_expect_tx(&full_bar[s], one_term ? TILE_A + TILE_B : G_STAGE);
                 const int x = (kt0 + kt) * GK;
                 tma_load_2d(st, &ahi, x, m0, &full_bar[s]);
-                tma_load_2d(st + TILE_A, &alo, x, m0, &full_bar[s]);
                 tma_load_2d(st + 2 * TILE_A, &bhi, x, n0, &full_bar[s]);
-                tma_load_2d(st + 2 * TILE_A + TILE_B, &blo, x, n0, &full_bar[s]);
+                if (!one_term) {
+                    tma_load_2d(st + TILE_A, &alo, x, m0, &full_bar[s]);
+                    tma_load_2d(st + 2 * TILE_A + TILE_B, &blo, x, n0, &full_bar[s]);
+                }
             }
         }
         __syncwarp();
@@ -167,9 +169,13 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
                         const uint64_t dbh = smem_desc(b_hi + off, 16, 1024);
                         const uint64_t dbl = smem_desc(b_lo + off, 16, 1024);
                         const uint32_t first = (kt == p * G_KF && kk == 0) ? 0u : 1u;
-                        mma_tf32(acc, dal, dbh, idesc, first);
-                        mma_tf32(acc, dah, dbl, idesc, 1u);
-                        mma_tf32(acc, dah, dbh, idesc, 1u);
+                        if (one_term) {
+                            mma_tf32(acc, dah, dbh, idesc, first);
+                        } else {
+                            mma_tf32(acc, dal, dbh, idesc, first);
+                            mma_tf32(acc, dah, dbl, idesc, 1u);
+                            mma_tf32(acc, dah, dbh, idesc, 1u);
+                        }
                     }
                     mma_commit(&empty_bar[s]);
                 }
@@ -379,14 +385,14 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
     const int kt_all = (int)((K + GK - 1) / GK);
     gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta,
-                                                    tri, Chi, Clo, ldcs, kt_all, 0, split_row0, split_ncols);
+                                                    tri, Chi, Clo, ldcs, kt_all, 0, split_row0, split_ncols, 0);
     count_launch();
     return cudaGetLastError();
 }
 
 cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, const float *Alo, int64_t lda,
                          const float *Bhi, const float *Blo, int64_t ldb, float *C, float *partials, int slices,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool one_term) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     if (K <= 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || slices < 1) return cudaErrorInvalidValue;
     static bool attr_set = false;
@@ -394,6 +400,11 @@ cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, cons
         cudaError_t e = cudaFuncSetAttribute(gemm3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
+    }
+    // One term: the lo operands are never read; their maps repeat the hi ones.
+    if (one_term) {
+        Alo = Ahi;
+        Blo = Bhi;
     }
     CUtensorMap mah, mal, mbh, mbl;
     if (!make_map(&mah, Ahi, K, M, lda, GM) || !make_map(&mal, Alo, K, M, lda, GM) ||
@@ -404,7 +415,7 @@ cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, cons
     const int z = (kt_all + per - 1) / per;
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM), (unsigned)z);
     gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, partials, N, (int)M, (int)N, (int)K, 1.f, 0.f,
-                                                    0, nullptr, nullptr, 0, per, M * N, 0, 0);
+                                                    0, nullptr, nullptr, 0, per, M * N, 0, 0, one_term ? 1 : 0);
     count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -10,8 +10,9 @@
 //   T = ZT G ZT^T (k x k), T = W diag(lam) W^T by cyclic Jacobi
 //
 // The Ritz vectors are the rows of W^T ZT; callers take the first r of them.
-// On the tensor-core path the products with G run as 3xTF32 GEMMs from the
-// split of G the caller provides.
+// On the tensor-core path the products with G run on the tensor cores from the
+// split of G the caller provides: one TF32 product per iteration, 3xTF32
+// (float32 accuracy) for the last three iterations and the Rayleigh-Ritz step.
 #include <climits>
 
 #include "common.cuh"
@@ -19,9 +20,20 @@
 namespace gq {
 namespace {
 
-constexpr int ITERS = 30;   // subspace iterations
+constexpr int ITERS = 30;        // subspace iterations
+constexpr int ACCURATE_TAIL = 3; // of which the last ones multiply with float32 accuracy
 constexpr int SPLITK = 64;  // K slices of the thin Gram products
-constexpr int ZSPLIT = 4;   // K slices of the block products on the tensor cores
+constexpr int ZSPLIT_MAX = 8;  // K slices of the block products on the tensor cores, at most
+
+// K slices for a block product with ceil(cols / 128) x ceil(k / 128) output
+// tiles: as many as keep every CTA in one wave on the 148 SMs (one CTA per SM).
+int zsplit(int64_t cols, int k) {
+    const int64_t tiles = ((cols + 127) / 128) * ((k + 127) / 128);
+    int64_t z = 148 / tiles;
+    if (z < 1) z = 1;
+    if (z > ZSPLIT_MAX) z = ZSPLIT_MAX;
+    return (int)z;
+}
 
 // Starting block: k x cols values in [-1, 1) from a counter hash of (i, j).
 __global__ void init_block_kernel(float *__restrict__ ZT, int k, int64_t cols) {
@@ -66,124 +78,139 @@ __global__ void shift_gram_kernel(float *__restrict__ Gm, int k) {
 }
 
 // Eigen-decomposition of the symmetric k x k matrix T (k <= 128) by the
-// cyclic Jacobi method in one CTA, parallel over the k/2 disjoint (p, q) pairs
-// of a round-robin ordering.  Outputs the eigenvalues in descending order and
-// the matching eigenvectors as the columns of W (row-major k x k).
-constexpr int JT = 512;
+// cyclic Jacobi method in one CTA.  Each round applies the k/2 disjoint plane
+// rotations of a round-robin pairing at once, T <- J^T T J, as independent
+// 2 x 2 blocks J_i^T T[{p_i, q_i}, {p_j, q_j}] J_j over pairs of pairs (blocks
+// i <= j, mirrored), so a round costs two barriers.  Outputs the eigenvalues in
+// descending order and the matching eigenvectors as the columns of W
+// (row-major k x k).
+constexpr int JT = 1024;
+constexpr int JNP = kSubspaceMaxK / 2;  // rotations per round, at most
 constexpr int JLD = kSubspaceMaxK + 1;
-constexpr size_t JACOBI_SMEM = (2 * kSubspaceMaxK * JLD + 2 * (kSubspaceMaxK / 2 + 1)) * sizeof(float) +
-                               (kSubspaceMaxK + 2 + 2 * (kSubspaceMaxK / 2 + 1)) * sizeof(int);
+constexpr int JNB = JNP * (JNP + 1) / 2;  // 2 x 2 blocks (i <= j) per round
+constexpr size_t JACOBI_SMEM =
+    (2 * kSubspaceMaxK * JLD + 2 * JNP) * sizeof(float) + (2 * JNP + kSubspaceMaxK + JNB) * sizeof(int);
 
 __global__ void __launch_bounds__(JT) jacobi_eig_kernel(const float *__restrict__ Tin, int k, float *__restrict__ lam,
                                                         float *__restrict__ W) {
     extern __shared__ __align__(16) float js[];
     float *T = js;                        // [k][JLD]
-    float *V = T + kSubspaceMaxK * JLD;      // [k][JLD]
-    float *cs = V + kSubspaceMaxK * JLD;     // [npairs] cosines
-    float *sn = cs + kSubspaceMaxK / 2 + 1;  // [npairs] sines
-    int *pos = (int *)(sn + kSubspaceMaxK / 2 + 1);  // [kk] round-robin positions
-    int *pp = pos + kSubspaceMaxK + 2;       // [npairs]
-    int *pq = pp + kSubspaceMaxK / 2 + 1;    // [npairs]
+    float *V = T + kSubspaceMaxK * JLD;   // [k][JLD]
+    float *cs = V + kSubspaceMaxK * JLD;  // [np] cosines
+    float *sn = cs + JNP;                 // [np] sines (0: no rotation this round)
+    int *pp = (int *)(sn + JNP);          // [np] first index of each pair
+    int *pq = pp + JNP;                   // [np] second index (k: the dummy of an odd k)
+    int *order = pq + JNP;                // [k] sort order of the eigenvalues
+    int *blk = order + kSubspaceMaxK;     // [np (np + 1) / 2] block (i, j), i <= j, as i << 16 | j
     __shared__ int rotated;
+    __shared__ float tol;
     const int t = threadIdx.x;
     const int kk = (k + 1) & ~1;  // even, with a dummy index k when k is odd
     const int np = kk / 2;
+    const int m = kk - 1;
 
     for (int idx = t; idx < k * k; idx += JT) {
         const int i = idx / k, j = idx % k;
         T[i * JLD + j] = 0.5f * (Tin[i * k + j] + Tin[j * k + i]);
         V[i * JLD + j] = (i == j) ? 1.f : 0.f;
     }
-    for (int i = t; i < kk; i += JT) pos[i] = i;
-    for (int i = t; i < np; i += JT) sn[i] = 0.f;
-    __shared__ float tol;
+    for (int idx = t; idx < np * np; idx += JT) {
+        const int i = idx / np, j = idx % np;
+        // row i of the upper triangle starts at i * np - i (i - 1) / 2
+        if (i <= j) blk[i * np - (i * (i - 1)) / 2 + (j - i)] = (i << 16) | j;
+    }
+    const int nblk = np * (np + 1) / 2;
     __syncthreads();
     if (t == 0) {
         // Off-diagonal entries below 1e-7 of the largest diagonal entry are at the
         // float32 rounding level of T: they move no eigenvalue by more than that.
-        float m = 0.f;
-        for (int i = 0; i < k; ++i) m = fmaxf(m, fabsf(T[i * JLD + i]));
-        tol = 1e-7f * m;
+        float mx = 0.f;
+        for (int i = 0; i < k; ++i) mx = fmaxf(mx, fabsf(T[i * JLD + i]));
+        tol = 1e-7f * mx;
     }
-    __syncthreads();
 
     for (int sweep = 0; sweep < 15; ++sweep) {
         if (t == 0) rotated = 0;
         __syncthreads();
-        for (int round = 0; round < kk - 1; ++round) {
+        for (int round = 0; round < m; ++round) {
             if (t < np) {
-                // The element the previous rotation of this slot annihilated is
-                // set to exactly zero (it holds rounding residue only).
-                if (round > 0 && sn[t] != 0.f) {
-                    T[pp[t] * JLD + pq[t]] = 0.f;
-                    T[pq[t] * JLD + pp[t]] = 0.f;
-                }
-                int p = pos[t], q = pos[kk - 1 - t];
+                // Round-robin (circle) pairing: kk - 1 stays fixed and meets `round`;
+                // slot t >= 1 pairs round + t with round - t (mod kk - 1).  Every pair
+                // meets exactly once in kk - 1 rounds.
+                int p = (t == 0) ? round : (round + t) % m;
+                int q = (t == 0) ? m : (round - t + m) % m;
                 if (p > q) { const int x = p; p = q; q = x; }
-                float c = 1.f, s = 0.f;
+                float c = 1.f, sv = 0.f;
                 if (q < k) {
                     const float apq = T[p * JLD + q];
-                    const float app = T[p * JLD + p], aqq = T[q * JLD + q];
                     // Rotate unless a_pq is at the rounding level of T.
                     if (fabsf(apq) > tol) {
+                        const float app = T[p * JLD + p], aqq = T[q * JLD + q];
                         const float tau = (aqq - app) / (2.f * apq);
                         const float tt = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
                         c = 1.f / sqrtf(1.f + tt * tt);
-                        s = tt * c;
+                        sv = tt * c;
                         rotated = 1;
                     }
                 }
                 pp[t] = p;
                 pq[t] = q;
                 cs[t] = c;
-                sn[t] = s;
+                sn[t] = sv;
             }
             __syncthreads();
-            // Rows p, q of T  <- J^T T.
-            for (int idx = t; idx < np * k; idx += JT) {
-                const int pr = idx / k, j = idx % k;
-                const int p = pp[pr], q = pq[pr];
-                if (q >= k || sn[pr] == 0.f) continue;
-                const float c = cs[pr], s = sn[pr];
-                const float a = T[p * JLD + j], b = T[q * JLD + j];
-                T[p * JLD + j] = c * a - s * b;
-                T[q * JLD + j] = s * a + c * b;
+            // T <- J^T T J by 2 x 2 blocks; rows: p' = c p - s q, q' = s p + c q;
+            // columns likewise.  A diagonal block's off-diagonal pair is the
+            // annihilated element: set to exactly zero.
+            for (int b = t; b < nblk; b += JT) {
+                const int i = blk[b] >> 16, j = blk[b] & 0xFFFF;
+                const float si = sn[i], sj = sn[j];
+                if (si == 0.f && sj == 0.f) continue;
+                const float ci = cs[i], cj = cs[j];
+                const int pi = pp[i], qi = pq[i], pj = pp[j], qj = pq[j];
+                const bool vi = qi < k, vj = qj < k;
+                const float a = T[pi * JLD + pj];
+                const float bb = vj ? T[pi * JLD + qj] : 0.f;
+                const float cc = vi ? T[qi * JLD + pj] : 0.f;
+                const float d = (vi && vj) ? T[qi * JLD + qj] : 0.f;
+                const float a1 = ci * a - si * cc, b1 = ci * bb - si * d;
+                const float c1 = si * a + ci * cc, d1 = si * bb + ci * d;
+                const float a2 = cj * a1 - sj * b1, d2 = sj * c1 + cj * d1;
+                float b2 = sj * a1 + cj * b1, c2 = cj * c1 - sj * d1;
+                if (i == j) {
+                    b2 = 0.f;
+                    c2 = 0.f;
+                }
+                T[pi * JLD + pj] = a2;
+                if (vj) T[pi * JLD + qj] = b2;
+                if (vi) T[qi * JLD + pj] = c2;
+                if (vi && vj) T[qi * JLD + qj] = d2;
+                if (i != j) {
+                    T[pj * JLD + pi] = a2;
+                    if (vj) T[qj * JLD + pi] = b2;
+                    if (vi) T[pj * JLD + qi] = c2;
+                    if (vi && vj) T[qj * JLD + qi] = d2;
+                }
             }
-            __syncthreads();
-            // Columns p, q of T and V  <- T J, V J.
-            for (int idx = t; idx < np * k; idx += JT) {
-                const int pr = idx / k, j = idx % k;
-                const int p = pp[pr], q = pq[pr];
-                if (q >= k || sn[pr] == 0.f) continue;
-                const float c = cs[pr], s = sn[pr];
-                const float a = T[j * JLD + p], b = T[j * JLD + q];
-                T[j * JLD + p] = c * a - s * b;
-                T[j * JLD + q] = s * a + c * b;
-                const float va = V[j * JLD + p], vb = V[j * JLD + q];
-                V[j * JLD + p] = c * va - s * vb;
-                V[j * JLD + q] = s * va + c * vb;
-            }
-            __syncthreads();
-            // Next round-robin arrangement: position 0 fixed, the others rotate.
-            if (t == 0) {
-                const int last = pos[kk - 1];
-                for (int i = kk - 1; i > 1; --i) pos[i] = pos[i - 1];
-                pos[1] = last;
+            // V <- V J: columns p_i, q_i of every row (q_i < k whenever s_i != 0).
+            // Thread t: pair i = t / 16 (+ 64 per pass), rows t % 16 + 16 m.
+            for (int i = t >> 4; i < np; i += JT >> 4) {
+                const float sv = sn[i];
+                if (sv == 0.f) continue;
+                const float c = cs[i];
+                const int p = pp[i], q = pq[i];
+                for (int r = t & 15; r < k; r += 16) {
+                    const float va = V[r * JLD + p], vb = V[r * JLD + q];
+                    V[r * JLD + p] = c * va - sv * vb;
+                    V[r * JLD + q] = sv * va + c * vb;
+                }
             }
             __syncthreads();
         }
-        if (t < np && sn[t] != 0.f) {
-            T[pp[t] * JLD + pq[t]] = 0.f;
-            T[pq[t] * JLD + pp[t]] = 0.f;
-            sn[t] = 0.f;
-        }
-        __syncthreads();
         if (!rotated) break;
         __syncthreads();
     }
     // Sort by descending eigenvalue (ties by index).
-    int *order = pos;
-    __syncthreads();
     for (int i = t; i < k; i += JT) {
         const float li = T[i * JLD + i];
         int rank = 0;
@@ -200,6 +227,7 @@ __global__ void __launch_bounds__(JT) jacobi_eig_kernel(const float *__restrict_
         W[idx] = V[row * JLD + order[col]];
     }
 }
+
 // Sign of each of nvec vectors of length n (entry e of vector v at
 // X[v * vs + e * es]): the entry of largest magnitude (first on ties) is made
 // positive; the vector is negated otherwise.  One CTA per vector.
@@ -265,13 +293,17 @@ cudaError_t cholqr_pass(const SubspaceBufs &w, float *src, float *dst, int k, in
     return sgemm<float>(k, cols, k, 1.f, w.Linv, 128, false, src, cols, false, 0.f, dst, cols, 0, s);
 }
 
-// Y = the block ZT (k x cols) times the symmetric G.
+// Y = the block ZT (k x cols) times the symmetric G.  On the tensor cores
+// either with float32 accuracy (3xTF32) or, when !accurate, as one TF32
+// product that reads only the hi half of G's split (half the bytes; for
+// cols <= 5120 that half fits in L2 across iterations).
 cudaError_t block_times_g(const SubspaceBufs &w, const float *ZT, float *Y, int k, int64_t cols, bool tc,
-                          cudaStream_t s) {
+                          bool accurate, cudaStream_t s) {
     if (!tc) return sgemm<float>(k, cols, cols, 1.f, ZT, cols, false, w.G, cols, false, 0.f, Y, cols, 0, s);
     cudaError_t e = split_tf32(ZT, k, cols, cols, w.Zhi, w.Zlo, cols, s);
     if (e != cudaSuccess) return e;
-    return gemm3_splitk(k, cols, cols, w.Zhi, w.Zlo, cols, w.Ghi, w.Glo, cols, Y, w.part, ZSPLIT, s);
+    return gemm3_splitk(k, cols, cols, w.Zhi, w.Zlo, cols, w.Ghi, w.Glo, cols, Y, w.part, zsplit(cols, k), s,
+                        !accurate);
 }
 
 }  // namespace
@@ -285,7 +317,7 @@ int subspace_width(int64_t cols, int r) {
 
 size_t subspace_part_floats(int k, int64_t cols, bool tc) {
     size_t part = (size_t)SPLITK * k * k;
-    if (tc && (size_t)ZSPLIT * k * cols > part) part = (size_t)ZSPLIT * k * cols;
+    if (tc && (size_t)zsplit(cols, k) * k * cols > part) part = (size_t)zsplit(cols, k) * k * cols;
     return part;
 }
 
@@ -298,7 +330,11 @@ cudaError_t subspace_ritz(const SubspaceBufs &w, int k, int64_t cols, bool tc, c
     if ((e = cudaMemcpyAsync(w.ZT, w.ZT2, (size_t)k * cols * sizeof(float), cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
         return e;
     for (int it = 0; it < ITERS; ++it) {
-        if ((e = block_times_g(w, w.ZT, w.ZT2, k, cols, tc, s)) != cudaSuccess) return e;
+        // TF32 products while the block converges; the last ACCURATE_TAIL
+        // iterations at float32 accuracy remove what TF32 rounding left in the
+        // subspace (each shrinks it by lambda_{k+1} / lambda_i per direction).
+        const bool accurate = it >= ITERS - ACCURATE_TAIL;
+        if ((e = block_times_g(w, w.ZT, w.ZT2, k, cols, tc, accurate, s)) != cudaSuccess) return e;
         if ((e = cholqr_pass(w, w.ZT2, w.ZT, k, cols, s)) != cudaSuccess) return e;
     }
     if ((e = cholqr_pass(w, w.ZT, w.ZT2, k, cols, s)) != cudaSuccess) return e;
@@ -306,7 +342,7 @@ cudaError_t subspace_ritz(const SubspaceBufs &w, int k, int64_t cols, bool tc, c
         return e;
 
     // Rayleigh-Ritz: T = Z^T G Z (k x k), eigenpairs by Jacobi.
-    if ((e = block_times_g(w, w.ZT, w.ZT2, k, cols, tc, s)) != cudaSuccess) return e;
+    if ((e = block_times_g(w, w.ZT, w.ZT2, k, cols, tc, true, s)) != cudaSuccess) return e;
     if ((e = sgemm_splitk(k, k, cols, w.ZT2, cols, false, w.ZT, cols, true, w.Gm, w.part, SPLITK, s)) != cudaSuccess)
         return e;
     static bool attr_set = false;

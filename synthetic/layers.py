@@ -67,6 +67,7 @@ class LayerSpec:
     block: int = 128
     damp: float = 0.01
     eora_rank: int = 0
+    lora_rank: int = 0  # GPTQ-intrinsic LoRA rank (0: plain GPTQ)
     notes: str = field(default="", compare=False)
 
     @property
@@ -110,12 +111,18 @@ LAYERS: dict[str, LayerSpec] = {
         LayerSpec("qwen72b_29568x8192", W=_w(29568, 8192, 0.015, (3, 1)), X=_X_QWEN72B_8192, bits=2, group=64),
         LayerSpec("qwen32b_5120x5120", W=_w(5120, 5120, 0.02, (4, 0)), X=_X_QWEN32B_5120, bits=2, group=64, eora_rank=64),
         LayerSpec("qwen32b_25600x5120", W=_w(25600, 5120, 0.02, (4, 1)), X=_X_QWEN32B_5120, bits=2, group=64, eora_rank=64),
+        # The same two layers with a rank-64 GPTQ-intrinsic LoRA in place of EoRA.
+        LayerSpec("qwen32b_5120x5120_intrinsic_r64", W=_w(5120, 5120, 0.02, (4, 0)), X=_X_QWEN32B_5120, bits=2,
+                  group=64, lora_rank=64),
+        LayerSpec("qwen32b_25600x5120_intrinsic_r64", W=_w(25600, 5120, 0.02, (4, 1)), X=_X_QWEN32B_5120, bits=2,
+                  group=64, lora_rank=64),
     ]
 }
 
 
 def custom_layer(name, rows, cols, n, *, bits=4, group=128, block=128, damp=0.01, x_dist="t", nu=4.0,
-                 n_outliers=0, outlier_scale=30.0, w_std=0.02, dtype="bf16", key=(9,), eora_rank=0) -> LayerSpec:
+                 n_outliers=0, outlier_scale=30.0, w_std=0.02, dtype="bf16", key=(9,), eora_rank=0,
+                 lora_rank=0) -> LayerSpec:
     """A small layer with the same recipe as the workloads, for parity cases."""
     key = tuple(key)
     return LayerSpec(
@@ -123,7 +130,7 @@ def custom_layer(name, rows, cols, n, *, bits=4, group=128, block=128, damp=0.01
         W=TensorSpec(rows, cols, "normal", std=w_std, dtype=dtype, key=key + (0,)),
         X=TensorSpec(n, cols, x_dist, nu=nu, n_outliers=n_outliers, outlier_scale=outlier_scale, dtype=dtype,
                      key=key + (1,)),
-        bits=bits, group=group, block=block, damp=damp, eora_rank=eora_rank,
+        bits=bits, group=group, block=block, damp=damp, eora_rank=eora_rank, lora_rank=lora_rank,
     )
 
 
