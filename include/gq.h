@@ -259,6 +259,34 @@ gq_status gptq_intrinsic_lora(const void *W, gq_dtype wt, int64_t rows, int64_t 
                               float *R, void *ws, size_t ws_bytes, gq_stream_t stream, int64_t *info);
 
 /*
+ * The quantized layer applied from its packed form ([LowBit] sections 1 and
+ * 6: codes, per-group scale and zero point, dequantized inside the product;
+ * [EoRA-blog] "Bucear en el espacio propio en busca de un adaptador": the
+ * adapter B A added to the quantized weights, which also carries a
+ * GPTQ-intrinsic LoRA with B = R, A = L^T):
+ *
+ *     Y = X Ŵ^T + (X A^T) B^T,    Ŵ[m, k] = scales[k / group][m] (q[m, k] - z[k / group][m])
+ *
+ * Ŵ is not rounded: each group's integer products are summed on the tensor
+ * cores and scaled in float32, so Y is exact up to float32 summation.
+ *
+ *   X        n x cols bf16, row stride ldx (ldx >= cols, ldx % 8 == 0), 16-byte aligned.
+ *   qweight, scales, qzeros   the layout gptq_quantize_layer writes for a layer of
+ *            rows x cols at `bits` (2, 3, 4) and `group`; qweight and scales 16-byte aligned.
+ *            Requires rows % 32 == 0, group % 64 == 0 (else GQ_EUNSUPPORTED), cols % group == 0.
+ *   A, B     the adapter, r x cols and rows x r float32, or both NULL with r = 0; 0 <= r <= 64.
+ *   Y        n x rows float32 output, row stride ldy (ldy >= rows, ldy % 4 == 0), 16-byte aligned.
+ *   n        0 <= n <= 65535 * 128 tokens; n = 0 returns GQ_OK at once (X, Y may then be NULL).
+ *   ws       >= gptq_packed_linear_workspace_size(n, r) bytes (holds X A^T); may be NULL when r = 0.
+ * Asynchronous.
+ */
+size_t gptq_packed_linear_workspace_size(int64_t n, int r);
+gq_status gptq_packed_linear(const void *X, int64_t n, int64_t ldx, const int32_t *qweight, const float *scales,
+                             const int32_t *qzeros, int64_t rows, int64_t cols, int bits, int group, const float *A,
+                             const float *B, int r, float *Y, int64_t ldy, void *ws, size_t ws_bytes,
+                             gq_stream_t stream);
+
+/*
  * gptq_quantize_layer without a caller-provided workspace, for callers that
  * cannot allocate device memory: code inside a host application that owns all
  * device memory through its own pool, a service that must not grow its device

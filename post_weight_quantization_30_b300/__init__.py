@@ -14,6 +14,7 @@ from ._lib import (  # noqa: F401
     gptq_hessian_accumulate,
     gptq_intrinsic_lora,
     gptq_lora_basis,
+    gptq_packed_linear,
     gptq_pack,
     gptq_quantize_layer,
     gptq_quantize_layer_noalloc,

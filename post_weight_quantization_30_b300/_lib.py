@@ -58,6 +58,8 @@ SIGNATURES = {
     "gptq_intrinsic_lora_workspace_size": (_sz, [_i64, _i64, _i, _i]),
     "gptq_intrinsic_lora": (_i, [_p, _i, _i64, _i64, _p, _p, _i, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p, _p,
                                  _sz, _p, ctypes.POINTER(_i64)]),
+    "gptq_packed_linear_workspace_size": (_sz, [_i64, _i]),
+    "gptq_packed_linear": (_i, [_p, _i64, _i64, _p, _p, _p, _i64, _i64, _i, _i, _p, _p, _i, _p, _i64, _p, _sz, _p]),
     "gptq_code_decisions": (_i, [_p, _p, _i64, _p, _p]),
     "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
     "gptq_unpack": (_i, [_p, _i64, _i64, _i, _p, _p]),
@@ -283,6 +285,26 @@ def gptq_intrinsic_lora(W: torch.Tensor, H: torch.Tensor, Lt: torch.Tensor, bits
                                    _ptr(o["R"]), _ptr(ws), ws.numel(), _stream(W.device), ctypes.byref(info)),
            "gptq_intrinsic_lora", info.value)
     return o
+
+
+def gptq_packed_linear(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor, rows: int,
+                       cols: int, bits: int, group: int, A: torch.Tensor | None = None, B: torch.Tensor | None = None,
+                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Y = X Ŵ^T (+ (X A^T) B^T) from the packed layer; X bf16 (n x cols), Y float32 (n x rows)."""
+    _need_cuda(X, qweight, scales, qzeros, A, B)
+    if X.dtype != torch.bfloat16:
+        raise ValueError("X must be bf16")
+    n = X.shape[0]
+    r = 0 if A is None else A.shape[0]
+    Y = out if out is not None else torch.empty((n, rows), dtype=torch.float32, device=X.device)
+    ws_bytes = lib.gptq_packed_linear_workspace_size(n, r)
+    ws = workspace if workspace is not None else (_workspace(ws_bytes, X.device) if ws_bytes else None)
+    _check(lib.gptq_packed_linear(_ptr(X), n, X.stride(0), _ptr(qweight.contiguous()), _ptr(scales.contiguous()),
+                                  _ptr(qzeros.contiguous()), rows, cols, bits, group,
+                                  _ptr(None if A is None else A.contiguous()),
+                                  _ptr(None if B is None else B.contiguous()), r, _ptr(Y), Y.stride(0), _ptr(ws),
+                                  0 if ws is None else ws.numel(), _stream(X.device)), "gptq_packed_linear")
+    return Y
 
 
 def gq_check_device(device=None):

@@ -281,8 +281,9 @@ gq_status gq_check_device(gq_stream_t stream) {
     if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return GQ_ECUDA;
     const unsigned int e1 = read_and_clear_device_error();
     const unsigned int e2 = gemm_read_and_clear_error();
-    if (e1 == ~0u || e2 == ~0u) return GQ_ECUDA;
-    return (e1 | e2) ? GQ_ETIMEOUT : GQ_OK;
+    const unsigned int e3 = packed_read_and_clear_error();
+    if (e1 == ~0u || e2 == ~0u || e3 == ~0u) return GQ_ECUDA;
+    return (e1 | e2 | e3) ? GQ_ETIMEOUT : GQ_OK;
 }
 
 gq_status gptq_hessian_accumulate(float *H, int64_t cols, const void *X, gq_dtype xt, int64_t n, int64_t ldx,
@@ -398,6 +399,35 @@ gq_status gptq_intrinsic_lora(const void *W, gq_dtype wt, int64_t rows, int64_t 
         return GQ_EWORKSPACE;
     return intrinsic_impl(W, wt, rows, cols, H, Lt, r, bits, group, block, damp, qweight, scales, qzeros, codes,
                           W_hat, row_err, R, ws, cs(stream), info);
+}
+
+size_t gptq_packed_linear_workspace_size(int64_t n, int r) {
+    if (n <= 0 || r <= 0) return 0;
+    return align_up((size_t)n * r * sizeof(float));
+}
+
+gq_status gptq_packed_linear(const void *X, int64_t n, int64_t ldx, const int32_t *qweight, const float *scales,
+                             const int32_t *qzeros, int64_t rows, int64_t cols, int bits, int group, const float *A,
+                             const float *B, int r, float *Y, int64_t ldy, void *ws, size_t ws_bytes,
+                             gq_stream_t stream) {
+    if (bits != 2 && bits != 3 && bits != 4) return GQ_EUNSUPPORTED;
+    if (group <= 0 || group % 64) return GQ_EUNSUPPORTED;
+    if (rows <= 0 || rows % 32 || rows > INT32_MAX || cols <= 0 || cols % group || cols > INT32_MAX) return GQ_EINVAL;
+    if (n < 0 || n > (int64_t)65535 * 128 || r < 0 || r > 64) return GQ_EINVAL;
+    if (n == 0) return GQ_OK;  // no token: nothing is read or written (X and Y may be NULL)
+    if (!X || !qweight || !scales || !qzeros || !Y) return GQ_EINVAL;
+    if (ldx < cols || ldx % 8 || !aligned(X, 16)) return GQ_EINVAL;
+    if (ldy < rows || ldy % 4 || !aligned(Y, 16)) return GQ_EINVAL;
+    if (!aligned(scales, 16) || !aligned(qweight, 16) || !aligned(qzeros, 4)) return GQ_EINVAL;
+    if (r > 0) {
+        if (!A || !B || !aligned(A, 4) || !aligned(B, 4)) return GQ_EINVAL;
+        if (!ws || !aligned(ws, kAlign) || ws_bytes < gptq_packed_linear_workspace_size(n, r)) return GQ_EWORKSPACE;
+    }
+    return packed_linear_launch((const __nv_bfloat16 *)X, n, ldx, qweight, scales, qzeros, rows, cols, bits, group,
+                                r > 0 ? A : nullptr, r > 0 ? B : nullptr, r, r > 0 ? (float *)ws : nullptr, Y, ldy,
+                                cs(stream)) == cudaSuccess
+               ? GQ_OK
+               : GQ_ECUDA;
 }
 
 gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *W_hat, float *dW,

@@ -200,6 +200,14 @@ cudaError_t schur_init_launch(const float *H, int64_t cols, const DeviceStatus *
 cudaError_t dw_split_launch(const void *W, bool w_bf16, const float *W_hat, const uint8_t *dead, int64_t rows,
                             int64_t cols, float *hi, float *lo, cudaStream_t s);
 
+// Packed quantized linear layer (packed_linear.cu): Y = X Ŵ^T (+ (X A^T) B^T when r > 0,
+// with T = X A^T written to T, n x r).  Requirements checked by the caller (gq.h).
+cudaError_t packed_linear_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const int32_t *qweight,
+                                 const float *scales, const int32_t *qzeros, int64_t rows, int64_t cols, int bits,
+                                 int group, const float *A, const float *B, int r, float *T, float *Y, int64_t ldy,
+                                 cudaStream_t s);
+unsigned int packed_read_and_clear_error();
+
 // dW = W - W_hat, n elements (W float32 or bf16).
 cudaError_t weight_error_launch(const void *W, bool w_bf16, int64_t n, const float *W_hat, float *dW, cudaStream_t s);
 

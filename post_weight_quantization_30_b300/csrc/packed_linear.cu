@@ -1,0 +1,553 @@
+// The quantized linear layer computed from its packed form, on the
+// fifth-generation tensor cores (sm_103a):
+//
+//     Y = X Ŵ^T + (X A^T) B^T,      Ŵ[m, k] = s[k / g, m] (q[m, k] - z[k / g, m])
+//
+// ("El balance de errores de la inferencia de pocos bits", sections 1 and 6:
+// codes, per-group scale and zero point, dequantized on the fly inside the
+// product; "Aumento de la precisión de LLM de 2 bits con EoRA", the adapter
+// B A added to the quantized weights.)
+//
+// Ŵ is never rounded.  Each code minus its zero point is a small integer
+// (|q - z| < 16), exact in bf16, and a bf16 input times such an integer is
+// exact in float32, so the tensor core accumulates exact products of one
+// group's K range into TMEM; the epilogue adds s[g, m] times that partial into
+// float32 registers.  The result is X Ŵ^T up to float32 summation.
+//
+// Design (one CTA per 128 tokens x 128 output columns = rows of W):
+// * warp 0 / lane 0: TMA loads, per stage, of the X tile (128 tokens x 64 K,
+//   bf16, K-major, 128-byte swizzle) and of the tile's packed words (64 K-values
+//   x 128 rows of W as 2b word-rows of 128 int32), four-stage mbarrier pipeline;
+// * warps 2-5 (one thread per row of W): read the row's words from shared
+//   memory, unpack the codes, subtract the group's zero point and write the
+//   bf16 integers straight into the 128-byte-swizzled K-major operand tile,
+//   then fence to the async proxy and arrive on the stage's ready barrier;
+// * warp 1 / lane 0: tcgen05.mma kind::f16 (M = N = 128, K = 16), one group's
+//   k-tiles into one of two TMEM accumulators;
+// * warps 6-13: per group, read the accumulator (TMEM lane quarter = warp % 4,
+//   one half of the 128 columns per warp), scale by the group's per-row scales
+//   and add into registers; at the end add the adapter term T B^T (T = X A^T
+//   from lora_t_kernel, B staged in shared memory) in float32 and store Y
+//   through shared memory, coalesced.
+// Every mbarrier wait is bounded; on expiry the CTA records the error flag that
+// gq_check_device reports and exits without writing Y.
+#include "tc_common.cuh"
+
+namespace gq {
+
+// Bit 0: a bounded wait of this file's kernels gave up.
+__device__ unsigned int g_packed_error = 0;
+
+namespace {
+using namespace tc;
+
+constexpr int PM = 128, PN = 128, PK = 64;
+constexpr int P_STAGES = 4;
+constexpr int TILE_X = PM * PK * 2;              // 16 KB
+constexpr int TILE_W = PN * PK * 2;              // 16 KB
+constexpr int TILE_Q = PN * PK * 4 / 8;          // packed words of one stage, at most (4-bit): 4 KB
+constexpr int P_STAGE = TILE_X + TILE_W + TILE_Q;  // 36 KB (X and W tiles 1024-byte aligned)
+constexpr int P_SMEM = P_STAGES * P_STAGE + 1024;
+constexpr uint32_t P_TMEM = PN;                  // columns per accumulator buffer
+constexpr int P_NWARPS = 14;                     // TMA, MMA, 4 dequant, 8 epilogue
+constexpr int P_EPI = 8;                         // epilogue warps: 4 lane quarters x 2 column halves
+constexpr int P_HALF = PN / 2;                   // columns per epilogue thread
+constexpr int P_STAGE_LD = PN + 4;               // epilogue staging row stride (floats)
+constexpr int ADAPTER_MAX_R = 64;
+static_assert(4 * 32 * P_STAGE_LD * 4 + PN * ADAPTER_MAX_R * 4 <= P_STAGES * P_STAGE, "epilogue smem");
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, N >> 3
+// at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16_kmajor(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// The b-bit field starting at bit `bit` of a little-endian stream of 32-bit
+// words, word i at p[i * stride] (fields may straddle two words).
+__device__ __forceinline__ uint32_t packed_field(const int32_t *__restrict__ p, int64_t stride, int64_t bit, int b) {
+    const int64_t wi = bit >> 5;
+    const int sh = (int)(bit & 31);
+    uint32_t v = (uint32_t)p[wi * stride] >> sh;
+    if (sh + b > 32) v |= (uint32_t)p[(wi + 1) * stride] << (32 - sh);
+    return v & ((1u << b) - 1u);
+}
+
+// Eight 4-bit codes of one word (code i at bits [4i, 4i + 4)) as four bf16x2
+// words holding (128 + q_2j, 128 + q_2j+1): a bf16 with biased exponent 134
+// (0x43) has a unit step, so 0x4300 | q is 128 + q exactly for q < 128.
+__device__ __forceinline__ void codes4_to_bf16(uint32_t w, uint32_t (&o)[4]) {
+    const uint32_t t = w & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6
+    const uint32_t u = (w >> 4) & 0x0F0F0F0Fu;   // codes 1, 3, 5, 7
+    const uint32_t m0 = __byte_perm(t, u, 0x5140);  // bytes c0 c1 c2 c3
+    const uint32_t m1 = __byte_perm(t, u, 0x7362);  // bytes c4 c5 c6 c7
+    o[0] = __byte_perm(m0, 0x43434343u, 0x4140);
+    o[1] = __byte_perm(m0, 0x43434343u, 0x4342);
+    o[2] = __byte_perm(m1, 0x43434343u, 0x4140);
+    o[3] = __byte_perm(m1, 0x43434343u, 0x4342);
+}
+
+// Sixteen 2-bit codes of one word (code i at bits [2i, 2i + 2)) likewise, as
+// eight bf16x2 words (128 + q_2j, 128 + q_2j+1).
+__device__ __forceinline__ void codes2_to_bf16(uint32_t w, uint32_t (&o)[8]) {
+    const uint32_t t0 = w & 0x03030303u;          // codes 0, 4, 8, 12
+    const uint32_t t1 = (w >> 2) & 0x03030303u;   // codes 1, 5, 9, 13
+    const uint32_t t2 = (w >> 4) & 0x03030303u;   // codes 2, 6, 10, 14
+    const uint32_t t3 = (w >> 6) & 0x03030303u;   // codes 3, 7, 11, 15
+    const uint32_t a0 = __byte_perm(t0, t1, 0x5140);  // c0 c1 c4 c5
+    const uint32_t a1 = __byte_perm(t2, t3, 0x5140);  // c2 c3 c6 c7
+    const uint32_t b0 = __byte_perm(t0, t1, 0x7362);  // c8 c9 c12 c13
+    const uint32_t b1 = __byte_perm(t2, t3, 0x7362);  // c10 c11 c14 c15
+    o[0] = __byte_perm(a0, 0x43434343u, 0x4140);  // c0 c1
+    o[1] = __byte_perm(a1, 0x43434343u, 0x4140);  // c2 c3
+    o[2] = __byte_perm(a0, 0x43434343u, 0x4342);  // c4 c5
+    o[3] = __byte_perm(a1, 0x43434343u, 0x4342);  // c6 c7
+    o[4] = __byte_perm(b0, 0x43434343u, 0x4140);  // c8 c9
+    o[5] = __byte_perm(b1, 0x43434343u, 0x4140);  // c10 c11
+    o[6] = __byte_perm(b0, 0x43434343u, 0x4342);  // c12 c13
+    o[7] = __byte_perm(b1, 0x43434343u, 0x4342);  // c14 c15
+}
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&b));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// The stage's 64 values (q - z) of one row as 32 bf16x2 words (K order).
+// Exact: every operand is an integer below 256.
+template <int BITS>
+__device__ __forceinline__ void dequant_row(const uint32_t (&w)[PK * BITS / 32], uint32_t zz, bool valid,
+                                            float zf, uint32_t (&o)[32]) {
+    if constexpr (BITS == 4) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t t[4];
+            codes4_to_bf16(w[i], t);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) o[i * 4 + h] = bf16x2_sub(t[h], zz);
+        }
+    } else if constexpr (BITS == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t t[8];
+            codes2_to_bf16(w[i], t);
+#pragma unroll
+            for (int h = 0; h < 8; ++h) o[i * 8 + h] = bf16x2_sub(t[h], zz);
+        }
+    } else {
+        // 3-bit codes straddle words: extract each one.
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+            float d[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int bit = (h * 2 + e) * BITS;
+                const int wi = bit >> 5, sh = bit & 31;
+                uint32_t v = w[wi] >> sh;
+                if (sh + BITS > 32) v |= w[wi + 1] << (32 - sh);
+                d[e] = (float)(v & ((1u << BITS) - 1u)) - zf;
+            }
+            const __nv_bfloat162 p2 = __floats2bfloat162_rn(d[0], d[1]);
+            o[h] = *reinterpret_cast<const uint32_t *>(&p2);
+        }
+    }
+    if (!valid) {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) o[h] = 0u;
+    }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(P_NWARPS * 32, 1)
+    packed_linear_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
+                         const float *__restrict__ scales, const int32_t *__restrict__ qzeros, int n, int rows,
+                         int cols, int group, const float *__restrict__ T, const float *__restrict__ Bad, int r,
+                         float *__restrict__ Y, int64_t ldy) {
+    constexpr int NW = PK * BITS / 32;  // packed words per row per stage
+    const int m0 = blockIdx.y * PM, n0 = blockIdx.x * PN;
+    const int ktiles = cols / PK;
+    const int ktg = group / PK;  // k-tiles per group
+    const int ngroups = cols / group;
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[P_STAGES];   // X and packed words landed (TMA)
+    __shared__ __align__(8) uint64_t ready_bar[P_STAGES];  // the bf16 operand tile is written
+    __shared__ __align__(8) uint64_t empty_bar[P_STAGES];
+    __shared__ __align__(8) uint64_t tfull[2];
+    __shared__ __align__(8) uint64_t tempty[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    // Scales of this tile's rows for groups gi (slot gi % 2) and gi + 1, staged by
+    // the epilogue warps themselves (next group's loaded while this one drains).
+    __shared__ __align__(16) float sc_ring[2][PN];
+    __shared__ int epi_abort;
+
+    unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);   // the TMA thread's expect_tx
+            mbar_init(&ready_bar[s], 4);  // one arrival per dequantization warp
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], P_EPI);
+        }
+        abort_flag = 0;
+        epi_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(2 * P_TMEM)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tmem_slot;
+    bool ok = true;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kt = 0; kt < ktiles; ++kt) {
+                const int s = kt % P_STAGES;
+                const uint32_t ph = (uint32_t)(kt / P_STAGES) & 1u;
+                if (!mbar_wait(&empty_bar[s], ph ^ 1u) || *(volatile int *)&abort_flag) {
+                    atomicOr(&g_packed_error, 1u);
+                    abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full_bar[s], TILE_X + NW * PN * 4);
+                tma_load_2d(smem + s * P_STAGE, &xmap, kt * PK, m0, &full_bar[s]);
+                tma_load_2d(smem + s * P_STAGE + TILE_X + TILE_W, &qmap, n0, kt * NW, &full_bar[s]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_kmajor(PM, PN);
+            for (int gi = 0; gi < ngroups && ok; ++gi) {
+                const int b = gi & 1;
+                const uint32_t u = (uint32_t)(gi >> 1) & 1u;
+                if (!mbar_wait(&tempty[b], u ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const uint32_t acc = tmem + (uint32_t)(b * P_TMEM);
+                for (int kt = gi * ktg; kt < (gi + 1) * ktg; ++kt) {
+                    const int s = kt % P_STAGES;
+                    const uint32_t ph = (uint32_t)(kt / P_STAGES) & 1u;
+                    // full: the X tile landed (TMA); ready: the W tile is written.
+                    if (!mbar_wait(&full_bar[s], ph) || !mbar_wait(&ready_bar[s], ph)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t xa = smem_u32(smem + s * P_STAGE);
+                    const uint32_t wa = xa + TILE_X;
+#pragma unroll
+                    for (int kk = 0; kk < PK / 16; ++kk) {
+                        // K-major, 128-byte swizzle: 8-row groups 1024 B apart; a
+                        // k-step of 16 bf16 values advances the start by 32 bytes.
+                        const uint64_t da = smem_desc(xa + kk * 32, 16, 1024);
+                        const uint64_t dw = smem_desc(wa + kk * 32, 16, 1024);
+                        mma_bf16(acc, da, dw, idesc, (kt == gi * ktg && kk == 0) ? 0u : 1u);
+                    }
+                    mma_commit(&empty_bar[s]);
+                }
+                if (!ok) break;
+                mma_commit(&tfull[b]);
+            }
+            if (!ok) {
+                atomicOr(&g_packed_error, 1u);
+                abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // Dequantization: thread t owns row n0 + t of W.  Its packed words arrive
+        // with the stage (TMA); the zero point of the next group is loaded one
+        // group ahead.
+        const int t = threadIdx.x - 64;
+        const int nrow = n0 + t;
+        const bool valid = nrow < rows;
+        const int64_t zwords = (int64_t)rows * BITS / 32;  // qzeros words per group
+        auto zero_of = [&](int g) -> float {
+            return valid ? (float)packed_field(qzeros + (int64_t)g * zwords, 1, (int64_t)nrow * BITS, BITS) : 0.f;
+        };
+        float zf = zero_of(0);
+        float znext = ngroups > 1 ? zero_of(1) : 0.f;
+        uint32_t zz = 0u;
+        {
+            const __nv_bfloat162 z2 = __floats2bfloat162_rn(128.f + zf, 128.f + zf);
+            zz = *reinterpret_cast<const uint32_t *>(&z2);
+        }
+        for (int kt = 0; kt < ktiles; ++kt) {
+            const int s = kt % P_STAGES;
+            const uint32_t ph = (uint32_t)(kt / P_STAGES) & 1u;
+            if (kt > 0 && kt % ktg == 0) {  // a new group starts
+                const int g = kt / ktg;
+                zf = znext;
+                znext = g + 1 < ngroups ? zero_of(g + 1) : 0.f;
+                const __nv_bfloat162 z2 = __floats2bfloat162_rn(128.f + zf, 128.f + zf);
+                zz = *reinterpret_cast<const uint32_t *>(&z2);
+            }
+            if (!mbar_wait(&full_bar[s], ph) || *(volatile int *)&abort_flag) {
+                ok = false;
+                break;
+            }
+            const uint32_t *wq = reinterpret_cast<const uint32_t *>(smem + s * P_STAGE + TILE_X + TILE_W);
+            uint32_t w[NW];
+#pragma unroll
+            for (int i = 0; i < NW; ++i) w[i] = wq[i * PN + t];
+            uint32_t o[32];
+            dequant_row<BITS>(w, zz, valid, zf, o);
+            unsigned char *dst = smem + s * P_STAGE + TILE_X + t * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(dst + ((c ^ (t & 7)) << 4)) =
+                    make_uint4(o[c * 4], o[c * 4 + 1], o[c * 4 + 2], o[c * 4 + 3]);
+            // Generic-proxy writes -> visible to the tensor core's async proxy.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ready_bar[s]);
+        }
+        if (!ok) {
+            atomicOr(&g_packed_error, 1u);
+            abort_flag = 1;
+        }
+        __syncwarp();
+    } else {
+        // Epilogue warps: TMEM lane quarter = warp % 4, column half hf; each
+        // thread owns one token row x 64 columns.
+        const int q = warp & 3, hf = (warp - 6) >> 2;
+        const int cb = hf * P_HALF;  // first column of this warp's half
+        float acc[P_HALF];
+#pragma unroll
+        for (int i = 0; i < P_HALF; ++i) acc[i] = 0.f;
+        const int et = threadIdx.x - 192;  // 0..255 over the eight epilogue warps
+        if (et < PN) sc_ring[0][et] = (n0 + et < rows) ? __ldg(scales + n0 + et) : 0.f;
+        asm volatile("bar.sync 1, %0;" ::"n"(P_EPI * 32) : "memory");
+        for (int gi = 0; gi < ngroups; ++gi) {
+            // Next group's scale for one row, in flight while this group drains.
+            float nxt = 0.f;
+            if (et < PN && gi + 1 < ngroups && n0 + et < rows) nxt = __ldg(scales + (int64_t)(gi + 1) * rows + n0 + et);
+            const int b = gi & 1;
+            const uint32_t u = (uint32_t)(gi >> 1) & 1u;
+            if (!mbar_wait(&tfull[b], u)) {
+                ok = false;
+                epi_abort = 1;
+            } else {
+                __syncwarp();
+                fence_after();
+                const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * P_TMEM + cb);
+                const float *sg = &sc_ring[gi & 1][cb];
+#pragma unroll
+                for (int ch = 0; ch < P_HALF / 32; ++ch) {
+                    float v[32];
+                    tmem_ld32(base + ch * 32, v);
+#pragma unroll
+                    for (int i4 = 0; i4 < 8; ++i4) {
+                        const float4 s4 = *(reinterpret_cast<const float4 *>(sg + ch * 32) + i4);
+                        acc[ch * 32 + i4 * 4 + 0] = fmaf(s4.x, v[i4 * 4 + 0], acc[ch * 32 + i4 * 4 + 0]);
+                        acc[ch * 32 + i4 * 4 + 1] = fmaf(s4.y, v[i4 * 4 + 1], acc[ch * 32 + i4 * 4 + 1]);
+                        acc[ch * 32 + i4 * 4 + 2] = fmaf(s4.z, v[i4 * 4 + 2], acc[ch * 32 + i4 * 4 + 2]);
+                        acc[ch * 32 + i4 * 4 + 3] = fmaf(s4.w, v[i4 * 4 + 3], acc[ch * 32 + i4 * 4 + 3]);
+                    }
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[b]);
+            }
+            if (et < PN) sc_ring[(gi + 1) & 1][et] = nxt;
+            // Every epilogue warp reaches this barrier once per group, failed or not,
+            // and all leave the loop together on a failure.
+            asm volatile("bar.sync 1, %0;" ::"n"(P_EPI * 32) : "memory");
+            if (*(volatile int *)&epi_abort) break;
+        }
+        if (!ok) {
+            atomicOr(&g_packed_error, 1u);
+            abort_flag = 1;
+        }
+        // The pipeline stages are idle now (every stage was consumed before the
+        // last group's accumulator completed): staging rows, then the adapter's B.
+        float *stage = reinterpret_cast<float *>(smem) + (size_t)q * 32 * P_STAGE_LD;
+        float *Bs = reinterpret_cast<float *>(smem) + (size_t)4 * 32 * P_STAGE_LD;
+        const int m = m0 + q * 32 + lane;  // this thread's token row
+        if (r > 0) {
+            // Bs[i][c] = B[n0 + c][i] (i-major: a thread's 64 columns are contiguous).
+            // The tile's rows of B are one contiguous block: read it in order.
+            const int nvalid = (rows - n0) < PN ? (rows - n0) : PN;
+            for (int idx = et; idx < PN * r; idx += P_EPI * 32) {
+                const int c = idx / r, i = idx - c * r;
+                Bs[i * PN + c] = (c < nvalid) ? __ldg(Bad + (int64_t)n0 * r + idx) : 0.f;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(P_EPI * 32) : "memory");
+            if (ok && m < n) {
+                const float *tm = T + (int64_t)m * r;
+                for (int i0 = 0; i0 < r; i0 += 16) {
+                    // sixteen independent loads in flight, then their products
+                    float tv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) tv[j] = (i0 + j < r) ? __ldg(tm + i0 + j) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (i0 + j >= r) break;
+                        const float *bi = Bs + (size_t)(i0 + j) * PN + cb;
+#pragma unroll
+                        for (int c = 0; c < P_HALF; c += 4) {
+                            const float4 b4 = *reinterpret_cast<const float4 *>(bi + c);
+                            acc[c] = fmaf(tv[j], b4.x, acc[c]);
+                            acc[c + 1] = fmaf(tv[j], b4.y, acc[c + 1]);
+                            acc[c + 2] = fmaf(tv[j], b4.z, acc[c + 2]);
+                            acc[c + 3] = fmaf(tv[j], b4.w, acc[c + 3]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < P_HALF; j += 4)
+            *reinterpret_cast<float4 *>(stage + lane * P_STAGE_LD + cb + j) =
+                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+        __syncwarp();
+        // Store this warp's 32 rows x 64 columns: lanes 0-15 one row, 16-31 the next,
+        // 16 bytes per lane (256 contiguous bytes per row).
+        const int c = n0 + cb + (lane & 15) * 4;  // rows % 4 == 0
+        if (ok && c < rows) {
+            for (int rr = lane >> 4; rr < 32; rr += 2) {
+                const int mr = m0 + q * 32 + rr;
+                if (mr >= n) break;
+                const float4 v = *reinterpret_cast<const float4 *>(stage + rr * P_STAGE_LD + cb + (lane & 15) * 4);
+                *reinterpret_cast<float4 *>(Y + (int64_t)mr * ldy + c) = v;
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * P_TMEM) : "memory");
+    }
+}
+
+// T = X A^T (n x r) in float32: X bf16 (n x cols), A float32 (r x cols), r <= 64.
+// One CTA per 32 tokens; K in chunks of 64 staged in shared memory; thread t
+// owns token t / 8 and the adapter rows t % 8 + 8 j.
+__global__ void __launch_bounds__(256) lora_t_kernel(const __nv_bfloat16 *__restrict__ X, int64_t ldx, int n,
+                                                     int cols, const float *__restrict__ A, int r,
+                                                     float *__restrict__ T) {
+    __shared__ float Xs[32][PK + 1];
+    __shared__ float As[ADAPTER_MAX_R][PK + 1];
+    const int m0 = blockIdx.x * 32;
+    const int t = threadIdx.x, tm = t >> 3, ig = t & 7;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int k0 = 0; k0 < cols; k0 += PK) {
+        for (int idx = t; idx < 32 * PK; idx += 256) {
+            const int row = idx / PK, col = idx % PK;
+            Xs[row][col] = (m0 + row < n) ? __bfloat162float(X[(int64_t)(m0 + row) * ldx + k0 + col]) : 0.f;
+        }
+        for (int idx = t; idx < ADAPTER_MAX_R * PK; idx += 256) {
+            const int i = idx / PK, col = idx % PK;
+            As[i][col] = (i < r) ? A[(int64_t)i * cols + k0 + col] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < PK; ++kk) {
+            const float x = Xs[tm][kk];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(x, As[ig + 8 * j][kk], acc[j]);
+        }
+        __syncthreads();
+    }
+    const int m = m0 + tm;
+    if (m < n)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (ig + 8 * j < r) T[(int64_t)m * r + ig + 8 * j] = acc[j];
+}
+
+bool make_x_map(CUtensorMap *map, const __nv_bfloat16 *X, int64_t n, int64_t cols, int64_t ldx) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)n};
+    cuuint64_t gstride[1] = {(cuuint64_t)ldx * 2};
+    cuuint32_t box[2] = {(cuuint32_t)PK, (cuuint32_t)PM};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)X, gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The packed words as a 2-D int32 tensor: rows (contiguous) x cols * bits / 32
+// word-rows; a stage's box is 128 rows x 2 bits word-rows.
+bool make_q_map(CUtensorMap *map, const int32_t *qweight, int64_t rows, int64_t cols, int bits) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)rows, (cuuint64_t)(cols * bits / 32)};
+    cuuint64_t gstride[1] = {(cuuint64_t)rows * 4};
+    cuuint32_t box[2] = {(cuuint32_t)PN, (cuuint32_t)(PK * bits / 32)};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, (void *)qweight, gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BITS>
+cudaError_t launch_bits(const CUtensorMap &xmap, const CUtensorMap &qmap, const float *scales, const int32_t *qzeros,
+                        int n, int rows, int cols, int group, const float *T, const float *B, int r, float *Y,
+                        int64_t ldy, cudaStream_t s) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e =
+            cudaFuncSetAttribute(packed_linear_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid((unsigned)((rows + PN - 1) / PN), (unsigned)((n + PM - 1) / PM));
+    packed_linear_kernel<BITS><<<grid, P_NWARPS * 32, P_SMEM, s>>>(xmap, qmap, scales, qzeros, n, rows, cols,
+                                                                   group, T, B, r, Y, ldy);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+unsigned int packed_read_and_clear_error() {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_packed_error, sizeof(v)) != cudaSuccess) return ~0u;
+    const unsigned int zero = 0;
+    if (v) cudaMemcpyToSymbol(g_packed_error, &zero, sizeof(zero));
+    return v;
+}
+
+cudaError_t packed_linear_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const int32_t *qweight,
+                                 const float *scales, const int32_t *qzeros, int64_t rows, int64_t cols, int bits,
+                                 int group, const float *A, const float *B, int r, float *T, float *Y, int64_t ldy,
+                                 cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    if (r > 0) {
+        lora_t_kernel<<<(unsigned)((n + 31) / 32), 256, 0, s>>>(X, ldx, (int)n, (int)cols, A, r, T);
+        count_launch();
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap xmap, qmap;
+    if (!make_x_map(&xmap, X, n, cols, ldx) || !make_q_map(&qmap, qweight, rows, cols, bits))
+        return cudaErrorInvalidValue;
+    switch (bits) {
+        case 2: return launch_bits<2>(xmap, qmap, scales, qzeros, (int)n, (int)rows, (int)cols, group, T, B, r, Y, ldy, s);
+        case 3: return launch_bits<3>(xmap, qmap, scales, qzeros, (int)n, (int)rows, (int)cols, group, T, B, r, Y, ldy, s);
+        case 4: return launch_bits<4>(xmap, qmap, scales, qzeros, (int)n, (int)rows, (int)cols, group, T, B, r, Y, ldy, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gq

@@ -114,3 +114,25 @@ def test_intrinsic_lora_host_side_validation(gq):
     assert call(Lt=None) == -1
     assert call(bits=5) == -3
     assert call(ws_bytes=ws - 1) == -7
+
+
+def test_packed_linear_host_side_validation(gq):
+    p = ctypes.c_void_p
+    f = gq.lib.gptq_packed_linear
+
+    def call(n=8, ldx=256, rows=64, cols=256, bits=4, group=64, A=None, B=None, r=0, Y=p(256), ldy=64, ws=None,
+             ws_bytes=0, X=p(256)):
+        return f(X, n, ldx, p(256), p(256), p(256), rows, cols, bits, group, A, B, r, Y, ldy, ws, ws_bytes, None)
+
+    assert call(group=32) == -3          # group 32: not supported by this kernel
+    assert call(bits=8) == -3
+    assert call(rows=48) == -1           # rows % 32
+    assert call(ldx=260) == -1           # row stride of X not a multiple of 8
+    assert call(X=p(258)) == -1          # X not 16-byte aligned
+    assert call(ldy=62) == -1
+    assert call(X=None) == -1
+    assert call(r=65, A=p(256), B=p(256)) == -1
+    assert call(r=4, A=None, B=p(256)) == -1
+    assert call(r=4, A=p(256), B=p(256)) == -7     # no workspace for X A^T
+    assert call(n=0) == 0                           # nothing to do, nothing launched
+    assert gq.lib.gptq_packed_linear_workspace_size(1000, 16) >= 1000 * 16 * 4
