@@ -277,10 +277,12 @@ gq_status gptq_intrinsic_lora(const void *W, gq_dtype wt, int64_t rows, int64_t 
  *   A, B     the adapter, r x cols and rows x r float32, or both NULL with r = 0; 0 <= r <= 64.
  *   Y        n x rows float32 output, row stride ldy (ldy >= rows, ldy % 4 == 0), 16-byte aligned.
  *   n        0 <= n <= 65535 * 128 tokens; n = 0 returns GQ_OK at once (X, Y may then be NULL).
- *   ws       >= gptq_packed_linear_workspace_size(n, r) bytes (holds X A^T); may be NULL when r = 0.
- * Asynchronous.
+ *   ws       >= gptq_packed_linear_workspace_size(n, rows, cols, group, r) bytes (X A^T, and for
+ *            n <= 32 the partial sums of the decode path); may be NULL when that size is 0.
+ * Up to 32 tokens (decode) the product runs on the SIMT pipes of every SM, split over K in
+ * whole groups and reduced in a fixed order; above, on the tensor cores.  Asynchronous.
  */
-size_t gptq_packed_linear_workspace_size(int64_t n, int r);
+size_t gptq_packed_linear_workspace_size(int64_t n, int64_t rows, int64_t cols, int group, int r);
 gq_status gptq_packed_linear(const void *X, int64_t n, int64_t ldx, const int32_t *qweight, const float *scales,
                              const int32_t *qzeros, int64_t rows, int64_t cols, int bits, int group, const float *A,
                              const float *B, int r, float *Y, int64_t ldy, void *ws, size_t ws_bytes,

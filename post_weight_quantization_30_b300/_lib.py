@@ -58,7 +58,7 @@ SIGNATURES = {
     "gptq_intrinsic_lora_workspace_size": (_sz, [_i64, _i64, _i, _i]),
     "gptq_intrinsic_lora": (_i, [_p, _i, _i64, _i64, _p, _p, _i, _i, _i, _i, _f, _p, _p, _p, _p, _p, _p, _p, _p,
                                  _sz, _p, ctypes.POINTER(_i64)]),
-    "gptq_packed_linear_workspace_size": (_sz, [_i64, _i]),
+    "gptq_packed_linear_workspace_size": (_sz, [_i64, _i64, _i64, _i, _i]),
     "gptq_packed_linear": (_i, [_p, _i64, _i64, _p, _p, _p, _i64, _i64, _i, _i, _p, _p, _i, _p, _i64, _p, _sz, _p]),
     "gptq_code_decisions": (_i, [_p, _p, _i64, _p, _p]),
     "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
@@ -297,7 +297,7 @@ def gptq_packed_linear(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Ten
     n = X.shape[0]
     r = 0 if A is None else A.shape[0]
     Y = out if out is not None else torch.empty((n, rows), dtype=torch.float32, device=X.device)
-    ws_bytes = lib.gptq_packed_linear_workspace_size(n, r)
+    ws_bytes = lib.gptq_packed_linear_workspace_size(n, rows, cols, group, r)
     ws = workspace if workspace is not None else (_workspace(ws_bytes, X.device) if ws_bytes else None)
     _check(lib.gptq_packed_linear(_ptr(X), n, X.stride(0), _ptr(qweight.contiguous()), _ptr(scales.contiguous()),
                                   _ptr(qzeros.contiguous()), rows, cols, bits, group,

@@ -207,6 +207,19 @@ cudaError_t packed_linear_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx,
                                  int group, const float *A, const float *B, int r, float *T, float *Y, int64_t ldy,
                                  cudaStream_t s);
 unsigned int packed_read_and_clear_error();
+// T = X A^T (n x r float32) for the adapter term.
+cudaError_t lora_t_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, int64_t cols, const float *A, int r,
+                          float *T, cudaStream_t s);
+// Decode path for few tokens (n <= kPackedDecodeMaxTokens): SIMT product split over K
+// into `slices` partial outputs (Ypart: slices x n x rows floats) and a fixed-order reduction.
+constexpr int64_t kPackedDecodeMaxTokens = 32;
+// The decode path holds a slice of X (16 tokens x whole groups) in 64 KB of shared memory.
+inline bool packed_use_decode(int64_t n, int group) { return n <= kPackedDecodeMaxTokens && group <= 1024; }
+void packed_gemv_split(int64_t rows, int64_t cols, int group, int64_t n, int *gps, int *slices);
+cudaError_t packed_gemv_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const int32_t *qweight,
+                               const float *scales, const int32_t *qzeros, int64_t rows, int64_t cols, int bits,
+                               int group, const float *T, const float *B, int r, float *Ypart, float *Y, int64_t ldy,
+                               cudaStream_t s);
 
 // dW = W - W_hat, n elements (W float32 or bf16).
 cudaError_t weight_error_launch(const void *W, bool w_bf16, int64_t n, const float *W_hat, float *dW, cudaStream_t s);

@@ -528,15 +528,20 @@ unsigned int packed_read_and_clear_error() {
     return v;
 }
 
+cudaError_t lora_t_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, int64_t cols, const float *A, int r,
+                          float *T, cudaStream_t s) {
+    lora_t_kernel<<<(unsigned)((n + 31) / 32), 256, 0, s>>>(X, ldx, (int)n, (int)cols, A, r, T);
+    count_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t packed_linear_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const int32_t *qweight,
                                  const float *scales, const int32_t *qzeros, int64_t rows, int64_t cols, int bits,
                                  int group, const float *A, const float *B, int r, float *T, float *Y, int64_t ldy,
                                  cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
     if (r > 0) {
-        lora_t_kernel<<<(unsigned)((n + 31) / 32), 256, 0, s>>>(X, ldx, (int)n, (int)cols, A, r, T);
-        count_launch();
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = lora_t_launch(X, n, ldx, cols, A, r, T, s);
         if (e != cudaSuccess) return e;
     }
     CUtensorMap xmap, qmap;
@@ -548,6 +553,202 @@ cudaError_t packed_linear_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx,
         case 4: return launch_bits<4>(xmap, qmap, scales, qzeros, (int)n, (int)rows, (int)cols, group, T, B, r, Y, ldy, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+}  // namespace gq
+
+// ---------------------------------------------------------------------------
+// Decode path (few tokens): the product is bound by reading the packed words,
+// so it runs on the SIMT pipes across every SM.  One lane per row of W, 256
+// rows per CTA; K split across CTAs in whole groups; the CTA's slice of X
+// (NT tokens x its K range) is staged in shared memory as float32.  Per group,
+// sum_k x[m, k] (q - z) is accumulated unscaled (exact integer weights) and
+// then scaled in float32, as in the tensor-core path.  Partial sums per K slice
+// go to a workspace and packed_reduce_kernel adds them in a fixed order
+// (deterministic), with the adapter term.
+// ---------------------------------------------------------------------------
+namespace gq {
+namespace {
+
+constexpr int DV_ROWS = 256;            // rows of W per CTA (8 warps, lane = row)
+constexpr int DV_SMEM_FLOATS = 16384;   // X slice in shared memory: NT x K-range floats (64 KB)
+
+template <int BITS, int NT>
+__global__ void __launch_bounds__(DV_ROWS) packed_gemv_kernel(const __nv_bfloat16 *__restrict__ X, int64_t ldx, int n,
+                                                              const int32_t *__restrict__ qweight,
+                                                              const float *__restrict__ scales,
+                                                              const int32_t *__restrict__ qzeros, int rows, int cols,
+                                                              int group, int gps, float *__restrict__ Ypart) {
+    extern __shared__ __align__(16) float xs[];  // [kc][NT]: the NT tokens of one k are contiguous
+    const int ngroups = cols / group;
+    const int g0 = blockIdx.y * gps;
+    const int g1 = (g0 + gps) < ngroups ? (g0 + gps) : ngroups;
+    const int k0 = g0 * group, kc = (g1 - g0) * group;
+    const int m0 = blockIdx.z * NT;
+    for (int idx = threadIdx.x; idx < NT * kc; idx += DV_ROWS) {
+        const int m = idx / kc, k = idx - m * kc;  // coalesced along k
+        xs[k * NT + m] = (m0 + m < n) ? __bfloat162float(X[(int64_t)(m0 + m) * ldx + k0 + k]) : 0.f;
+    }
+    __syncthreads();
+    const int nr = blockIdx.x * DV_ROWS + threadIdx.x;
+    if (nr >= rows) return;
+    const int64_t zwords = (int64_t)rows * BITS / 32;
+    // The slice as chunks of 64 codes (2 BITS words per row, one word-row apart by
+    // `rows`); the next chunk's words and the next group's zero point and scale are
+    // loaded while the current chunk is summed.
+    const int nch = kc / 64;
+    const int cpg = group / 64;  // chunks per group
+    const int32_t *src = qweight + (int64_t)k0 * BITS / 32 * rows + nr;
+    auto load_chunk = [&](int ch, uint32_t (&w)[2 * BITS]) {
+#pragma unroll
+        for (int i = 0; i < 2 * BITS; ++i) w[i] = (uint32_t)__ldg(src + (int64_t)(ch * 2 * BITS + i) * rows);
+    };
+    auto zero_of = [&](int g) { return (float)packed_field(qzeros + (int64_t)g * zwords, 1, (int64_t)nr * BITS, BITS); };
+    float acc[NT], accg[NT];
+#pragma unroll
+    for (int m = 0; m < NT; ++m) acc[m] = accg[m] = 0.f;
+    uint32_t wcur[2 * BITS], wnxt[2 * BITS];
+    load_chunk(0, wcur);
+    float zf = zero_of(g0), sc = __ldg(scales + (int64_t)g0 * rows + nr);
+    float zn = 0.f, sn = 0.f;
+    if (g0 + 1 < g1) {
+        zn = zero_of(g0 + 1);
+        sn = __ldg(scales + (int64_t)(g0 + 1) * rows + nr);
+    }
+    for (int ch = 0; ch < nch; ++ch) {
+        if (ch + 1 < nch) load_chunk(ch + 1, wnxt);
+        if (ch > 0 && ch % cpg == 0) {  // a new group: scale and add the finished one
+            const int g = g0 + ch / cpg;
+#pragma unroll
+            for (int m = 0; m < NT; ++m) {
+                acc[m] = fmaf(sc, accg[m], acc[m]);
+                accg[m] = 0.f;
+            }
+            zf = zn;
+            sc = sn;
+            if (g + 1 < g1) {
+                zn = zero_of(g + 1);
+                sn = __ldg(scales + (int64_t)(g + 1) * rows + nr);
+            }
+        }
+        const float *xc = xs + (size_t)ch * 64 * NT;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            const int bit = j * BITS;
+            const int wi = bit >> 5, sh = bit & 31;
+            uint32_t v = wcur[wi] >> sh;
+            if (sh + BITS > 32) v |= wcur[wi + 1] << (32 - sh);
+            const float d = (float)(v & ((1u << BITS) - 1u)) - zf;
+            const float *xk = xc + j * NT;  // same address in every lane: a broadcast
+            if constexpr (NT % 4 == 0) {
+#pragma unroll
+                for (int m4 = 0; m4 < NT; m4 += 4) {
+                    const float4 x4 = *reinterpret_cast<const float4 *>(xk + m4);
+                    accg[m4] = fmaf(x4.x, d, accg[m4]);
+                    accg[m4 + 1] = fmaf(x4.y, d, accg[m4 + 1]);
+                    accg[m4 + 2] = fmaf(x4.z, d, accg[m4 + 2]);
+                    accg[m4 + 3] = fmaf(x4.w, d, accg[m4 + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < NT; ++m) accg[m] = fmaf(xk[m], d, accg[m]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2 * BITS; ++i) wcur[i] = wnxt[i];
+    }
+#pragma unroll
+    for (int m = 0; m < NT; ++m) acc[m] = fmaf(sc, accg[m], acc[m]);
+    float *yp = Ypart + (int64_t)blockIdx.y * n * rows;
+#pragma unroll
+    for (int m = 0; m < NT; ++m)
+        if (m0 + m < n) yp[(int64_t)(m0 + m) * rows + nr] = acc[m];
+}
+
+// Y[m, c] = sum over slices of Ypart[z, m, c] (fixed order) + sum_i T[m, i] B[c, i].
+__global__ void packed_reduce_kernel(const float *__restrict__ Ypart, int slices, int n, int rows,
+                                     const float *__restrict__ T, const float *__restrict__ B, int r,
+                                     float *__restrict__ Y, int64_t ldy) {
+    const int64_t total = (int64_t)n * rows;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int m = (int)(idx / rows), c = (int)(idx - (int64_t)m * rows);
+        float v = 0.f;
+        for (int z = 0; z < slices; ++z) v += Ypart[(int64_t)z * total + idx];
+        for (int i = 0; i < r; ++i) v = fmaf(T[(int64_t)m * r + i], B[(int64_t)c * r + i], v);
+        Y[(int64_t)m * ldy + c] = v;
+    }
+}
+
+template <int BITS, int NT>
+cudaError_t gemv_launch(const __nv_bfloat16 *X, int64_t ldx, int n, const int32_t *qweight, const float *scales,
+                        const int32_t *qzeros, int rows, int cols, int group, int gps, int slices, float *Ypart,
+                        cudaStream_t s) {
+    const size_t smem = (size_t)NT * gps * group * sizeof(float);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(packed_gemv_kernel<BITS, NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DV_SMEM_FLOATS * (int)sizeof(float));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid((unsigned)((rows + DV_ROWS - 1) / DV_ROWS), (unsigned)slices, (unsigned)((n + NT - 1) / NT));
+    packed_gemv_kernel<BITS, NT><<<grid, DV_ROWS, smem, s>>>(X, ldx, n, qweight, scales, qzeros, rows, cols, group,
+                                                             gps, Ypart);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <int NT>
+cudaError_t gemv_bits(int bits, const __nv_bfloat16 *X, int64_t ldx, int n, const int32_t *qweight,
+                      const float *scales, const int32_t *qzeros, int rows, int cols, int group, int gps, int slices,
+                      float *Ypart, cudaStream_t s) {
+    switch (bits) {
+        case 2: return gemv_launch<2, NT>(X, ldx, n, qweight, scales, qzeros, rows, cols, group, gps, slices, Ypart, s);
+        case 3: return gemv_launch<3, NT>(X, ldx, n, qweight, scales, qzeros, rows, cols, group, gps, slices, Ypart, s);
+        case 4: return gemv_launch<4, NT>(X, ldx, n, qweight, scales, qzeros, rows, cols, group, gps, slices, Ypart, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+// Groups per K slice of the decode path: enough slices for about two CTAs per SM,
+// each slice's X (NT = 16 tokens) within DV_SMEM_FLOATS.
+void packed_gemv_split(int64_t rows, int64_t cols, int group, int64_t n, int *gps_out, int *slices_out) {
+    const int ngroups = (int)(cols / group);
+    const int64_t rb = (rows + DV_ROWS - 1) / DV_ROWS, nt = (n + 15) / 16;
+    int64_t want = (2 * 148 + rb * nt - 1) / (rb * nt);
+    if (want < 1) want = 1;
+    int gps = (int)((ngroups + want - 1) / want);
+    const int gmax = DV_SMEM_FLOATS / (16 * group);
+    if (gps > gmax) gps = gmax;
+    if (gps < 1) gps = 1;
+    *gps_out = gps;
+    *slices_out = (ngroups + gps - 1) / gps;
+}
+
+cudaError_t packed_gemv_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const int32_t *qweight,
+                               const float *scales, const int32_t *qzeros, int64_t rows, int64_t cols, int bits,
+                               int group, const float *T, const float *B, int r, float *Ypart, float *Y, int64_t ldy,
+                               cudaStream_t s) {
+    int gps, slices;
+    packed_gemv_split(rows, cols, group, n, &gps, &slices);
+    cudaError_t e;
+    if (n <= 1)
+        e = gemv_bits<1>(bits, X, ldx, (int)n, qweight, scales, qzeros, (int)rows, (int)cols, group, gps, slices, Ypart, s);
+    else if (n <= 4)
+        e = gemv_bits<4>(bits, X, ldx, (int)n, qweight, scales, qzeros, (int)rows, (int)cols, group, gps, slices, Ypart, s);
+    else
+        e = gemv_bits<16>(bits, X, ldx, (int)n, qweight, scales, qzeros, (int)rows, (int)cols, group, gps, slices, Ypart, s);
+    if (e != cudaSuccess) return e;
+    const int64_t total = n * rows;
+    int64_t gr = (total + 255) / 256;
+    if (gr > 148 * 8) gr = 148 * 8;
+    packed_reduce_kernel<<<(unsigned)gr, 256, 0, s>>>(Ypart, slices, (int)n, (int)rows, T, B, r, Y, ldy);
+    count_launch();
+    return cudaGetLastError();
 }
 
 }  // namespace gq

@@ -134,5 +134,8 @@ def test_packed_linear_host_side_validation(gq):
     assert call(r=65, A=p(256), B=p(256)) == -1
     assert call(r=4, A=None, B=p(256)) == -1
     assert call(r=4, A=p(256), B=p(256)) == -7     # no workspace for X A^T
+    assert call(n=8) == -7                          # decode path: no workspace for the partial sums
     assert call(n=0) == 0                           # nothing to do, nothing launched
-    assert gq.lib.gptq_packed_linear_workspace_size(1000, 16) >= 1000 * 16 * 4
+    assert gq.lib.gptq_packed_linear_workspace_size(1000, 64, 256, 64, 16) >= 1000 * 16 * 4
+    assert gq.lib.gptq_packed_linear_workspace_size(1000, 64, 256, 64, 0) == 0     # prefill, no adapter
+    assert gq.lib.gptq_packed_linear_workspace_size(16, 64, 256, 64, 0) >= 16 * 64 * 4

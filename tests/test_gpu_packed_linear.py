@@ -5,8 +5,10 @@ kernel forms exact bf16 x integer products, sums one group's K range on the
 tensor cores and scales it in float32, so Y differs from the exact value only by
 float32 summation.  The bar is the classic bound for a sum of products,
 |fl(sum) - sum| <= gamma * sum |x_k w_k|, for the order used: at most
-group / 16 + cols / group + r + 2 float32 additions on the path of a product of
-X Ŵ^T (tensor-core partial sums of 16 products taken as rounded once per step),
+group / 16 + 2 cols / group + r + 2 float32 additions on the path of a product
+of X Ŵ^T on the tensor cores (partial sums of 16 products taken as rounded once
+per step; group + 2 cols / group + r + 2 on the decode path, n <= 32, which sums
+a group's products one by one and adds its K slices at the end),
 and cols + r + 2 on the path of the adapter term (T = X A^T is summed over cols
 in float32), with gamma = steps * 2^-23 (round-to-nearest or truncation),
 applied to |X| |Ŵ|^T and |X| |A|^T |B|^T respectively.
@@ -70,7 +72,10 @@ def _check(Yg, x64, packed, rows, cols, bits, group, A=None, B=None):
     B64 = None if B is None else B.astype(np.float32).astype(np.float64)
     ref = pl.packed_linear(x64, qw, s, qz, bits, group, rows, cols, A64, B64)
     W_hat = pl.dequantize(qw, s, qz, bits, group, rows, cols)
-    bound = (group // 16 + cols // group + r + 2) * 2.0 ** -23 * (np.abs(x64) @ np.abs(W_hat).T)
+    # the decode path (n <= 32) sums a group's products one by one and its K slices in a final pass
+    decode = x64.shape[0] <= 32
+    steps = (group if decode else group // 16) + 2 * (cols // group) + r + 2
+    bound = steps * 2.0 ** -23 * (np.abs(x64) @ np.abs(W_hat).T)
     if r:
         # T = X A^T is a float32 sum of cols products, then r more additions into Y
         bound = bound + (cols + r + 2) * 2.0 ** -23 * ((np.abs(x64) @ np.abs(A64).T) @ np.abs(B64).T)
@@ -88,6 +93,12 @@ CASES = [
     (1, 64, 256, 4, 64, 8),        # a single token (decode)
     (1000, 384, 1024, 2, 128, 5),  # r = 5
     (129, 160, 192, 3, 192, 0),    # one group spanning three k-tiles
+    # decode path (n <= 32): SIMT, split over K, fixed-order reduction
+    (16, 256, 1024, 3, 128, 8),
+    (32, 96, 640, 2, 64, 0),
+    (4, 384, 512, 4, 128, 64),
+    (5, 64, 256, 3, 64, 3),
+    (33, 128, 256, 4, 64, 4),      # the smallest tensor-core case
 ]
 
 
