@@ -68,6 +68,7 @@ class LayerSpec:
     damp: float = 0.01
     eora_rank: int = 0
     lora_rank: int = 0  # GPTQ-intrinsic LoRA rank (0: plain GPTQ)
+    packed_tokens: int = 0  # > 0: the workload is the packed layer applied to this many tokens (X is n x cols)
     notes: str = field(default="", compare=False)
 
     @property
@@ -111,6 +112,21 @@ LAYERS: dict[str, LayerSpec] = {
         LayerSpec("qwen72b_29568x8192", W=_w(29568, 8192, 0.015, (3, 1)), X=_X_QWEN72B_8192, bits=2, group=64),
         LayerSpec("qwen32b_5120x5120", W=_w(5120, 5120, 0.02, (4, 0)), X=_X_QWEN32B_5120, bits=2, group=64, eora_rank=64),
         LayerSpec("qwen32b_25600x5120", W=_w(25600, 5120, 0.02, (4, 1)), X=_X_QWEN32B_5120, bits=2, group=64, eora_rank=64),
+        # The quantized layer applied from its packed form (inference): prefill and decode
+        # token counts; the EoRA-shaped layer with its rank-64 adapter.  X here holds the
+        # tokens the layer is applied to.
+        LayerSpec("llama7b_q_proj_packed_prefill_n4096", W=_w(4096, 4096, 0.02, (1, 0)),
+                  X=TensorSpec(4096, 4096, "t", nu=4.0, n_outliers=41, outlier_scale=30.0, key=(5, 1)), bits=4,
+                  group=128, packed_tokens=4096),
+        LayerSpec("llama7b_q_proj_packed_decode_n1", W=_w(4096, 4096, 0.02, (1, 0)),
+                  X=TensorSpec(1, 4096, "t", nu=4.0, n_outliers=41, outlier_scale=30.0, key=(5, 2)), bits=4,
+                  group=128, packed_tokens=1),
+        LayerSpec("llama7b_q_proj_packed_decode_n16", W=_w(4096, 4096, 0.02, (1, 0)),
+                  X=TensorSpec(16, 4096, "t", nu=4.0, n_outliers=41, outlier_scale=30.0, key=(5, 3)), bits=4,
+                  group=128, packed_tokens=16),
+        LayerSpec("qwen32b_5120x5120_packed_eora_r64_n4096", W=_w(5120, 5120, 0.02, (4, 0)),
+                  X=TensorSpec(4096, 5120, "normal", n_outliers=51, outlier_scale=30.0, key=(5, 4)), bits=2,
+                  group=64, eora_rank=64, packed_tokens=4096),
         # The same two layers with a rank-64 GPTQ-intrinsic LoRA in place of EoRA.
         LayerSpec("qwen32b_5120x5120_intrinsic_r64", W=_w(5120, 5120, 0.02, (4, 0)), X=_X_QWEN32B_5120, bits=2,
                   group=64, lora_rank=64),
