@@ -401,16 +401,9 @@ gq_status gptq_intrinsic_lora(const void *W, gq_dtype wt, int64_t rows, int64_t 
                           W_hat, row_err, R, ws, cs(stream), info);
 }
 
-// Packed-linear workspace: [T = X A^T: n x r floats][decode partials: slices x n x rows floats].
 size_t gptq_packed_linear_workspace_size(int64_t n, int64_t rows, int64_t cols, int group, int r) {
-    if (n <= 0 || rows <= 0 || cols <= 0 || group <= 0 || cols % group || r < 0) return 0;
-    size_t b = r > 0 ? align_up((size_t)n * r * sizeof(float)) : 0;
-    if (packed_use_decode(n, group)) {
-        int gps, slices;
-        packed_gemv_split(rows, cols, group, n, &gps, &slices);
-        b += align_up((size_t)slices * n * rows * sizeof(float));
-    }
-    return b;
+    if (n <= 0 || rows <= 0 || cols <= 0 || group <= 0 || cols % group || r < 0 || r > 64) return 0;
+    return packed_ws_bytes(n, rows, cols, group, r);
 }
 
 gq_status gptq_packed_linear(const void *X, int64_t n, int64_t ldx, const int32_t *qweight, const float *scales,
@@ -429,19 +422,8 @@ gq_status gptq_packed_linear(const void *X, int64_t n, int64_t ldx, const int32_
     if (r > 0 && (!A || !B || !aligned(A, 4) || !aligned(B, 4))) return GQ_EINVAL;
     const size_t need = gptq_packed_linear_workspace_size(n, rows, cols, group, r);
     if (need > 0 && (!ws || !aligned(ws, kAlign) || ws_bytes < need)) return GQ_EWORKSPACE;
-    float *T = r > 0 ? (float *)ws : nullptr;
-    cudaError_t e;
-    if (packed_use_decode(n, group)) {
-        float *Ypart = (float *)((char *)ws + (r > 0 ? align_up((size_t)n * r * sizeof(float)) : 0));
-        e = cudaSuccess;
-        if (r > 0) e = lora_t_launch((const __nv_bfloat16 *)X, n, ldx, cols, A, r, T, cs(stream));
-        if (e == cudaSuccess)
-            e = packed_gemv_launch((const __nv_bfloat16 *)X, n, ldx, qweight, scales, qzeros, rows, cols, bits,
-                                   group, T, r > 0 ? B : nullptr, r, Ypart, Y, ldy, cs(stream));
-    } else {
-        e = packed_linear_launch((const __nv_bfloat16 *)X, n, ldx, qweight, scales, qzeros, rows, cols, bits, group,
-                                 r > 0 ? A : nullptr, r > 0 ? B : nullptr, r, T, Y, ldy, cs(stream));
-    }
+    const cudaError_t e = packed_forward((const __nv_bfloat16 *)X, n, ldx, qweight, scales, qzeros, rows, cols, bits,
+                                         group, r > 0 ? A : nullptr, r > 0 ? B : nullptr, r, Y, ldy, ws, cs(stream));
     return e == cudaSuccess ? GQ_OK : GQ_ECUDA;
 }
 

@@ -200,16 +200,14 @@ cudaError_t schur_init_launch(const float *H, int64_t cols, const DeviceStatus *
 cudaError_t dw_split_launch(const void *W, bool w_bf16, const float *W_hat, const uint8_t *dead, int64_t rows,
                             int64_t cols, float *hi, float *lo, cudaStream_t s);
 
-// Packed quantized linear layer (packed_linear.cu): Y = X Ŵ^T (+ (X A^T) B^T when r > 0,
-// with T = X A^T written to T, n x r).  Requirements checked by the caller (gq.h).
-cudaError_t packed_linear_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const int32_t *qweight,
-                                 const float *scales, const int32_t *qzeros, int64_t rows, int64_t cols, int bits,
-                                 int group, const float *A, const float *B, int r, float *T, float *Y, int64_t ldy,
-                                 cudaStream_t s);
+// Packed quantized linear layer (packed_linear.cu): Y = X Ŵ^T (+ (X A^T) B^T when r > 0).
+// Requirements checked by the caller (gq.h); ws holds packed_ws_bytes(...) bytes.
+size_t packed_ws_bytes(int64_t n, int64_t rows, int64_t cols, int group, int r);
+cudaError_t packed_forward(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const int32_t *qweight,
+                           const float *scales, const int32_t *qzeros, int64_t rows, int64_t cols, int bits,
+                           int group, const float *A, const float *B, int r, float *Y, int64_t ldy, void *ws,
+                           cudaStream_t s);
 unsigned int packed_read_and_clear_error();
-// T = X A^T (n x r float32) for the adapter term.
-cudaError_t lora_t_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, int64_t cols, const float *A, int r,
-                          float *T, cudaStream_t s);
 // Decode path for few tokens (n <= kPackedDecodeMaxTokens): SIMT product split over K
 // into `slices` partial outputs (Ypart: slices x n x rows floats) and a fixed-order reduction.
 constexpr int64_t kPackedDecodeMaxTokens = 32;

@@ -26,9 +26,11 @@
 //   k-tiles into one of two TMEM accumulators;
 // * warps 6-13: per group, read the accumulator (TMEM lane quarter = warp % 4,
 //   one half of the 128 columns per warp), scale by the group's per-row scales
-//   and add into registers; at the end add the adapter term T B^T (T = X A^T
-//   from lora_t_kernel, B staged in shared memory) in float32 and store Y
-//   through shared memory, coalesced.
+//   and add into registers; store Y through shared memory, coalesced.
+// * The adapter term T B^T (T = X A^T from lora_t2_kernel) is one more group
+//   with scale 1: T and B as bf16 hi / lo pairs (x = hi + lo + O(2^-16 x)),
+//   three pseudo k-tiles T_hi B_hi, T_hi B_lo, T_lo B_hi loaded by TMA into the
+//   stage slots of X and W (K = r <= 64, zero-padded to 64).
 // Every mbarrier wait is bounded; on expiry the CTA records the error flag that
 // gq_check_device reports and exits without writing Y.
 #include "tc_common.cuh"
@@ -54,7 +56,8 @@ constexpr int P_EPI = 8;                         // epilogue warps: 4 lane quart
 constexpr int P_HALF = PN / 2;                   // columns per epilogue thread
 constexpr int P_STAGE_LD = PN + 4;               // epilogue staging row stride (floats)
 constexpr int ADAPTER_MAX_R = 64;
-static_assert(4 * 32 * P_STAGE_LD * 4 + PN * ADAPTER_MAX_R * 4 <= P_STAGES * P_STAGE, "epilogue smem");
+constexpr int ADAPTER_TILES = 3;                 // T_hi B_hi, T_hi B_lo, T_lo B_hi
+static_assert(4 * 32 * P_STAGE_LD * 4 <= P_STAGES * P_STAGE, "epilogue smem");
 
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, N >> 3
 // at bit 17, M >> 4 at bit 24.
@@ -160,14 +163,17 @@ __device__ __forceinline__ void dequant_row(const uint32_t (&w)[PK * BITS / 32],
 template <int BITS>
 __global__ void __launch_bounds__(P_NWARPS * 32, 1)
     packed_linear_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
+                         const __grid_constant__ CUtensorMap thi, const __grid_constant__ CUtensorMap tlo,
+                         const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo,
                          const float *__restrict__ scales, const int32_t *__restrict__ qzeros, int n, int rows,
-                         int cols, int group, const float *__restrict__ T, const float *__restrict__ Bad, int r,
-                         float *__restrict__ Y, int64_t ldy) {
+                         int cols, int group, int adapter, float *__restrict__ Y, int64_t ldy) {
     constexpr int NW = PK * BITS / 32;  // packed words per row per stage
     const int m0 = blockIdx.y * PM, n0 = blockIdx.x * PN;
     const int ktiles = cols / PK;
     const int ktg = group / PK;  // k-tiles per group
     const int ngroups = cols / group;
+    const int kt_all = ktiles + (adapter ? ADAPTER_TILES : 0);  // with the adapter's pseudo k-tiles
+    const int groups_all = ngroups + (adapter ? 1 : 0);
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[P_STAGES];   // X and packed words landed (TMA)
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int kt = 0; kt < ktiles; ++kt) {
+            for (int kt = 0; kt < kt_all; ++kt) {
                 const int s = kt % P_STAGES;
                 const uint32_t ph = (uint32_t)(kt / P_STAGES) & 1u;
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u) || *(volatile int *)&abort_flag) {
@@ -222,16 +228,24 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
                     abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(&full_bar[s], TILE_X + NW * PN * 4);
-                tma_load_2d(smem + s * P_STAGE, &xmap, kt * PK, m0, &full_bar[s]);
-                tma_load_2d(smem + s * P_STAGE + TILE_X + TILE_W, &qmap, n0, kt * NW, &full_bar[s]);
+                if (kt < ktiles) {
+                    mbar_arrive_expect_tx(&full_bar[s], TILE_X + NW * PN * 4);
+                    tma_load_2d(smem + s * P_STAGE, &xmap, kt * PK, m0, &full_bar[s]);
+                    tma_load_2d(smem + s * P_STAGE + TILE_X + TILE_W, &qmap, n0, kt * NW, &full_bar[s]);
+                } else {
+                    // adapter pseudo k-tile a: (T_hi, B_hi), (T_hi, B_lo), (T_lo, B_hi)
+                    const int a = kt - ktiles;
+                    mbar_arrive_expect_tx(&full_bar[s], TILE_X + TILE_W);
+                    tma_load_2d(smem + s * P_STAGE, a == 2 ? &tlo : &thi, 0, m0, &full_bar[s]);
+                    tma_load_2d(smem + s * P_STAGE + TILE_X, a == 1 ? &blo : &bhi, 0, n0, &full_bar[s]);
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_kmajor(PM, PN);
-            for (int gi = 0; gi < ngroups && ok; ++gi) {
+            for (int gi = 0; gi < groups_all && ok; ++gi) {
                 const int b = gi & 1;
                 const uint32_t u = (uint32_t)(gi >> 1) & 1u;
                 if (!mbar_wait(&tempty[b], u ^ 1u)) {
@@ -240,7 +254,8 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
                 }
                 fence_after();
                 const uint32_t acc = tmem + (uint32_t)(b * P_TMEM);
-                for (int kt = gi * ktg; kt < (gi + 1) * ktg; ++kt) {
+                const int kb = gi * ktg, ke = gi < ngroups ? (gi + 1) * ktg : kt_all;
+                for (int kt = kb; kt < ke; ++kt) {
                     const int s = kt % P_STAGES;
                     const uint32_t ph = (uint32_t)(kt / P_STAGES) & 1u;
                     // full: the X tile landed (TMA); ready: the W tile is written.
@@ -257,7 +272,7 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
                         // k-step of 16 bf16 values advances the start by 32 bytes.
                         const uint64_t da = smem_desc(xa + kk * 32, 16, 1024);
                         const uint64_t dw = smem_desc(wa + kk * 32, 16, 1024);
-                        mma_bf16(acc, da, dw, idesc, (kt == gi * ktg && kk == 0) ? 0u : 1u);
+                        mma_bf16(acc, da, dw, idesc, (kt == kb && kk == 0) ? 0u : 1u);
                     }
                     mma_commit(&empty_bar[s]);
                 }
@@ -288,9 +303,19 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
             const __nv_bfloat162 z2 = __floats2bfloat162_rn(128.f + zf, 128.f + zf);
             zz = *reinterpret_cast<const uint32_t *>(&z2);
         }
-        for (int kt = 0; kt < ktiles; ++kt) {
+        for (int kt = 0; kt < kt_all; ++kt) {
             const int s = kt % P_STAGES;
             const uint32_t ph = (uint32_t)(kt / P_STAGES) & 1u;
+            if (kt >= ktiles) {
+                // adapter pseudo k-tile: both operands came by TMA; pass the stage on
+                if (!mbar_wait(&full_bar[s], ph) || *(volatile int *)&abort_flag) {
+                    ok = false;
+                    break;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ready_bar[s]);
+                continue;
+            }
             if (kt > 0 && kt % ktg == 0) {  // a new group starts
                 const int g = kt / ktg;
                 zf = znext;
@@ -334,10 +359,12 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
         const int et = threadIdx.x - 192;  // 0..255 over the eight epilogue warps
         if (et < PN) sc_ring[0][et] = (n0 + et < rows) ? __ldg(scales + n0 + et) : 0.f;
         asm volatile("bar.sync 1, %0;" ::"n"(P_EPI * 32) : "memory");
-        for (int gi = 0; gi < ngroups; ++gi) {
-            // Next group's scale for one row, in flight while this group drains.
+        for (int gi = 0; gi < groups_all; ++gi) {
+            // Next group's scale for one row, in flight while this group drains (the
+            // adapter's group, last, has scale 1).
             float nxt = 0.f;
-            if (et < PN && gi + 1 < ngroups && n0 + et < rows) nxt = __ldg(scales + (int64_t)(gi + 1) * rows + n0 + et);
+            if (et < PN && gi + 1 < groups_all && n0 + et < rows)
+                nxt = (gi + 1 < ngroups) ? __ldg(scales + (int64_t)(gi + 1) * rows + n0 + et) : 1.f;
             const int b = gi & 1;
             const uint32_t u = (uint32_t)(gi >> 1) & 1u;
             if (!mbar_wait(&tfull[b], u)) {
@@ -376,42 +403,8 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
             abort_flag = 1;
         }
         // The pipeline stages are idle now (every stage was consumed before the
-        // last group's accumulator completed): staging rows, then the adapter's B.
+        // last group's accumulator completed): staging rows for the coalesced store.
         float *stage = reinterpret_cast<float *>(smem) + (size_t)q * 32 * P_STAGE_LD;
-        float *Bs = reinterpret_cast<float *>(smem) + (size_t)4 * 32 * P_STAGE_LD;
-        const int m = m0 + q * 32 + lane;  // this thread's token row
-        if (r > 0) {
-            // Bs[i][c] = B[n0 + c][i] (i-major: a thread's 64 columns are contiguous).
-            // The tile's rows of B are one contiguous block: read it in order.
-            const int nvalid = (rows - n0) < PN ? (rows - n0) : PN;
-            for (int idx = et; idx < PN * r; idx += P_EPI * 32) {
-                const int c = idx / r, i = idx - c * r;
-                Bs[i * PN + c] = (c < nvalid) ? __ldg(Bad + (int64_t)n0 * r + idx) : 0.f;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(P_EPI * 32) : "memory");
-            if (ok && m < n) {
-                const float *tm = T + (int64_t)m * r;
-                for (int i0 = 0; i0 < r; i0 += 16) {
-                    // sixteen independent loads in flight, then their products
-                    float tv[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) tv[j] = (i0 + j < r) ? __ldg(tm + i0 + j) : 0.f;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        if (i0 + j >= r) break;
-                        const float *bi = Bs + (size_t)(i0 + j) * PN + cb;
-#pragma unroll
-                        for (int c = 0; c < P_HALF; c += 4) {
-                            const float4 b4 = *reinterpret_cast<const float4 *>(bi + c);
-                            acc[c] = fmaf(tv[j], b4.x, acc[c]);
-                            acc[c + 1] = fmaf(tv[j], b4.y, acc[c + 1]);
-                            acc[c + 2] = fmaf(tv[j], b4.z, acc[c + 2]);
-                            acc[c + 3] = fmaf(tv[j], b4.w, acc[c + 3]);
-                        }
-                    }
-                }
-            }
-        }
 #pragma unroll
         for (int j = 0; j < P_HALF; j += 4)
             *reinterpret_cast<float4 *>(stage + lane * P_STAGE_LD + cb + j) =
@@ -436,42 +429,116 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
     }
 }
 
-// T = X A^T (n x r) in float32: X bf16 (n x cols), A float32 (r x cols), r <= 64.
-// One CTA per 32 tokens; K in chunks of 64 staged in shared memory; thread t
-// owns token t / 8 and the adapter rows t % 8 + 8 j.
-__global__ void __launch_bounds__(256) lora_t_kernel(const __nv_bfloat16 *__restrict__ X, int64_t ldx, int n,
-                                                     int cols, const float *__restrict__ A, int r,
-                                                     float *__restrict__ T) {
-    __shared__ float Xs[32][PK + 1];
-    __shared__ float As[ADAPTER_MAX_R][PK + 1];
-    const int m0 = blockIdx.x * 32;
-    const int t = threadIdx.x, tm = t >> 3, ig = t & 7;
-    float acc[8];
+// Partial sums of T = X A^T over K slices, Tpart[z] (n x r float32), X bf16
+// (n x cols), A float32 (r x cols), r <= 64.  SIMT, register-tiled: a CTA owns
+// 64 tokens x 64 adapter rows of one K slice; thread t computes tokens
+// 4 (t / 8) .. + 3 and adapter rows 8 (t % 8) .. + 7 from float4 reads of the
+// staged tiles (K-major in shared memory).
+constexpr int LT_TOK = 64, LT_K = 32, LT_LD = 68;
+
+__global__ void __launch_bounds__(128) lora_t2_kernel(const __nv_bfloat16 *__restrict__ X, int64_t ldx, int n,
+                                                      int cols, const float *__restrict__ A, int r, int kslice,
+                                                      float *__restrict__ Tpart) {
+    __shared__ __align__(16) float Xs[LT_K][LT_LD];
+    __shared__ __align__(16) float As[LT_K][LT_LD];
+    const int t = threadIdx.x, tx = t & 7, ty = t >> 3;
+    const int m0 = blockIdx.x * LT_TOK;
+    const int kz0 = blockIdx.y * kslice;
+    const int kz1 = (kz0 + kslice) < cols ? (kz0 + kslice) : cols;
+    float acc[4][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-    for (int k0 = 0; k0 < cols; k0 += PK) {
-        for (int idx = t; idx < 32 * PK; idx += 256) {
-            const int row = idx / PK, col = idx % PK;
-            Xs[row][col] = (m0 + row < n) ? __bfloat162float(X[(int64_t)(m0 + row) * ldx + k0 + col]) : 0.f;
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int k0 = kz0; k0 < kz1; k0 += LT_K) {
+        for (int idx = t; idx < LT_TOK * LT_K; idx += 128) {
+            const int tok = idx / LT_K, kk = idx % LT_K, k = k0 + kk;
+            Xs[kk][tok] = (m0 + tok < n && k < kz1) ? __bfloat162float(X[(int64_t)(m0 + tok) * ldx + k]) : 0.f;
         }
-        for (int idx = t; idx < ADAPTER_MAX_R * PK; idx += 256) {
-            const int i = idx / PK, col = idx % PK;
-            As[i][col] = (i < r) ? A[(int64_t)i * cols + k0 + col] : 0.f;
+        for (int idx = t; idx < ADAPTER_MAX_R * LT_K; idx += 128) {
+            const int i = idx / LT_K, kk = idx % LT_K, k = k0 + kk;
+            As[kk][i] = (i < r && k < kz1) ? A[(int64_t)i * cols + k] : 0.f;
         }
         __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < PK; ++kk) {
-            const float x = Xs[tm][kk];
+#pragma unroll 4
+        for (int kk = 0; kk < LT_K; ++kk) {
+            const float4 x4 = *reinterpret_cast<const float4 *>(&Xs[kk][ty * 4]);
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[kk][tx * 8]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[kk][tx * 8 + 4]);
+            const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = fmaf(x, As[ig + 8 * j][kk], acc[j]);
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv[i], av[j], acc[i][j]);
         }
         __syncthreads();
     }
-    const int m = m0 + tm;
-    if (m < n)
+    float *out = Tpart + (int64_t)blockIdx.y * n * r;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (ig + 8 * j < r) T[(int64_t)m * r + ig + 8 * j] = acc[j];
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + ty * 4 + i;
+        if (m < n)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (tx * 8 + j < r) out[(int64_t)m * r + tx * 8 + j] = acc[i][j];
+    }
+}
+
+// rowsxr float32 sum over `slices` stacked copies (fixed order) -> T (may be NULL),
+// and its bf16 split hi + lo (lo = bf16(v - hi); NULL to skip) with row stride 64,
+// columns r..63 zero.
+__global__ void sum_split_kernel(const float *__restrict__ parts, int slices, int nrow, int r, float *__restrict__ T,
+                                 __nv_bfloat16 *__restrict__ hi, __nv_bfloat16 *__restrict__ lo) {
+    const int64_t total = (int64_t)nrow * ADAPTER_MAX_R;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int m = (int)(idx / ADAPTER_MAX_R), c = (int)(idx % ADAPTER_MAX_R);
+        float v = 0.f;
+        if (c < r) {
+            for (int z = 0; z < slices; ++z) v += parts[(int64_t)z * nrow * r + (int64_t)m * r + c];
+            if (T) T[(int64_t)m * r + c] = v;
+        }
+        if (hi) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(v);
+            hi[idx] = h;
+            lo[idx] = __float2bfloat16_rn(v - __bfloat162float(h));
+        }
+    }
+}
+
+// A bf16 operand of r <= 64 columns stored with row stride 64 (K-major, one
+// 128-byte swizzle row per matrix row): dims {64, nrow}, box {64, 128}.
+bool make_r_map(CUtensorMap *map, const __nv_bfloat16 *p, int64_t nrow) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)ADAPTER_MAX_R, (cuuint64_t)nrow};
+    cuuint64_t gstride[1] = {(cuuint64_t)ADAPTER_MAX_R * 2};
+    cuuint32_t box[2] = {(cuuint32_t)PK, (cuuint32_t)PM};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)p, gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+unsigned grid_cap(int64_t total) {
+    int64_t g = (total + 255) / 256;
+    if (g < 1) g = 1;
+    if (g > 148 * 8) g = 148 * 8;
+    return (unsigned)g;
+}
+
+// K slices of lora_t2_kernel: about two CTAs per SM, slices a multiple of LT_K wide.
+void lora_t_split(int64_t n, int64_t cols, int *kslice, int *slices) {
+    const int64_t tiles = (n + LT_TOK - 1) / LT_TOK;
+    int64_t z = (2 * 148 + tiles - 1) / tiles;
+    if (z < 1) z = 1;
+    if (z > cols / LT_K) z = cols / LT_K;
+    if (z < 1) z = 1;
+    int64_t ks = (cols + z - 1) / z;
+    ks = (ks + LT_K - 1) / LT_K * LT_K;
+    *kslice = (int)ks;
+    *slices = (int)((cols + ks - 1) / ks);
 }
 
 bool make_x_map(CUtensorMap *map, const __nv_bfloat16 *X, int64_t n, int64_t cols, int64_t ldx) {
@@ -501,8 +568,9 @@ bool make_q_map(CUtensorMap *map, const int32_t *qweight, int64_t rows, int64_t 
 }
 
 template <int BITS>
-cudaError_t launch_bits(const CUtensorMap &xmap, const CUtensorMap &qmap, const float *scales, const int32_t *qzeros,
-                        int n, int rows, int cols, int group, const float *T, const float *B, int r, float *Y,
+cudaError_t launch_bits(const CUtensorMap &xmap, const CUtensorMap &qmap, const CUtensorMap &thi,
+                        const CUtensorMap &tlo, const CUtensorMap &bhi, const CUtensorMap &blo, const float *scales,
+                        const int32_t *qzeros, int n, int rows, int cols, int group, int adapter, float *Y,
                         int64_t ldy, cudaStream_t s) {
     static bool attr_set = false;
     if (!attr_set) {
@@ -512,10 +580,49 @@ cudaError_t launch_bits(const CUtensorMap &xmap, const CUtensorMap &qmap, const 
         attr_set = true;
     }
     dim3 grid((unsigned)((rows + PN - 1) / PN), (unsigned)((n + PM - 1) / PM));
-    packed_linear_kernel<BITS><<<grid, P_NWARPS * 32, P_SMEM, s>>>(xmap, qmap, scales, qzeros, n, rows, cols,
-                                                                   group, T, B, r, Y, ldy);
+    packed_linear_kernel<BITS><<<grid, P_NWARPS * 32, P_SMEM, s>>>(xmap, qmap, thi, tlo, bhi, blo, scales, qzeros, n,
+                                                                   rows, cols, group, adapter, Y, ldy);
     count_launch();
     return cudaGetLastError();
+}
+
+// Workspace of packed_forward (256-byte aligned regions):
+//   [Tpart: slices x n x r][T: n x r]                       when r > 0
+//   [T_hi, T_lo: n x 64 bf16][B_hi, B_lo: rows x 64 bf16]   when r > 0 and the tensor-core path
+//   [decode partials: slices x n x rows]                    on the decode path
+struct PackedWs {
+    float *Tpart, *T, *Ypart;
+    __nv_bfloat16 *Thi, *Tlo, *Bhi, *Blo;
+};
+
+size_t packed_layout(int64_t n, int64_t rows, int64_t cols, int group, int r, PackedWs *w, char *base) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *p = base ? base + off : nullptr;
+        off += align_up(bytes);
+        return p;
+    };
+    PackedWs t = {};
+    const bool decode = packed_use_decode(n, group);
+    if (r > 0) {
+        int ks, z;
+        lora_t_split(n, cols, &ks, &z);
+        t.Tpart = (float *)take((size_t)z * n * r * sizeof(float));
+        t.T = (float *)take((size_t)n * r * sizeof(float));
+        if (!decode) {
+            t.Thi = (__nv_bfloat16 *)take((size_t)n * ADAPTER_MAX_R * 2);
+            t.Tlo = (__nv_bfloat16 *)take((size_t)n * ADAPTER_MAX_R * 2);
+            t.Bhi = (__nv_bfloat16 *)take((size_t)rows * ADAPTER_MAX_R * 2);
+            t.Blo = (__nv_bfloat16 *)take((size_t)rows * ADAPTER_MAX_R * 2);
+        }
+    }
+    if (decode) {
+        int gps, slices;
+        packed_gemv_split(rows, cols, group, n, &gps, &slices);
+        t.Ypart = (float *)take((size_t)slices * n * rows * sizeof(float));
+    }
+    if (w) *w = t;
+    return off;
 }
 
 }  // namespace
@@ -528,29 +635,54 @@ unsigned int packed_read_and_clear_error() {
     return v;
 }
 
-cudaError_t lora_t_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, int64_t cols, const float *A, int r,
-                          float *T, cudaStream_t s) {
-    lora_t_kernel<<<(unsigned)((n + 31) / 32), 256, 0, s>>>(X, ldx, (int)n, (int)cols, A, r, T);
-    count_launch();
-    return cudaGetLastError();
+size_t packed_ws_bytes(int64_t n, int64_t rows, int64_t cols, int group, int r) {
+    return packed_layout(n, rows, cols, group, r, nullptr, nullptr);
 }
 
-cudaError_t packed_linear_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const int32_t *qweight,
-                                 const float *scales, const int32_t *qzeros, int64_t rows, int64_t cols, int bits,
-                                 int group, const float *A, const float *B, int r, float *T, float *Y, int64_t ldy,
-                                 cudaStream_t s) {
+cudaError_t packed_forward(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const int32_t *qweight,
+                           const float *scales, const int32_t *qzeros, int64_t rows, int64_t cols, int bits,
+                           int group, const float *A, const float *B, int r, float *Y, int64_t ldy, void *ws,
+                           cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
+    PackedWs w;
+    packed_layout(n, rows, cols, group, r, &w, (char *)ws);
+    const bool decode = packed_use_decode(n, group);
+    cudaError_t e;
     if (r > 0) {
-        cudaError_t e = lora_t_launch(X, n, ldx, cols, A, r, T, s);
-        if (e != cudaSuccess) return e;
+        int ks, z;
+        lora_t_split(n, cols, &ks, &z);
+        dim3 g((unsigned)((n + LT_TOK - 1) / LT_TOK), (unsigned)z);
+        lora_t2_kernel<<<g, 128, 0, s>>>(X, ldx, (int)n, (int)cols, A, r, ks, w.Tpart);
+        count_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        sum_split_kernel<<<grid_cap(n * ADAPTER_MAX_R), 256, 0, s>>>(w.Tpart, z, (int)n, r, w.T, w.Thi, w.Tlo);
+        count_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (!decode) {
+            sum_split_kernel<<<grid_cap(rows * ADAPTER_MAX_R), 256, 0, s>>>(B, 1, (int)rows, r, nullptr, w.Bhi,
+                                                                            w.Blo);
+            count_launch();
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
     }
-    CUtensorMap xmap, qmap;
+    if (decode)
+        return packed_gemv_launch(X, n, ldx, qweight, scales, qzeros, rows, cols, bits, group, w.T, B, r, w.Ypart, Y,
+                                  ldy, s);
+    CUtensorMap xmap, qmap, thi, tlo, bhi, blo;
     if (!make_x_map(&xmap, X, n, cols, ldx) || !make_q_map(&qmap, qweight, rows, cols, bits))
         return cudaErrorInvalidValue;
+    if (r > 0) {
+        if (!make_r_map(&thi, w.Thi, n) || !make_r_map(&tlo, w.Tlo, n) || !make_r_map(&bhi, w.Bhi, rows) ||
+            !make_r_map(&blo, w.Blo, rows))
+            return cudaErrorInvalidValue;
+    } else {
+        thi = tlo = bhi = blo = xmap;  // never read without the adapter
+    }
+    const int ad = r > 0 ? 1 : 0;
     switch (bits) {
-        case 2: return launch_bits<2>(xmap, qmap, scales, qzeros, (int)n, (int)rows, (int)cols, group, T, B, r, Y, ldy, s);
-        case 3: return launch_bits<3>(xmap, qmap, scales, qzeros, (int)n, (int)rows, (int)cols, group, T, B, r, Y, ldy, s);
-        case 4: return launch_bits<4>(xmap, qmap, scales, qzeros, (int)n, (int)rows, (int)cols, group, T, B, r, Y, ldy, s);
+        case 2: return launch_bits<2>(xmap, qmap, thi, tlo, bhi, blo, scales, qzeros, (int)n, (int)rows, (int)cols, group, ad, Y, ldy, s);
+        case 3: return launch_bits<3>(xmap, qmap, thi, tlo, bhi, blo, scales, qzeros, (int)n, (int)rows, (int)cols, group, ad, Y, ldy, s);
+        case 4: return launch_bits<4>(xmap, qmap, thi, tlo, bhi, blo, scales, qzeros, (int)n, (int)rows, (int)cols, group, ad, Y, ldy, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -11,7 +11,8 @@ per step; group + 2 cols / group + r + 2 on the decode path, n <= 32, which sums
 a group's products one by one and adds its K slices at the end),
 and cols + r + 2 on the path of the adapter term (T = X A^T is summed over cols
 in float32), with gamma = steps * 2^-23 (round-to-nearest or truncation),
-applied to |X| |Ŵ|^T and |X| |A|^T |B|^T respectively.
+applied to |X| |Ŵ|^T and |X| |A|^T |B|^T respectively; the adapter term adds
+2^-15 for the bf16 hi / lo split of T and B on the tensor-core path.
 
 Inputs are seeded: codes, zeros and scales drawn at random and packed, or a
 layer quantized by the GPTQ oracle; the loss of the packed layer measured from
@@ -77,8 +78,10 @@ def _check(Yg, x64, packed, rows, cols, bits, group, A=None, B=None):
     steps = (group if decode else group // 16) + 2 * (cols // group) + r + 2
     bound = steps * 2.0 ** -23 * (np.abs(x64) @ np.abs(W_hat).T)
     if r:
-        # T = X A^T is a float32 sum of cols products, then r more additions into Y
-        bound = bound + (cols + r + 2) * 2.0 ** -23 * ((np.abs(x64) @ np.abs(A64).T) @ np.abs(B64).T)
+        # T = X A^T is a float32 sum of cols products, then r more additions into Y; on the tensor-core
+        # path T and B also go through a bf16 hi + lo split (each off by <= 2^-18 relative, the dropped
+        # lo x lo term likewise): 2^-15 covers the four of them twice over.
+        bound = bound + ((cols + r + 2) * 2.0 ** -23 + 2.0 ** -15) * ((np.abs(x64) @ np.abs(A64).T) @ np.abs(B64).T)
     err = np.abs(Yg - ref)
     assert np.all(err <= bound + 1e-30), float(np.max(err / (bound + 1e-30)))
     assert rel_fro(Yg, ref) <= 1e-5
