@@ -17,20 +17,25 @@
 // Design (one CTA per 128 tokens x 128 output columns = rows of W):
 // * warp 0 / lane 0: TMA loads, per stage, of the X tile (128 tokens x 64 K,
 //   bf16, K-major, 128-byte swizzle) and of the tile's packed words (64 K-values
-//   x 128 rows of W as 2b word-rows of 128 int32), four-stage mbarrier pipeline;
+//   x 128 rows of W as 2b word-rows of 128 int32): eight stages, deep enough to
+//   cover the load latency;
+// * the bf16 W operand tiles live in three separate buffers, written by the
+//   dequantization warps just ahead of the MMA;
 // * warps 2-5 (one thread per row of W): read the row's words from shared
 //   memory, unpack the codes, subtract the group's zero point and write the
 //   bf16 integers straight into the 128-byte-swizzled K-major operand tile,
-//   then fence to the async proxy and arrive on the stage's ready barrier;
+//   then fence to the async proxy and arrive on the buffer's ready barrier;
 // * warp 1 / lane 0: tcgen05.mma kind::f16 (M = N = 128, K = 16), one group's
 //   k-tiles into one of two TMEM accumulators;
-// * warps 6-13: per group, read the accumulator (TMEM lane quarter = warp % 4,
-//   one half of the 128 columns per warp), scale by the group's per-row scales
-//   and add into registers; store Y through shared memory, coalesced.
+// * warps 6-21: per group, read the accumulator (TMEM lane quarter = warp % 4,
+//   one quarter of the 128 columns per warp: one TMEM round trip per group),
+//   scale by the group's per-row scales and add into registers; store Y
+//   through shared memory, coalesced.
 // * The adapter term T B^T (T = X A^T from lora_t2_kernel) is one more group
 //   with scale 1: T and B as bf16 hi / lo pairs (x = hi + lo + O(2^-16 x)),
-//   three pseudo k-tiles T_hi B_hi, T_hi B_lo, T_lo B_hi loaded by TMA into the
-//   stage slots of X and W (K = r <= 64, zero-padded to 64).
+//   three pseudo k-tiles T_hi B_hi, T_hi B_lo, T_lo B_hi: T by TMA into the X
+//   slot, B copied into a W buffer by the dequantization warps (K = r <= 64,
+//   zero-padded to 64).
 // Every mbarrier wait is bounded; on expiry the CTA records the error flag that
 // gq_check_device reports and exits without writing Y.
 #include "tc_common.cuh"
@@ -44,20 +49,24 @@ namespace {
 using namespace tc;
 
 constexpr int PM = 128, PN = 128, PK = 64;
-constexpr int P_STAGES = 4;
+constexpr int P_STAGES = 6;                      // TMA stages: X tile + packed words
 constexpr int TILE_X = PM * PK * 2;              // 16 KB
 constexpr int TILE_W = PN * PK * 2;              // 16 KB
 constexpr int TILE_Q = PN * PK * 4 / 8;          // packed words of one stage, at most (4-bit): 4 KB
-constexpr int P_STAGE = TILE_X + TILE_W + TILE_Q;  // 36 KB (X and W tiles 1024-byte aligned)
-constexpr int P_SMEM = P_STAGES * P_STAGE + 1024;
+constexpr int P_STAGE = TILE_X + TILE_Q;         // 20 KB (X tiles 1024-byte aligned)
+constexpr int W_BUFS = 5;                        // bf16 W operand tiles
+constexpr int P_SMEM = P_STAGES * P_STAGE + W_BUFS * TILE_W + 1024;
 constexpr uint32_t P_TMEM = PN;                  // columns per accumulator buffer
-constexpr int P_NWARPS = 14;                     // TMA, MMA, 4 dequant, 8 epilogue
-constexpr int P_EPI = 8;                         // epilogue warps: 4 lane quarters x 2 column halves
-constexpr int P_HALF = PN / 2;                   // columns per epilogue thread
+constexpr int P_DEQ = 8;                         // dequantization warps: 2 sets of 4, alternate k-tiles
+constexpr int DEQ_SETS = 2;
+constexpr int P_EPI = 16;                        // epilogue warps: 4 lane quarters x 4 column quarters
+constexpr int P_NWARPS = 2 + P_DEQ + P_EPI;      // TMA, MMA, dequantization, epilogue
+constexpr int P_COLS = PN / 4;                   // columns per epilogue thread
 constexpr int P_STAGE_LD = PN + 4;               // epilogue staging row stride (floats)
 constexpr int ADAPTER_MAX_R = 64;
 constexpr int ADAPTER_TILES = 3;                 // T_hi B_hi, T_hi B_lo, T_lo B_hi
 static_assert(4 * 32 * P_STAGE_LD * 4 <= P_STAGES * P_STAGE, "epilogue smem");
+static_assert(P_SMEM <= 227 * 1024 - 4096, "shared memory");
 
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, N >> 3
 // at bit 17, M >> 4 at bit 24.
@@ -116,14 +125,14 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-// The stage's 64 values (q - z) of one row as 32 bf16x2 words (K order).
-// Exact: every operand is an integer below 256.
-template <int BITS>
-__device__ __forceinline__ void dequant_row(const uint32_t (&w)[PK * BITS / 32], uint32_t zz, bool valid,
-                                            float zf, uint32_t (&o)[32]) {
+// NC consecutive values (q - z) of one row (NC a multiple of 32) as NC / 2
+// bf16x2 words in K order.  Exact: every operand is an integer below 256.
+template <int BITS, int NC>
+__device__ __forceinline__ void dequant_row(const uint32_t (&w)[NC * BITS / 32], uint32_t zz, bool valid,
+                                            float zf, uint32_t (&o)[NC / 2]) {
     if constexpr (BITS == 4) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < NC / 8; ++i) {
             uint32_t t[4];
             codes4_to_bf16(w[i], t);
 #pragma unroll
@@ -131,7 +140,7 @@ __device__ __forceinline__ void dequant_row(const uint32_t (&w)[PK * BITS / 32],
         }
     } else if constexpr (BITS == 2) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < NC / 16; ++i) {
             uint32_t t[8];
             codes2_to_bf16(w[i], t);
 #pragma unroll
@@ -140,7 +149,7 @@ __device__ __forceinline__ void dequant_row(const uint32_t (&w)[PK * BITS / 32],
     } else {
         // 3-bit codes straddle words: extract each one.
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
+        for (int h = 0; h < NC / 2; ++h) {
             float d[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -156,15 +165,39 @@ __device__ __forceinline__ void dequant_row(const uint32_t (&w)[PK * BITS / 32],
     }
     if (!valid) {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) o[h] = 0u;
+        for (int h = 0; h < NC / 2; ++h) o[h] = 0u;
     }
+}
+
+// Bounded wait that polls with the non-blocking test_wait instead of the
+// suspending try_wait, for the waits on the critical path of the pipeline
+// (producer hand-offs that usually complete within a few hundred cycles).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity)) {
+        if (clock64() - t0 > WAIT_BUDGET) return false;
+    }
+    return true;
 }
 
 template <int BITS>
 __global__ void __launch_bounds__(P_NWARPS * 32, 1)
     packed_linear_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap thi, const __grid_constant__ CUtensorMap tlo,
-                         const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo,
+                         const __nv_bfloat16 *__restrict__ Bhi, const __nv_bfloat16 *__restrict__ Blo,
                          const float *__restrict__ scales, const int32_t *__restrict__ qzeros, int n, int rows,
                          int cols, int group, int adapter, float *__restrict__ Y, int64_t ldy) {
     constexpr int NW = PK * BITS / 32;  // packed words per row per stage
@@ -177,8 +210,9 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[P_STAGES];   // X and packed words landed (TMA)
-    __shared__ __align__(8) uint64_t ready_bar[P_STAGES];  // the bf16 operand tile is written
-    __shared__ __align__(8) uint64_t empty_bar[P_STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[P_STAGES];  // the MMA is done with the stage
+    __shared__ __align__(8) uint64_t wready[W_BUFS];       // a bf16 W tile is written
+    __shared__ __align__(8) uint64_t wempty[W_BUFS];       // the MMA is done with it
     __shared__ __align__(8) uint64_t tfull[2];
     __shared__ __align__(8) uint64_t tempty[2];
     __shared__ uint32_t tmem_slot;
@@ -194,8 +228,11 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
             mbar_init(&full_bar[s], 1);   // the TMA thread's expect_tx
-            mbar_init(&ready_bar[s], 4);  // one arrival per dequantization warp
             mbar_init(&empty_bar[s], 1);
+        }
+        for (int d = 0; d < W_BUFS; ++d) {
+            mbar_init(&wready[d], P_DEQ / DEQ_SETS);  // one arrival per warp of the set on this k-tile
+            mbar_init(&wempty[d], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -231,13 +268,12 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
                 if (kt < ktiles) {
                     mbar_arrive_expect_tx(&full_bar[s], TILE_X + NW * PN * 4);
                     tma_load_2d(smem + s * P_STAGE, &xmap, kt * PK, m0, &full_bar[s]);
-                    tma_load_2d(smem + s * P_STAGE + TILE_X + TILE_W, &qmap, n0, kt * NW, &full_bar[s]);
+                    tma_load_2d(smem + s * P_STAGE + TILE_X, &qmap, n0, kt * NW, &full_bar[s]);
                 } else {
-                    // adapter pseudo k-tile a: (T_hi, B_hi), (T_hi, B_lo), (T_lo, B_hi)
+                    // adapter pseudo k-tile a: T_hi, T_hi, T_lo (with B_hi, B_lo, B_hi)
                     const int a = kt - ktiles;
-                    mbar_arrive_expect_tx(&full_bar[s], TILE_X + TILE_W);
+                    mbar_arrive_expect_tx(&full_bar[s], TILE_X);
                     tma_load_2d(smem + s * P_STAGE, a == 2 ? &tlo : &thi, 0, m0, &full_bar[s]);
-                    tma_load_2d(smem + s * P_STAGE + TILE_X, a == 1 ? &blo : &bhi, 0, n0, &full_bar[s]);
                 }
             }
         }
@@ -245,6 +281,8 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_kmajor(PM, PN);
+            const uint64_t dx0 = smem_desc(smem_u32(smem), 16, 1024);                       // stage 0, X
+            const uint64_t dw0 = smem_desc(smem_u32(smem + P_STAGES * P_STAGE), 16, 1024);  // W buffer 0
             for (int gi = 0; gi < groups_all && ok; ++gi) {
                 const int b = gi & 1;
                 const uint32_t u = (uint32_t)(gi >> 1) & 1u;
@@ -258,23 +296,26 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
                 for (int kt = kb; kt < ke; ++kt) {
                     const int s = kt % P_STAGES;
                     const uint32_t ph = (uint32_t)(kt / P_STAGES) & 1u;
-                    // full: the X tile landed (TMA); ready: the W tile is written.
-                    if (!mbar_wait(&full_bar[s], ph) || !mbar_wait(&ready_bar[s], ph)) {
+                    const int d = kt % W_BUFS;
+                    const uint32_t pd = (uint32_t)(kt / W_BUFS) & 1u;
+                    // wready: the W tile is written -- by dequantization warps that first
+                    // waited for the stage's TMA (X and packed words), so X has landed too;
+                    // the adapter's W tiles are copied without that wait, so check full.
+                    if ((kt >= ktiles && !mbar_spin(&full_bar[s], ph)) || !mbar_spin(&wready[d], pd)) {
                         ok = false;
                         break;
                     }
                     fence_after();
-                    const uint32_t xa = smem_u32(smem + s * P_STAGE);
-                    const uint32_t wa = xa + TILE_X;
+                    // K-major, 128-byte swizzle: 8-row groups 1024 B apart; a k-step of
+                    // 16 bf16 values advances the start address (field in 16-byte units)
+                    // by 32 bytes, i.e. the descriptor by 2.
+                    const uint64_t da = dx0 + (uint64_t)(s * (P_STAGE >> 4));
+                    const uint64_t dw = dw0 + (uint64_t)(d * (TILE_W >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < PK / 16; ++kk) {
-                        // K-major, 128-byte swizzle: 8-row groups 1024 B apart; a
-                        // k-step of 16 bf16 values advances the start by 32 bytes.
-                        const uint64_t da = smem_desc(xa + kk * 32, 16, 1024);
-                        const uint64_t dw = smem_desc(wa + kk * 32, 16, 1024);
-                        mma_bf16(acc, da, dw, idesc, (kt == kb && kk == 0) ? 0u : 1u);
-                    }
+                    for (int kk = 0; kk < PK / 16; ++kk)
+                        mma_bf16(acc, da + 2 * kk, dw + 2 * kk, idesc, (kt == kb && kk == 0) ? 0u : 1u);
                     mma_commit(&empty_bar[s]);
+                    mma_commit(&wempty[d]);
                 }
                 if (!ok) break;
                 mma_commit(&tfull[b]);
@@ -285,17 +326,21 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // Dequantization: thread t owns row n0 + t of W.  Its packed words arrive
-        // with the stage (TMA); the zero point of the next group is loaded one
-        // group ahead.
-        const int t = threadIdx.x - 64;
+    } else if (warp < 2 + P_DEQ) {
+        // Dequantization: two sets of four warps take alternate k-tiles (the
+        // per-k-tile chain of one warp -- words, unpacking, stores, proxy fence,
+        // arrival -- is latency-bound); in a set thread t owns row n0 + t of W.
+        // The packed words arrive with the stage (TMA); the zero point of the next
+        // group is loaded one group ahead.
+        const int t = (threadIdx.x - 64) & (PN - 1);
+        const int set = (threadIdx.x - 64) >> 7;
         const int nrow = n0 + t;
         const bool valid = nrow < rows;
         const int64_t zwords = (int64_t)rows * BITS / 32;  // qzeros words per group
         auto zero_of = [&](int g) -> float {
             return valid ? (float)packed_field(qzeros + (int64_t)g * zwords, 1, (int64_t)nrow * BITS, BITS) : 0.f;
         };
+        int zg = 0;
         float zf = zero_of(0);
         float znext = ngroups > 1 ? zero_of(1) : 0.f;
         uint32_t zz = 0u;
@@ -303,22 +348,35 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
             const __nv_bfloat162 z2 = __floats2bfloat162_rn(128.f + zf, 128.f + zf);
             zz = *reinterpret_cast<const uint32_t *>(&z2);
         }
-        for (int kt = 0; kt < kt_all; ++kt) {
+        for (int kt = set; kt < kt_all; kt += DEQ_SETS) {
             const int s = kt % P_STAGES;
             const uint32_t ph = (uint32_t)(kt / P_STAGES) & 1u;
+            const int d = kt % W_BUFS;
+            const uint32_t pd = (uint32_t)(kt / W_BUFS) & 1u;
+            unsigned char *dst = smem + P_STAGES * P_STAGE + d * TILE_W + t * 128;
             if (kt >= ktiles) {
-                // adapter pseudo k-tile: both operands came by TMA; pass the stage on
-                if (!mbar_wait(&full_bar[s], ph) || *(volatile int *)&abort_flag) {
+                // adapter pseudo k-tile a: copy row t of B_hi (a = 0, 2) or B_lo (a = 1),
+                // 64 bf16, into the swizzled W tile.
+                const __nv_bfloat16 *bsrc = (kt - ktiles == 1 ? Blo : Bhi) + (int64_t)nrow * ADAPTER_MAX_R;
+                uint4 v[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    v[c] = valid ? __ldg(reinterpret_cast<const uint4 *>(bsrc) + c) : make_uint4(0u, 0u, 0u, 0u);
+                if (!mbar_wait(&wempty[d], pd ^ 1u) || *(volatile int *)&abort_flag) {
                     ok = false;
                     break;
                 }
+#pragma unroll
+                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(dst + ((c ^ (t & 7)) << 4)) = v[c];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ready_bar[s]);
+                if (lane == 0) mbar_arrive(&wready[d]);
                 continue;
             }
-            if (kt > 0 && kt % ktg == 0) {  // a new group starts
-                const int g = kt / ktg;
-                zf = znext;
+            const int g = kt / ktg;
+            if (g != zg) {  // a new group
+                zf = (g == zg + 1) ? znext : zero_of(g);
+                zg = g;
                 znext = g + 1 < ngroups ? zero_of(g + 1) : 0.f;
                 const __nv_bfloat162 z2 = __floats2bfloat162_rn(128.f + zf, 128.f + zf);
                 zz = *reinterpret_cast<const uint32_t *>(&z2);
@@ -327,13 +385,16 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
                 ok = false;
                 break;
             }
-            const uint32_t *wq = reinterpret_cast<const uint32_t *>(smem + s * P_STAGE + TILE_X + TILE_W);
+            const uint32_t *wq = reinterpret_cast<const uint32_t *>(smem + s * P_STAGE + TILE_X);
             uint32_t w[NW];
 #pragma unroll
             for (int i = 0; i < NW; ++i) w[i] = wq[i * PN + t];
             uint32_t o[32];
-            dequant_row<BITS>(w, zz, valid, zf, o);
-            unsigned char *dst = smem + s * P_STAGE + TILE_X + t * 128;
+            dequant_row<BITS, 64>(w, zz, valid, zf, o);
+            if (!mbar_wait(&wempty[d], pd ^ 1u) || *(volatile int *)&abort_flag) {
+                ok = false;
+                break;
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<uint4 *>(dst + ((c ^ (t & 7)) << 4)) =
@@ -341,7 +402,7 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
             // Generic-proxy writes -> visible to the tensor core's async proxy.
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ready_bar[s]);
+            if (lane == 0) mbar_arrive(&wready[d]);
         }
         if (!ok) {
             atomicOr(&g_packed_error, 1u);
@@ -349,14 +410,14 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
         }
         __syncwarp();
     } else {
-        // Epilogue warps: TMEM lane quarter = warp % 4, column half hf; each
-        // thread owns one token row x 64 columns.
-        const int q = warp & 3, hf = (warp - 6) >> 2;
-        const int cb = hf * P_HALF;  // first column of this warp's half
-        float acc[P_HALF];
+        // Epilogue warps: TMEM lane quarter = warp % 4, column quarter cq; each
+        // thread owns one token row x 32 columns.
+        const int q = warp & 3, cq = (warp - 2 - P_DEQ) >> 2;
+        const int cb = cq * P_COLS;  // first column of this warp's quarter
+        float acc[P_COLS];
 #pragma unroll
-        for (int i = 0; i < P_HALF; ++i) acc[i] = 0.f;
-        const int et = threadIdx.x - 192;  // 0..255 over the eight epilogue warps
+        for (int i = 0; i < P_COLS; ++i) acc[i] = 0.f;
+        const int et = threadIdx.x - (2 + P_DEQ) * 32;  // 0..511 over the epilogue warps
         if (et < PN) sc_ring[0][et] = (n0 + et < rows) ? __ldg(scales + n0 + et) : 0.f;
         asm volatile("bar.sync 1, %0;" ::"n"(P_EPI * 32) : "memory");
         for (int gi = 0; gi < groups_all; ++gi) {
@@ -375,18 +436,15 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
                 fence_after();
                 const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * P_TMEM + cb);
                 const float *sg = &sc_ring[gi & 1][cb];
+                float v[32];
+                tmem_ld32(base, v);
 #pragma unroll
-                for (int ch = 0; ch < P_HALF / 32; ++ch) {
-                    float v[32];
-                    tmem_ld32(base + ch * 32, v);
-#pragma unroll
-                    for (int i4 = 0; i4 < 8; ++i4) {
-                        const float4 s4 = *(reinterpret_cast<const float4 *>(sg + ch * 32) + i4);
-                        acc[ch * 32 + i4 * 4 + 0] = fmaf(s4.x, v[i4 * 4 + 0], acc[ch * 32 + i4 * 4 + 0]);
-                        acc[ch * 32 + i4 * 4 + 1] = fmaf(s4.y, v[i4 * 4 + 1], acc[ch * 32 + i4 * 4 + 1]);
-                        acc[ch * 32 + i4 * 4 + 2] = fmaf(s4.z, v[i4 * 4 + 2], acc[ch * 32 + i4 * 4 + 2]);
-                        acc[ch * 32 + i4 * 4 + 3] = fmaf(s4.w, v[i4 * 4 + 3], acc[ch * 32 + i4 * 4 + 3]);
-                    }
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float4 s4 = *(reinterpret_cast<const float4 *>(sg) + i4);
+                    acc[i4 * 4 + 0] = fmaf(s4.x, v[i4 * 4 + 0], acc[i4 * 4 + 0]);
+                    acc[i4 * 4 + 1] = fmaf(s4.y, v[i4 * 4 + 1], acc[i4 * 4 + 1]);
+                    acc[i4 * 4 + 2] = fmaf(s4.z, v[i4 * 4 + 2], acc[i4 * 4 + 2]);
+                    acc[i4 * 4 + 3] = fmaf(s4.w, v[i4 * 4 + 3], acc[i4 * 4 + 3]);
                 }
                 fence_before();
                 __syncwarp();
@@ -406,18 +464,18 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
         // last group's accumulator completed): staging rows for the coalesced store.
         float *stage = reinterpret_cast<float *>(smem) + (size_t)q * 32 * P_STAGE_LD;
 #pragma unroll
-        for (int j = 0; j < P_HALF; j += 4)
+        for (int j = 0; j < P_COLS; j += 4)
             *reinterpret_cast<float4 *>(stage + lane * P_STAGE_LD + cb + j) =
                 make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
         __syncwarp();
-        // Store this warp's 32 rows x 64 columns: lanes 0-15 one row, 16-31 the next,
-        // 16 bytes per lane (256 contiguous bytes per row).
-        const int c = n0 + cb + (lane & 15) * 4;  // rows % 4 == 0
+        // Store this warp's 32 rows x 32 columns: lanes 8 i .. 8 i + 7 one row,
+        // 16 bytes per lane (128 contiguous bytes per row).
+        const int c = n0 + cb + (lane & 7) * 4;  // rows % 4 == 0
         if (ok && c < rows) {
-            for (int rr = lane >> 4; rr < 32; rr += 2) {
+            for (int rr = lane >> 3; rr < 32; rr += 4) {
                 const int mr = m0 + q * 32 + rr;
                 if (mr >= n) break;
-                const float4 v = *reinterpret_cast<const float4 *>(stage + rr * P_STAGE_LD + cb + (lane & 15) * 4);
+                const float4 v = *reinterpret_cast<const float4 *>(stage + rr * P_STAGE_LD + cb + (lane & 7) * 4);
                 *reinterpret_cast<float4 *>(Y + (int64_t)mr * ldy + c) = v;
             }
         }
@@ -569,7 +627,7 @@ bool make_q_map(CUtensorMap *map, const int32_t *qweight, int64_t rows, int64_t 
 
 template <int BITS>
 cudaError_t launch_bits(const CUtensorMap &xmap, const CUtensorMap &qmap, const CUtensorMap &thi,
-                        const CUtensorMap &tlo, const CUtensorMap &bhi, const CUtensorMap &blo, const float *scales,
+                        const CUtensorMap &tlo, const __nv_bfloat16 *bhi, const __nv_bfloat16 *blo, const float *scales,
                         const int32_t *qzeros, int n, int rows, int cols, int group, int adapter, float *Y,
                         int64_t ldy, cudaStream_t s) {
     static bool attr_set = false;
@@ -668,21 +726,19 @@ cudaError_t packed_forward(const __nv_bfloat16 *X, int64_t n, int64_t ldx, const
     if (decode)
         return packed_gemv_launch(X, n, ldx, qweight, scales, qzeros, rows, cols, bits, group, w.T, B, r, w.Ypart, Y,
                                   ldy, s);
-    CUtensorMap xmap, qmap, thi, tlo, bhi, blo;
+    CUtensorMap xmap, qmap, thi, tlo;
     if (!make_x_map(&xmap, X, n, cols, ldx) || !make_q_map(&qmap, qweight, rows, cols, bits))
         return cudaErrorInvalidValue;
     if (r > 0) {
-        if (!make_r_map(&thi, w.Thi, n) || !make_r_map(&tlo, w.Tlo, n) || !make_r_map(&bhi, w.Bhi, rows) ||
-            !make_r_map(&blo, w.Blo, rows))
-            return cudaErrorInvalidValue;
+        if (!make_r_map(&thi, w.Thi, n) || !make_r_map(&tlo, w.Tlo, n)) return cudaErrorInvalidValue;
     } else {
-        thi = tlo = bhi = blo = xmap;  // never read without the adapter
+        thi = tlo = xmap;  // never read without the adapter
     }
     const int ad = r > 0 ? 1 : 0;
     switch (bits) {
-        case 2: return launch_bits<2>(xmap, qmap, thi, tlo, bhi, blo, scales, qzeros, (int)n, (int)rows, (int)cols, group, ad, Y, ldy, s);
-        case 3: return launch_bits<3>(xmap, qmap, thi, tlo, bhi, blo, scales, qzeros, (int)n, (int)rows, (int)cols, group, ad, Y, ldy, s);
-        case 4: return launch_bits<4>(xmap, qmap, thi, tlo, bhi, blo, scales, qzeros, (int)n, (int)rows, (int)cols, group, ad, Y, ldy, s);
+        case 2: return launch_bits<2>(xmap, qmap, thi, tlo, w.Bhi, w.Blo, scales, qzeros, (int)n, (int)rows, (int)cols, group, ad, Y, ldy, s);
+        case 3: return launch_bits<3>(xmap, qmap, thi, tlo, w.Bhi, w.Blo, scales, qzeros, (int)n, (int)rows, (int)cols, group, ad, Y, ldy, s);
+        case 4: return launch_bits<4>(xmap, qmap, thi, tlo, w.Bhi, w.Blo, scales, qzeros, (int)n, (int)rows, (int)cols, group, ad, Y, ldy, s);
         default: return cudaErrorInvalidValue;
     }
 }
