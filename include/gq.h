@@ -289,6 +289,34 @@ gq_status gptq_packed_linear(const void *X, int64_t n, int64_t ldx, const int32_
                              gq_stream_t stream);
 
 /*
+ * One Bid-Up sweep ([GPTQ-LoRA] "Metodología", item 4 "Refinamiento Bid-Up"):
+ * the codes of a quantized layer are refined in place on their fixed grid
+ * (each group's scale and zero point kept) against the target T = W - B A, the
+ * layer minus its low-rank correction.  Column by column, in order, each code
+ * moves to the grid point nearest ŵ_j + g_j / H_jj, where g = (T - Ŵ) H is kept
+ * current after every move; each move minimizes 1/2 tr((T - Ŵ) H (T - Ŵ)^T)
+ * over that one coordinate, so the objective never increases.  Alternated with
+ * OLrC -- the optimal rank-r B A for fixed codes, which is eora_compensate on
+ * W - Ŵ -- it gives the page's refinement cycle.
+ *
+ *   W        rows x cols, type wt, read only.   H  cols x cols float32 (undamped), 16-byte aligned.
+ *   A, B     the correction, r x cols and rows x r float32, or both NULL with r = 0; 0 <= r <= 64.
+ *   codes    rows x cols uint8, in/out (the layout gptq_quantize_layer writes).
+ *   scales, qzeros   the grid, as gptq_quantize_layer writes them (read only).
+ *   W_hat    rows x cols float32 output: s (q - z) of the refined codes.
+ *   qweight  [cols*bits/32][rows] int32 output (the refined codes packed), may be NULL.
+ *   changed  one device uint64, may be NULL: the number of codes that moved is ADDED to it.
+ *   Requires rows % 32 == 0, cols % 32 == 0, group % 32 == 0, cols % group == 0.
+ *   ws       >= gptq_bidup_workspace_size(rows, cols) bytes.
+ * The integer decision rint(g_j / (H_jj s)) is taken in float32.  Asynchronous.
+ */
+size_t gptq_bidup_workspace_size(int64_t rows, int64_t cols);
+gq_status gptq_bidup(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *H, const float *A,
+                     const float *B, int r, int bits, int group, uint8_t *codes, const float *scales,
+                     const int32_t *qzeros, float *W_hat, int32_t *qweight, unsigned long long *changed, void *ws,
+                     size_t ws_bytes, gq_stream_t stream);
+
+/*
  * gptq_quantize_layer without a caller-provided workspace, for callers that
  * cannot allocate device memory: code inside a host application that owns all
  * device memory through its own pool, a service that must not grow its device

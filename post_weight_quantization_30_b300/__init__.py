@@ -9,6 +9,7 @@ from ._lib import (  # noqa: F401
     LIB_PATH,
     SIGNATURES,
     eora_compensate,
+    gptq_bidup,
     gptq_code_decisions,
     gptq_factor,
     gptq_hessian_accumulate,

@@ -60,6 +60,8 @@ SIGNATURES = {
                                  _sz, _p, ctypes.POINTER(_i64)]),
     "gptq_packed_linear_workspace_size": (_sz, [_i64, _i64, _i64, _i, _i]),
     "gptq_packed_linear": (_i, [_p, _i64, _i64, _p, _p, _p, _i64, _i64, _i, _i, _p, _p, _i, _p, _i64, _p, _sz, _p]),
+    "gptq_bidup_workspace_size": (_sz, [_i64, _i64]),
+    "gptq_bidup": (_i, [_p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "gptq_code_decisions": (_i, [_p, _p, _i64, _p, _p]),
     "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
     "gptq_unpack": (_i, [_p, _i64, _i64, _i, _p, _p]),
@@ -305,6 +307,25 @@ def gptq_packed_linear(X: torch.Tensor, qweight: torch.Tensor, scales: torch.Ten
                                   _ptr(None if B is None else B.contiguous()), r, _ptr(Y), Y.stride(0), _ptr(ws),
                                   0 if ws is None else ws.numel(), _stream(X.device)), "gptq_packed_linear")
     return Y
+
+
+def gptq_bidup(W: torch.Tensor, H: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, qzeros: torch.Tensor,
+               bits: int, group: int, A: torch.Tensor | None = None, B: torch.Tensor | None = None,
+               W_hat: torch.Tensor | None = None, qweight: torch.Tensor | None = None,
+               workspace: torch.Tensor | None = None) -> dict:
+    """One Bid-Up sweep: `codes` refined in place against W - B A.  Returns dict(codes, W_hat, qweight, changed)."""
+    _need_cuda(W, H, codes, scales, qzeros, A, B)
+    rows, cols = W.shape
+    W = W.contiguous()
+    r = 0 if A is None else A.shape[0]
+    Wh = W_hat if W_hat is not None else torch.empty((rows, cols), dtype=torch.float32, device=W.device)
+    changed = torch.zeros(1, dtype=torch.int64, device=W.device)
+    ws = workspace if workspace is not None else _workspace(lib.gptq_bidup_workspace_size(rows, cols), W.device)
+    _check(lib.gptq_bidup(_ptr(W), _dtype_code(W), rows, cols, _ptr(H.contiguous()),
+                          _ptr(None if A is None else A.contiguous()), _ptr(None if B is None else B.contiguous()), r,
+                          bits, group, _ptr(codes), _ptr(scales.contiguous()), _ptr(qzeros.contiguous()), _ptr(Wh),
+                          _ptr(qweight), _ptr(changed), _ptr(ws), ws.numel(), _stream(W.device)), "gptq_bidup")
+    return dict(codes=codes, W_hat=Wh, qweight=qweight, changed=changed)
 
 
 def gq_check_device(device=None):

@@ -427,6 +427,30 @@ gq_status gptq_packed_linear(const void *X, int64_t n, int64_t ldx, const int32_
     return e == cudaSuccess ? GQ_OK : GQ_ECUDA;
 }
 
+size_t gptq_bidup_workspace_size(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return bidup_workspace_bytes(rows, cols);
+}
+
+gq_status gptq_bidup(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *H, const float *A,
+                     const float *B, int r, int bits, int group, uint8_t *codes, const float *scales,
+                     const int32_t *qzeros, float *W_hat, int32_t *qweight, unsigned long long *changed, void *ws,
+                     size_t ws_bytes, gq_stream_t stream) {
+    if (wt != GQ_F32 && wt != GQ_BF16) return GQ_EUNSUPPORTED;
+    if (bits != 2 && bits != 3 && bits != 4) return GQ_EUNSUPPORTED;
+    if (!W || !H || !codes || !scales || !qzeros || !W_hat) return GQ_EINVAL;
+    if (rows <= 0 || cols <= 0 || rows % 32 || cols % 32) return GQ_EINVAL;
+    if (group <= 0 || group % 32 || cols % group) return GQ_EINVAL;
+    if (r < 0 || r > 64 || (r > 0 && (!A || !B))) return GQ_EINVAL;
+    if (!aligned(H, 16) || !aligned(W_hat, 4) || !aligned(scales, 4) || !aligned(qzeros, 4)) return GQ_EINVAL;
+    if ((qweight && !aligned(qweight, 4)) || (changed && !aligned(changed, 8))) return GQ_EINVAL;
+    if (!ws || !aligned(ws, kAlign) || ws_bytes < bidup_workspace_bytes(rows, cols)) return GQ_EWORKSPACE;
+    return bidup_run(W, wt == GQ_BF16, rows, cols, H, r > 0 ? A : nullptr, r > 0 ? B : nullptr, r, bits, group,
+                     codes, scales, qzeros, W_hat, qweight, changed, ws, cs(stream)) == cudaSuccess
+               ? GQ_OK
+               : GQ_ECUDA;
+}
+
 gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *W_hat, float *dW,
                             gq_stream_t stream) {
     if (wt != GQ_F32 && wt != GQ_BF16) return GQ_EUNSUPPORTED;

@@ -219,6 +219,15 @@ cudaError_t packed_gemv_launch(const __nv_bfloat16 *X, int64_t n, int64_t ldx, c
                                int group, const float *T, const float *B, int r, float *Ypart, float *Y, int64_t ldy,
                                cudaStream_t s);
 
+// Bid-Up sweep (refine.cu): codes refined in place on their fixed grid against the target
+// W - B A; W_hat written; qweight repacked when non-NULL; the number of moved codes added
+// into *changed_out (device) when non-NULL.
+size_t bidup_workspace_bytes(int64_t rows, int64_t cols);
+cudaError_t bidup_run(const void *W, bool w_bf16, int64_t rows, int64_t cols, const float *H, const float *A,
+                      const float *B, int r, int bits, int group, uint8_t *codes, const float *scales,
+                      const int32_t *qzeros, float *W_hat, int32_t *qweight, unsigned long long *changed_out,
+                      void *ws, cudaStream_t s);
+
 // dW = W - W_hat, n elements (W float32 or bf16).
 cudaError_t weight_error_launch(const void *W, bool w_bf16, int64_t n, const float *W_hat, float *dW, cudaStream_t s);
 

@@ -139,3 +139,22 @@ def test_packed_linear_host_side_validation(gq):
     assert gq.lib.gptq_packed_linear_workspace_size(1000, 64, 256, 64, 16) >= 1000 * 16 * 4
     assert gq.lib.gptq_packed_linear_workspace_size(1000, 64, 256, 64, 0) == 0     # prefill, no adapter
     assert gq.lib.gptq_packed_linear_workspace_size(16, 64, 256, 64, 0) >= 16 * 64 * 4
+
+
+def test_bidup_host_side_validation(gq):
+    p = ctypes.c_void_p
+    f = gq.lib.gptq_bidup
+    ws = gq.lib.gptq_bidup_workspace_size(64, 256)
+    assert ws >= 4 * 64 * 256 * 4 + 2 * 256 * 256 * 4
+
+    def call(rows=64, cols=256, bits=4, group=64, r=0, A=None, B=None, H=p(256), ws_bytes=ws):
+        return f(p(256), 0, rows, cols, H, A, B, r, bits, group, p(256), p(256), p(256), p(256), None, None, p(256),
+                 ws_bytes, None)
+
+    assert call(bits=5) == -3
+    assert call(rows=48) == -1          # rows % 32 (packing)
+    assert call(group=48) == -1
+    assert call(r=4) == -1              # a correction needs A and B
+    assert call(r=65, A=p(256), B=p(256)) == -1
+    assert call(H=p(260)) == -1         # H 16-byte aligned
+    assert call(ws_bytes=ws - 1) == -7
