@@ -2,9 +2,11 @@
 
 One step = one pass of the whole path over one synthetic layer:
     H = 0; gptq_hessian_accumulate(H, X); gptq_quantize_layer(W, H, ...)
-(+ gptq_weight_error and eora_compensate on the EoRA workloads; on the
+(+ gptq_weight_error and eora_compensate on the EoRA workloads, + cycles of
+eora_compensate and gptq_bidup on the refinement workloads; on the
 GPTQ-intrinsic LoRA workloads gptq_lora_basis and gptq_intrinsic_lora in place
-of gptq_quantize_layer) with X and W resident in HBM.  X (2.15 GB for the default workload) is larger
+of gptq_quantize_layer; the packed-layer workloads time gptq_packed_linear)
+with X and W resident in HBM.  X (2.15 GB for the default workload) is larger
 than the 126 MB L2, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
@@ -180,8 +182,13 @@ def run_ours(args, rank: int, world: int):
     ws = torch.empty(gq.lib.gptq_quantize_layer_workspace_size(R, C, spec.block), dtype=torch.uint8, device=dev)
     r = spec.eora_rank
     rl = spec.lora_rank
-    # Ŵ is an output only when EoRA or the intrinsic LoRA needs it (the error they compensate is W - Ŵ).
-    out = gq._lib._sweep_outputs(R, C, spec.bits, spec.group, dev, codes=False, W_hat=(r or rl) > 0, row_err=False)
+    rc = spec.refine_cycles
+    # Ŵ is an output only when EoRA or the intrinsic LoRA needs it (the error they compensate is W - Ŵ);
+    # the refinement also needs the codes.
+    out = gq._lib._sweep_outputs(R, C, spec.bits, spec.group, dev, codes=rc > 0, W_hat=(r or rl) > 0,
+                                 row_err=False)
+    if rc:
+        bu_ws = torch.empty(gq.lib.gptq_bidup_workspace_size(R, C), dtype=torch.uint8, device=dev)
     if rl:
         ws = torch.empty(gq.lib.gptq_intrinsic_lora_workspace_size(R, C, rl, spec.block), dtype=torch.uint8,
                          device=dev)
@@ -201,6 +208,13 @@ def run_ours(args, rank: int, world: int):
         gq.gptq_weight_error(Wsrc, out["W_hat"], out=dW)
         gq.eora_compensate(dW, H, r, workspace=ews, out=eout)
 
+    def refine_part(Wsrc):
+        # rc cycles of OLrC (EoRA of W - Ŵ) then Bid-Up against W - B A; codes, Ŵ and qweight refined in place
+        for _ in range(rc):
+            eora_part(Wsrc)
+            gq.gptq_bidup(Wsrc, H, out["codes"], out["scales"], out["qzeros"], spec.bits, spec.group, eout["A"],
+                          eout["B"], W_hat=out["W_hat"], qweight=out["qweight"], workspace=bu_ws)
+
     def quantize(Wsrc):
         if rl:
             gq.gptq_lora_basis(H, rl, workspace=bws, out=bout)
@@ -208,7 +222,9 @@ def run_ours(args, rank: int, world: int):
                                    out=out)
             return
         gq.gptq_quantize_layer(Wsrc, H, spec.bits, spec.group, spec.block, spec.damp, workspace=ws, out=out)
-        if r:
+        if rc:
+            refine_part(Wsrc)
+        elif r:
             eora_part(Wsrc)
 
     def step(ev=None):
@@ -281,7 +297,7 @@ def run_ours(args, rank: int, world: int):
     else:
         reps_done = False
     if r:
-        acc["eora"] = 0.0
+        acc["eora" if not rc else "refine"] = 0.0
         e.append(torch.cuda.Event(enable_timing=True))
     for _ in range(0 if reps_done else reps):
         H.zero_()
@@ -294,10 +310,15 @@ def run_ours(args, rank: int, world: int):
                                 ctypes.c_void_p(stream.cuda_stream), ctypes.byref(info))
         assert st == 0, st
         e[2].record(stream)
-        so = gq.gptq_sweep(W, F, dead, spec.bits, spec.group, spec.block, codes=False, W_hat=r > 0, row_err=False,
+        so = gq.gptq_sweep(W, F, dead, spec.bits, spec.group, spec.block, codes=rc > 0, W_hat=r > 0, row_err=False,
                            workspace=sws)
         e[3].record(stream)
-        if r:
+        if rc:
+            for kk in ("codes", "W_hat"):
+                out[kk].copy_(so[kk])
+            refine_part(W)
+            e[4].record(stream)
+        elif r:
             gq.gptq_weight_error(W, so["W_hat"], out=dW)
             gq.eora_compensate(dW, H, r, workspace=ews, out=eout)
             e[4].record(stream)
@@ -306,7 +327,7 @@ def run_ours(args, rank: int, world: int):
         acc["factor"] += e[1].elapsed_time(e[2])
         acc["sweep"] += e[2].elapsed_time(e[3])
         if r:
-            acc["eora"] += e[3].elapsed_time(e[4])
+            acc["eora" if not rc else "refine"] += e[3].elapsed_time(e[4])
     phase = {k: v / reps for k, v in acc.items()}
 
     # End to end through the public API from pinned host buffers, every step:
@@ -359,7 +380,7 @@ def run_ours(args, rank: int, world: int):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16 x bf16 -> f32 (Hessian); f32 (factor, sweep, 3xTF32 GEMMs" +
-                 (", EoRA)" if r else ", intrinsic LoRA)" if rl else ")"),
+                 (", OLrC + Bid-Up)" if rc else ", EoRA)" if r else ", intrinsic LoRA)" if rl else ")"),
         "data": describe_inputs(spec),
         "config": {
             "workload": args.workload, "rows": R, "cols": C, "tokens": N, "bits": spec.bits, "group": spec.group,
@@ -642,7 +663,8 @@ def cpu_baseline(spec, budget_s: float = 20.0) -> dict:
                    if spec.lora_rank else
                    f"full float64 inverse + Cholesky of {spec.cols}x{spec.cols}; ") +
                   f"eager sweep + pack on {r_s} of {spec.rows} rows (x{spec.rows / r_s:g})" +
-                  ("; EoRA not included" if spec.eora_rank else ""),
+                  ("; the OLrC + Bid-Up cycles not included" if spec.refine_cycles else
+                   "; EoRA not included" if spec.eora_rank else ""),
         "sample_s": round(t4 - t0, 2),
         "phases_s": {"hessian": round((t1 - t0) * spec.n / n_s, 3), "factor": round(t2 - t1, 3),
                      "sweep": round((t3 - t2) * spec.rows / r_s, 3), "pack": round((t4 - t3) * spec.rows / r_s, 3)},

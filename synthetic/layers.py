@@ -69,6 +69,7 @@ class LayerSpec:
     eora_rank: int = 0
     lora_rank: int = 0  # GPTQ-intrinsic LoRA rank (0: plain GPTQ)
     packed_tokens: int = 0  # > 0: the workload is the packed layer applied to this many tokens (X is n x cols)
+    refine_cycles: int = 0  # > 0: after GPTQ, this many OLrC (rank eora_rank) + Bid-Up cycles
     notes: str = field(default="", compare=False)
 
     @property
@@ -127,6 +128,9 @@ LAYERS: dict[str, LayerSpec] = {
         LayerSpec("qwen32b_5120x5120_packed_eora_r64_n4096", W=_w(5120, 5120, 0.02, (4, 0)),
                   X=TensorSpec(4096, 5120, "normal", n_outliers=51, outlier_scale=30.0, key=(5, 4)), bits=2,
                   group=64, eora_rank=64, packed_tokens=4096),
+        # GPTQ followed by two OLrC + Bid-Up refinement cycles at rank 64.
+        LayerSpec("qwen32b_5120x5120_refine_r64_c2", W=_w(5120, 5120, 0.02, (4, 0)), X=_X_QWEN32B_5120, bits=2,
+                  group=64, eora_rank=64, refine_cycles=2),
         # The same two layers with a rank-64 GPTQ-intrinsic LoRA in place of EoRA.
         LayerSpec("qwen32b_5120x5120_intrinsic_r64", W=_w(5120, 5120, 0.02, (4, 0)), X=_X_QWEN32B_5120, bits=2,
                   group=64, lora_rank=64),
