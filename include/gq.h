@@ -317,6 +317,23 @@ gq_status gptq_bidup(const void *W, gq_dtype wt, int64_t rows, int64_t cols, con
                      size_t ws_bytes, gq_stream_t stream);
 
 /*
+ * Round to nearest on the GPTQ grid, for low-precision low-rank factors
+ * ([GPTQ-LoRA] "Resultados Clave": L and R quantized to 4 and 8 bits are often
+ * lossless): per row and group of `group` consecutive columns, xmin = min(0,
+ * min x), xmax = max(0, max x) ([-1, 1] when both are 0), s = (xmax - xmin) /
+ * (2^bits - 1), z = rint(-xmin / s), q = clamp(rint(x / s) + z, 0, 2^bits - 1),
+ * x̂ = s (q - z), every division IEEE float32 -- the grid of the GPTQ sweep
+ * without its error propagation.
+ *
+ *   M       nrows x ncols float32, read only.   bits  2 .. 8.   ncols % group == 0.
+ *   M_hat   nrows x ncols float32 output.   codes  nrows x ncols uint8 output, may be NULL.
+ *   scales  [ncols/group][nrows] float32 output.   zeros  [ncols/group][nrows] uint8 output.
+ * Asynchronous.
+ */
+gq_status gptq_quantize_rtn(const float *M, int64_t nrows, int64_t ncols, int bits, int group, float *M_hat,
+                            uint8_t *codes, float *scales, uint8_t *zeros, gq_stream_t stream);
+
+/*
  * gptq_quantize_layer without a caller-provided workspace, for callers that
  * cannot allocate device memory: code inside a host application that owns all
  * device memory through its own pool, a service that must not grow its device

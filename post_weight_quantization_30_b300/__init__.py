@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401
     gptq_pack,
     gptq_quantize_layer,
     gptq_quantize_layer_noalloc,
+    gptq_quantize_rtn,
     gptq_sweep,
     gptq_unpack,
     gptq_weight_error,

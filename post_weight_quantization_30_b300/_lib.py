@@ -62,6 +62,7 @@ SIGNATURES = {
     "gptq_packed_linear": (_i, [_p, _i64, _i64, _p, _p, _p, _i64, _i64, _i, _i, _p, _p, _i, _p, _i64, _p, _sz, _p]),
     "gptq_bidup_workspace_size": (_sz, [_i64, _i64]),
     "gptq_bidup": (_i, [_p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "gptq_quantize_rtn": (_i, [_p, _i64, _i64, _i, _i, _p, _p, _p, _p, _p]),
     "gptq_code_decisions": (_i, [_p, _p, _i64, _p, _p]),
     "gptq_pack": (_i, [_p, _i64, _i64, _i, _p, _p]),
     "gptq_unpack": (_i, [_p, _i64, _i64, _i, _p, _p]),
@@ -326,6 +327,22 @@ def gptq_bidup(W: torch.Tensor, H: torch.Tensor, codes: torch.Tensor, scales: to
                           bits, group, _ptr(codes), _ptr(scales.contiguous()), _ptr(qzeros.contiguous()), _ptr(Wh),
                           _ptr(qweight), _ptr(changed), _ptr(ws), ws.numel(), _stream(W.device)), "gptq_bidup")
     return dict(codes=codes, W_hat=Wh, qweight=qweight, changed=changed)
+
+
+def gptq_quantize_rtn(M: torch.Tensor, bits: int, group: int | None = None) -> dict:
+    """Round to nearest on the GPTQ grid per row and group (default: the whole row).  float32 M."""
+    _need_cuda(M)
+    if M.dtype != torch.float32:
+        raise ValueError("M must be float32")
+    nrows, ncols = M.shape
+    group = ncols if group is None else group
+    M = M.contiguous()
+    o = dict(M_hat=torch.empty_like(M), codes=torch.empty((nrows, ncols), dtype=torch.uint8, device=M.device),
+             scales=torch.empty((ncols // group, nrows), dtype=torch.float32, device=M.device),
+             zeros=torch.empty((ncols // group, nrows), dtype=torch.uint8, device=M.device))
+    _check(lib.gptq_quantize_rtn(_ptr(M), nrows, ncols, bits, group, _ptr(o["M_hat"]), _ptr(o["codes"]),
+                                 _ptr(o["scales"]), _ptr(o["zeros"]), _stream(M.device)), "gptq_quantize_rtn")
+    return o
 
 
 def gq_check_device(device=None):

@@ -451,6 +451,17 @@ gq_status gptq_bidup(const void *W, gq_dtype wt, int64_t rows, int64_t cols, con
                : GQ_ECUDA;
 }
 
+gq_status gptq_quantize_rtn(const float *M, int64_t nrows, int64_t ncols, int bits, int group, float *M_hat,
+                            uint8_t *codes, float *scales, uint8_t *zeros, gq_stream_t stream) {
+    if (bits < 2 || bits > 8) return GQ_EUNSUPPORTED;
+    if (!M || !M_hat || !scales || !zeros) return GQ_EINVAL;
+    if (nrows <= 0 || ncols <= 0 || group <= 0 || ncols % group) return GQ_EINVAL;
+    if (!aligned(M, 4) || !aligned(M_hat, 4) || !aligned(scales, 4)) return GQ_EINVAL;
+    return rtn_launch(M, nrows, ncols, bits, group, M_hat, codes, scales, zeros, cs(stream)) == cudaSuccess
+               ? GQ_OK
+               : GQ_ECUDA;
+}
+
 gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t cols, const float *W_hat, float *dW,
                             gq_stream_t stream) {
     if (wt != GQ_F32 && wt != GQ_BF16) return GQ_EUNSUPPORTED;

@@ -228,6 +228,10 @@ cudaError_t bidup_run(const void *W, bool w_bf16, int64_t rows, int64_t cols, co
                       const int32_t *qzeros, float *W_hat, int32_t *qweight, unsigned long long *changed_out,
                       void *ws, cudaStream_t s);
 
+// Round to nearest on the GPTQ grid per row and group (refine.cu).
+cudaError_t rtn_launch(const float *M, int64_t nrows, int64_t ncols, int bits, int group, float *M_hat,
+                       uint8_t *codes, float *scales, uint8_t *zeros, cudaStream_t s);
+
 // dW = W - W_hat, n elements (W float32 or bf16).
 cudaError_t weight_error_launch(const void *W, bool w_bf16, int64_t n, const float *W_hat, float *dW, cudaStream_t s);
 

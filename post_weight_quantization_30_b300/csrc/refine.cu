@@ -267,3 +267,65 @@ cudaError_t bidup_run(const void *W, bool w_bf16, int64_t rows, int64_t cols, co
 }
 
 }  // namespace gq
+
+// ---------------------------------------------------------------------------
+// Round to nearest on the GPTQ grid, for the low-rank factors ("Resumen
+// Técnico: GPTQ-intrinsic LoRA", "Resultados Clave": 4-bit L and 8-bit R).
+// Per row and group of `group` columns: xmin = min(0, min x), xmax = max(0,
+// max x) (both 0: [-1, 1]), s = (xmax - xmin) / maxq, z = rint(-xmin / s),
+// q = clamp(rint(x / s) + z, 0, maxq), x̂ = s (q - z); every division IEEE.
+// One warp per (row, group).
+// ---------------------------------------------------------------------------
+namespace gq {
+namespace {
+
+__global__ void rtn_kernel(const float *__restrict__ M, int64_t nrows, int64_t ncols, int bits, int group,
+                           float *__restrict__ M_hat, uint8_t *__restrict__ codes, float *__restrict__ scales,
+                           uint8_t *__restrict__ zeros) {
+    const int64_t ngr = ncols / group;
+    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= nrows * ngr) return;
+    const int64_t row = wid / ngr, g = wid - row * ngr;
+    const float *x = M + row * ncols + g * group;
+    float mn = 0.f, mx = 0.f;
+    for (int k = lane; k < group; k += 32) {
+        mn = fminf(mn, x[k]);
+        mx = fmaxf(mx, x[k]);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (mn == 0.f && mx == 0.f) {
+        mn = -1.f;
+        mx = 1.f;
+    }
+    const float maxq = (float)((1 << bits) - 1);
+    const float s = __fdiv_rn(mx - mn, maxq);
+    const float z = rintf(__fdiv_rn(-mn, s));
+    if (lane == 0) {
+        scales[g * nrows + row] = s;
+        zeros[g * nrows + row] = (uint8_t)z;
+    }
+    for (int k = lane; k < group; k += 32) {
+        const float q = fminf(fmaxf(rintf(__fdiv_rn(x[k], s)) + z, 0.f), maxq);
+        const int64_t o = row * ncols + g * group + k;
+        M_hat[o] = s * (q - z);
+        if (codes) codes[o] = (uint8_t)q;
+    }
+}
+
+}  // namespace
+
+cudaError_t rtn_launch(const float *M, int64_t nrows, int64_t ncols, int bits, int group, float *M_hat,
+                       uint8_t *codes, float *scales, uint8_t *zeros, cudaStream_t s) {
+    const int64_t warps = nrows * (ncols / group);
+    int64_t g = (warps * 32 + 255) / 256;
+    if (g < 1) g = 1;
+    rtn_kernel<<<(unsigned)g, 256, 0, s>>>(M, nrows, ncols, bits, group, M_hat, codes, scales, zeros);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace gq

@@ -158,3 +158,12 @@ def test_bidup_host_side_validation(gq):
     assert call(r=65, A=p(256), B=p(256)) == -1
     assert call(H=p(260)) == -1         # H 16-byte aligned
     assert call(ws_bytes=ws - 1) == -7
+
+
+def test_rtn_host_side_validation(gq):
+    p = ctypes.c_void_p
+    f = gq.lib.gptq_quantize_rtn
+    assert f(p(256), 8, 64, 9, 64, p(256), None, p(256), p(256), None) == -3   # bits > 8
+    assert f(p(256), 8, 64, 1, 64, p(256), None, p(256), p(256), None) == -3   # bits < 2
+    assert f(p(256), 8, 64, 4, 48, p(256), None, p(256), p(256), None) == -1   # ncols % group
+    assert f(None, 8, 64, 4, 64, p(256), None, p(256), p(256), None) == -1
