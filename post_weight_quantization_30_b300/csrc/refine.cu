@@ -12,7 +12,7 @@
 //
 // Layout of the sweep (the same blocking as the GPTQ sweep):
 //   G = (T - Ŵ) H                      3xTF32 GEMM
-//   for each 128-column block:         bidup_block_kernel, one warp per 32 rows:
+//   for each 128-column block:         bidup_block_kernel, one warp per 8 rows:
 //                                      the block's g, codes and moves in shared
 //                                      memory, the diagonal block of H too;
 //                                      later columns of the block updated at once
@@ -24,8 +24,8 @@ namespace gq {
 namespace {
 
 constexpr int BU_B = 128;   // columns per block
-constexpr int BU_R = 32;    // rows per CTA (one warp, lane = row)
-constexpr int BU_LD = 33;   // row stride of the transposed tiles (column-major in shared memory)
+constexpr int BU_R = 8;     // rows per CTA (one warp, four lanes per row)
+constexpr int BU_LD = 9;    // row stride of the transposed tiles (column-major in shared memory)
 constexpr size_t BU_SMEM = (size_t)BU_B * BU_B * 4 + 2 * (size_t)BU_B * BU_LD * 4 + (size_t)BU_B * BU_LD;
 
 __device__ __forceinline__ uint32_t field_at(const int32_t *__restrict__ p, int64_t bit, int b) {
@@ -65,45 +65,59 @@ __global__ void bidup_residual_kernel(const float *__restrict__ T, const uint8_t
     }
 }
 
-// One 128-column block of the sweep for 32 rows.  g (current gradient), codes
-// and the moves d are kept column-major in shared memory so that lane = row
-// reads its own entries without bank conflicts; the block's diagonal part of H
-// is shared by all lanes (broadcast reads).  Writes back the codes, Ŵ and the
-// TF32 split of d for the block's columns (d = 0 where the code did not move).
-__global__ void __launch_bounds__(BU_R) bidup_block_kernel(const float *__restrict__ H, int64_t cols,
-                                                           const float *__restrict__ G, uint8_t *__restrict__ codes,
-                                                           const float *__restrict__ scales,
-                                                           const int32_t *__restrict__ qzeros, int bits, int group,
-                                                           int64_t rows, int64_t c0, int bw, float *__restrict__ W_hat,
-                                                           float *__restrict__ Dhi, float *__restrict__ Dlo,
-                                                           unsigned long long *__restrict__ changed) {
+// One 128-column block of the sweep for 8 rows: a warp, four lanes per row,
+// lane part p owning the block's columns [32 p, 32 p + 32) of its row's gradient
+// g (so a move updates at most 32 later columns per lane).  At column j the
+// owning lane broadcasts g_j to the row's four lanes, which all take the same
+// decision.  g, codes and moves are kept column-major in shared memory; the
+// block's diagonal part of H is shared by all lanes (broadcast reads).  Writes
+// back the codes, Ŵ and the TF32 split of the moves d for the block's columns
+// (d = 0 where the code did not move).
+__global__ void __launch_bounds__(32) bidup_block_kernel(const float *__restrict__ H, int64_t cols,
+                                                         const float *__restrict__ G, uint8_t *__restrict__ codes,
+                                                         const float *__restrict__ scales,
+                                                         const int32_t *__restrict__ qzeros, int bits, int group,
+                                                         int64_t rows, int64_t c0, int bw, float *__restrict__ W_hat,
+                                                         float *__restrict__ Dhi, float *__restrict__ Dlo,
+                                                         unsigned long long *__restrict__ changed) {
     extern __shared__ __align__(16) float bsm[];
     float *Hb = bsm;                          // [bw][BU_B]
-    float *Gs = Hb + BU_B * BU_B;             // [bw][BU_LD], column j of the block, lane = row
+    float *Gs = Hb + BU_B * BU_B;             // [bw][BU_LD]: column j, row rl at j * BU_LD + rl
     float *Ds = Gs + BU_B * BU_LD;            // [bw][BU_LD]
     uint8_t *Cs = (uint8_t *)(Ds + BU_B * BU_LD);  // [bw][BU_LD]
     const int lane = threadIdx.x;
+    const int rl = lane >> 2, part = lane & 3;  // row within the CTA, column quarter
     const int64_t r0 = (int64_t)blockIdx.x * BU_R;
-    const int64_t row = r0 + lane;
+    const int64_t row = r0 + rl;
     const bool valid = row < rows;
     const int maxq = (1 << bits) - 1;
     const int64_t zwords = rows * bits / 32;
 
-    for (int idx = lane; idx < bw * bw; idx += BU_R) {
-        const int j = idx / bw, k = idx - j * bw;
-        Hb[j * BU_B + k] = H[(c0 + j) * cols + c0 + k];
+    // The diagonal block of H by asynchronous 16-byte copies, all in flight at once
+    // (H is 16-byte aligned, cols and c0 multiples of 32; bw a multiple of 32).
+    const int q4 = bw / 4;  // 16-byte chunks per row of the block
+    for (int idx = lane; idx < bw * q4; idx += 32) {
+        const int j = idx / q4, k4 = idx - j * q4;
+        const float *src = H + (c0 + j) * cols + c0 + k4 * 4;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(Hb + j * BU_B + k4 * 4)),
+                     "l"(src)
+                     : "memory");
     }
-    for (int idx = lane; idx < BU_R * bw; idx += BU_R) {  // coalesced along the row
-        const int rl = idx / bw, j = idx - rl * bw;
-        const bool v = r0 + rl < rows;
-        Gs[j * BU_LD + rl] = v ? G[(r0 + rl) * cols + c0 + j] : 0.f;
-        Cs[j * BU_LD + rl] = v ? codes[(r0 + rl) * cols + c0 + j] : 0;
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    for (int idx = lane; idx < BU_R * bw; idx += 32) {  // coalesced along the row
+        const int r = idx / bw, j = idx - r * bw;
+        const bool v = r0 + r < rows;
+        Gs[j * BU_LD + r] = v ? G[(r0 + r) * cols + c0 + j] : 0.f;
+        Cs[j * BU_LD + r] = v ? codes[(r0 + r) * cols + c0 + j] : 0;
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncwarp();
 
     unsigned moved_count = 0;
     int64_t gcur = -1;
     float s = 1.f, zf = 0.f;
+    const int k_lo = part * 32, k_hi = (k_lo + 32) < bw ? (k_lo + 32) : bw;
     for (int j = 0; j < bw; ++j) {
         const int64_t g = (c0 + j) / group;
         if (g != gcur) {
@@ -111,38 +125,43 @@ __global__ void __launch_bounds__(BU_R) bidup_block_kernel(const float *__restri
             s = valid ? scales[g * rows + row] : 1.f;
             zf = valid ? (float)field_at(qzeros + g * zwords, row * bits, bits) : 0.f;
         }
-        const int q = Cs[j * BU_LD + lane];
+        const int owner = (rl << 2) | (j >> 5);
+        const float gj = __shfl_sync(0xffffffffu, Gs[j * BU_LD + rl], owner);
+        const int q = Cs[j * BU_LD + rl];
         const float hjj = Hb[j * BU_B + j];
         int qn = q;
         if (valid && hjj > 0.f) {
-            float u = rintf(Gs[j * BU_LD + lane] / (hjj * s));
+            float u = rintf(gj / (hjj * s));
             u = fminf(fmaxf(u, (float)-maxq), (float)maxq);  // finite and small before the integer step
             qn = q + (int)u;
             qn = qn < 0 ? 0 : (qn > maxq ? maxq : qn);
         }
         const bool moved = qn != q;
-        const float wq = s * ((float)q - zf);
-        const float wn = s * ((float)qn - zf);
-        const float d = moved ? wn - wq : 0.f;
-        Ds[j * BU_LD + lane] = d;
-        Cs[j * BU_LD + lane] = (uint8_t)qn;
-        moved_count += moved;
+        const float d = moved ? s * ((float)qn - zf) - s * ((float)q - zf) : 0.f;
+        __syncwarp();  // every lane has read Cs[j] before the owner rewrites it
+        if (lane == owner) {
+            Ds[j * BU_LD + rl] = d;
+            Cs[j * BU_LD + rl] = (uint8_t)qn;
+            moved_count += moved;
+        }
         if (__any_sync(0xffffffffu, moved)) {
             const float *hr = Hb + j * BU_B;
-            for (int k = j + 1; k < bw; ++k) Gs[k * BU_LD + lane] = fmaf(-d, hr[k], Gs[k * BU_LD + lane]);
+            const int kb = (j + 1) > k_lo ? (j + 1) : k_lo;
+#pragma unroll 8
+            for (int k = kb; k < k_hi; ++k) Gs[k * BU_LD + rl] = fmaf(-d, hr[k], Gs[k * BU_LD + rl]);
         }
     }
     __syncwarp();
-    for (int idx = lane; idx < BU_R * bw; idx += BU_R) {
-        const int rl = idx / bw, j = idx - rl * bw;
-        const int64_t rr = r0 + rl;
+    for (int idx = lane; idx < BU_R * bw; idx += 32) {
+        const int r = idx / bw, j = idx - r * bw;
+        const int64_t rr = r0 + r;
         if (rr >= rows) continue;
         const int64_t o = rr * cols + c0 + j;
         const int64_t g = (c0 + j) / group;
-        const uint8_t q = Cs[j * BU_LD + rl];
+        const uint8_t q = Cs[j * BU_LD + r];
         codes[o] = q;
         W_hat[o] = scales[g * rows + rr] * ((float)q - (float)field_at(qzeros + g * zwords, rr * bits, bits));
-        const float d = Ds[j * BU_LD + rl];
+        const float d = Ds[j * BU_LD + r];
         const float h = tf32_hi(d);
         Dhi[o] = h;
         Dlo[o] = d - h;
@@ -175,7 +194,7 @@ cudaError_t bidup_range(const BidupCtx &c, int64_t a, int64_t b) {
     if (b - a == 1) {
         const int64_t c0 = a * BU_B;
         const int bw = (int)((c.cols - c0) < BU_B ? (c.cols - c0) : BU_B);
-        bidup_block_kernel<<<(unsigned)((c.rows + BU_R - 1) / BU_R), BU_R, BU_SMEM, c.s>>>(
+        bidup_block_kernel<<<(unsigned)((c.rows + BU_R - 1) / BU_R), 32, BU_SMEM, c.s>>>(
             c.H, c.cols, c.G, c.codes, c.scales, c.qzeros, c.bits, c.group, c.rows, c0, bw, c.W_hat, c.Dhi, c.Dlo,
             c.changed);
         count_launch();
