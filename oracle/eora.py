@@ -10,7 +10,7 @@
   ``X~ X~^T = Q Λ Q^T`` (our ``H``, cols x cols), ``ΔW' = ΔW Q'``, truncates the
   SVD of ΔW' and projects the result back to the original space.
 
-Readings (listed in DESIGN.md):
+Readings of points the pages leave open:
 
 * ``Q' = Q sqrt(Λ)``.  The page prints ``Q' = QΛ``, but states that the
   projection makes the truncation minimise the layer loss rather than the raw

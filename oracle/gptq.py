@@ -19,7 +19,7 @@ What it computes, and from where:
   consecutive input columns of each row ([LowBit] section 1; [GPTQ-wiki]
   "Enfoque Técnico": per-group scale factors).
 
-Readings of points the pages leave open (each is listed in the design doc):
+Readings of points the pages leave open:
 
 * H is the literal ``2 X^T X`` (no 1/N).  Codes do not depend on the scale of
   H because the damping is relative to ``mean(diag H)``.

@@ -16,7 +16,7 @@ it.
 * Then X~ [Q, R]^T = X Q^T + X L R^T, i.e. W ~ Q + R L^T: a LoRA pair with
   B = R and A = L^T.
 
-Readings (listed in DESIGN.md):
+Readings of points the pages leave open:
 
 * The Hessian is damped like GPTQ's, H~ + damp * mean(diag H~) * I, which
   makes it positive definite for damp > 0, and factored by the same Cholesky

@@ -19,7 +19,7 @@ over part of the variables, so the objective never increases:
   q' = clamp(q + rint(g_j / (H_jj s)), 0, 2^b - 1).  One sweep takes the
   columns in order (Gauss-Seidel), updating r and g after every change.
 
-Readings (listed in DESIGN.md):
+Readings of points the pages leave open:
 
 * H is used undamped (as EoRA uses it); it must be positive definite for OLrC.
 * The integer decision rint(g_j / (H_jj s)) is taken in float32 from the
