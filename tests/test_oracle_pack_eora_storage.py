@@ -147,3 +147,37 @@ def test_qwen3_14b_adapter_overhead():
     for r, mb in ((32, 257), (64, 514)):
         p = storage.adapter_params(layer * 40, r)
         assert abs(p * 2 / 1e6 - mb) < 1.0
+
+
+def _golden_layer_storage():
+    rows = []
+    with open(os.path.join(GOLDEN, "layer_storage_4096x4096_g128.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            rows.append(tuple(int(p) for p in line.split("|")))
+    return rows
+
+
+@pytest.mark.parametrize("case", _golden_layer_storage(), ids=lambda c: f"{c[0]}bit")
+def test_layer_storage_hand_computed(case):
+    """Weights + per-group scale and zero point of a 4096 x 4096 layer in groups of 128."""
+    bits, w_bytes, s_bytes, z_bytes, meta, total = case
+    assert storage.weight_bytes(4096 * 4096, bits) == w_bytes
+    assert storage.group_metadata_bytes(4096, 4096, 128, bits) == meta == s_bytes + z_bytes
+    assert storage.quantized_layer_bytes(4096, 4096, bits, 128) == total == w_bytes + meta
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_layer_storage_equals_packed_arrays(bits):
+    """The accounting equals the bytes of the arrays the packing produces (qweight, qzeros)
+    plus float32 scales, on a small layer."""
+    rows, cols, group = 64, 512, 128
+    rng = np.random.default_rng(bits)
+    codes = rng.integers(0, 2 ** bits, (rows, cols)).astype(np.uint8)
+    zeros = rng.integers(0, 2 ** bits, (cols // group, rows)).astype(np.uint8)
+    scales = np.ones((cols // group, rows), dtype=np.float32)
+    qw, qz = pack.pack_qweight(codes, bits), pack.pack_qzeros(zeros, bits)
+    assert storage.weight_bytes(rows * cols, bits) == qw.nbytes
+    assert storage.group_metadata_bytes(rows, cols, group, bits) == scales.nbytes + qz.nbytes
+    assert storage.quantized_layer_bytes(rows, cols, bits, group) == qw.nbytes + scales.nbytes + qz.nbytes
