@@ -350,6 +350,8 @@ gq_status gptq_quantize_rtn(const float *M, int64_t nrows, int64_t ncols, int bi
  *   Size limit: gptq_quantize_layer_workspace_size(rows, cols, block) must be
  *   <= GQ_NOALLOC_SCRATCH_BYTES (e.g. rows = cols = 768, block = 128 fits);
  *   larger layers are rejected with GQ_EWORKSPACE before anything is enqueued.
+ *   Arguments are checked first, in gptq_quantize_layer's order, so a bad
+ *   argument returns the status gptq_quantize_layer gives it at any size.
  *   All buffers must live on the current CUDA device, and `stream` must belong
  *   to it.  The first call on a device looks up the scratch's device address
  *   (cudaGetSymbolAddress); make that first call before any stream capture.

@@ -109,6 +109,14 @@ def _need_cuda(*ts):
             raise ValueError("tensors must be CUDA device tensors")
 
 
+def _same_device(*ts):
+    """The one device every given tensor lives on; ValueError if they differ."""
+    devs = {t.device for t in ts if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"tensors must all live on one device, got {sorted(str(d) for d in devs)}")
+    return devs.pop()
+
+
 def _workspace(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
@@ -208,12 +216,15 @@ def gptq_quantize_layer_noalloc(W: torch.Tensor, H: torch.Tensor, bits: int, gro
                          f"holds {NOALLOC_SCRATCH_BYTES}: use gptq_quantize_layer with a workspace")
     W = W.contiguous()
     o = out if out is not None else _sweep_outputs(rows, cols, bits, group, W.device, codes, W_hat, row_err)
+    # The library takes the scratch of the current device: make W's device current for the call.
+    dev = _same_device(W, H, *o.values())
     info = _i64(-1)
-    _check(lib.gptq_quantize_layer_noalloc(_ptr(W), _dtype_code(W), rows, cols, _ptr(H.contiguous()), bits, group,
-                                           block, float(damp), _ptr(o["qweight"]), _ptr(o["scales"]),
-                                           _ptr(o["qzeros"]), _ptr(o.get("codes")), _ptr(o.get("W_hat")),
-                                           _ptr(o.get("row_err")), _stream(W.device), ctypes.byref(info)),
-           "gptq_quantize_layer_noalloc", info.value)
+    with torch.cuda.device(dev):
+        _check(lib.gptq_quantize_layer_noalloc(_ptr(W), _dtype_code(W), rows, cols, _ptr(H.contiguous()), bits,
+                                               group, block, float(damp), _ptr(o["qweight"]), _ptr(o["scales"]),
+                                               _ptr(o["qzeros"]), _ptr(o.get("codes")), _ptr(o.get("W_hat")),
+                                               _ptr(o.get("row_err")), _stream(dev), ctypes.byref(info)),
+               "gptq_quantize_layer_noalloc", info.value)
     return o
 
 

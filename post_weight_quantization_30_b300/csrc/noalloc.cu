@@ -50,8 +50,15 @@ extern "C" gq_status gptq_quantize_layer_noalloc(const void *W, gq_dtype wt, int
                                                  int32_t *qweight, float *scales, int32_t *qzeros, uint8_t *codes,
                                                  float *W_hat, float *row_err, gq_stream_t stream, int64_t *info) {
     const size_t need = gptq_quantize_layer_workspace_size(rows, cols, block);
-    if (need == 0) return GQ_EINVAL;
-    if (need > kNoAllocScratchBytes) return GQ_EWORKSPACE;  // layer too large for the fixed scratch
+    if (need == 0 || need > kNoAllocScratchBytes) {
+        // Invalid sizes, or a layer too large for the fixed scratch.  Called with no
+        // workspace, gptq_quantize_layer runs its own argument checks in its own
+        // order and, when they pass, returns GQ_EWORKSPACE; it enqueues nothing
+        // either way.  So a bad argument gets the status gptq_quantize_layer
+        // would give it, whatever the layer's size.
+        return gptq_quantize_layer(W, wt, rows, cols, H, bits, group, block, damp, qweight, scales, qzeros, codes,
+                                   W_hat, row_err, nullptr, 0, stream, info);
+    }
     void *ws = scratch_on_current_device();
     if (!ws) return GQ_ECUDA;
     // The wrapped call clears every part of the scratch that must start at zero

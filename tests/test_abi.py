@@ -167,3 +167,34 @@ def test_rtn_host_side_validation(gq):
     assert f(p(256), 8, 64, 1, 64, p(256), None, p(256), p(256), None) == -3   # bits < 2
     assert f(p(256), 8, 64, 4, 48, p(256), None, p(256), p(256), None) == -1   # ncols % group
     assert f(None, 8, 64, 4, 64, p(256), None, p(256), p(256), None) == -1
+
+
+def test_noalloc_checks_arguments_before_the_size_limit(gq):
+    """An oversized layer with a bad argument gets the status gptq_quantize_layer gives that
+    argument; only a valid oversized layer gets GQ_EWORKSPACE.  Nothing reaches the GPU."""
+    p = ctypes.c_void_p
+    rows = cols = 4096  # workspace far above the 16 MiB scratch
+    assert gq.lib.gptq_quantize_layer_workspace_size(rows, cols, 128) > gq._lib.NOALLOC_SCRATCH_BYTES
+
+    def call(bits=4, group=128, qweight=256, H=256):
+        info = ctypes.c_int64(-1)
+        return gq.lib.gptq_quantize_layer_noalloc(p(256), 1, rows, cols, p(H), bits, group, 128, 0.01, p(qweight),
+                                                  p(256), p(256), None, None, None, None, ctypes.byref(info))
+
+    assert call(bits=5) == -3           # GQ_EUNSUPPORTED
+    assert call(group=100) == -1        # GQ_EINVAL
+    assert call(qweight=0) == -1        # GQ_EINVAL: NULL output
+    assert call(H=0) == -1              # GQ_EINVAL: NULL H
+    assert call() == -7                 # GQ_EWORKSPACE: valid, but larger than the scratch
+    info = ctypes.c_int64(-1)
+    assert gq.lib.gptq_quantize_layer_noalloc(p(256), 1, 0, cols, p(256), 4, 128, 128, 0.01, p(256), p(256),
+                                              p(256), None, None, None, None, ctypes.byref(info)) == -1
+
+
+def test_binding_rejects_tensors_on_different_devices(gq):
+    import torch
+
+    a = torch.empty(4)
+    assert gq._lib._same_device(a, None, torch.empty(2)) == a.device
+    with pytest.raises(ValueError):
+        gq._lib._same_device(a, torch.empty(4, device="meta"))
