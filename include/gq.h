@@ -16,7 +16,14 @@
  * are returned as GQ_EINVAL / GQ_EUNSUPPORTED / GQ_EWORKSPACE.  A launch error is
  * returned as GQ_ECUDA.  Calls that factor H synchronize `stream` once, after the
  * factorization, to read the device status word; they return GQ_ENOTPD with
- * *info = the first input column whose pivot was not positive.  On any non-OK
+ * *info = the first input column whose pivot was not positive.  The same
+ * synchronization reports an Inf or NaN in the inputs they read: GQ_ENONFINITE
+ * with *info = 0 when it is in H (the diagonal and upper triangle, the part the
+ * factor reads) and *info = 1 when it is in W (or EoRA's dW).  A non-finite
+ * calibration token makes H non-finite, so it is reported as *info = 0 by the
+ * first factoring call after gptq_hessian_accumulate; the asynchronous calls
+ * (gptq_hessian_accumulate, gptq_sweep, the packed and Bid-Up calls) do not
+ * check.  GQ_ENONFINITE takes precedence over GQ_ENOTPD.  On any non-OK
  * return the contents of the outputs are unspecified.
  *
  * Pages the operations follow (cited by title and section):
@@ -47,7 +54,7 @@ typedef enum {
     GQ_ENOTPD = -2,       /* damped H not positive definite; *info = column */
     GQ_EUNSUPPORTED = -3, /* bits not in {2,3,4}, unknown dtype */
     GQ_ECUDA = -4,        /* CUDA runtime / launch error */
-    GQ_ENONFINITE = -5,   /* non-finite value found in an input */
+    GQ_ENONFINITE = -5,   /* Inf or NaN in an input; *info = 0 (H) or 1 (W / dW) */
     GQ_ETIMEOUT = -6,     /* a bounded device-side wait gave up */
     GQ_EWORKSPACE = -7    /* workspace missing, too small or not 256-byte aligned */
 } gq_status;
@@ -70,6 +77,18 @@ const char *gq_status_string(gq_status s);
  * affected outputs are then invalid) and clears that record.  GQ_OK otherwise.
  */
 gq_status gq_check_device(gq_stream_t stream);
+
+/*
+ * Sets, on the current device, the budget in SM clock cycles of each bounded
+ * wait in the pipelines of the tensor-core kernels (Hessian, 3xTF32 GEMM,
+ * packed linear); cycles <= 0 restores the default of 4e9 cycles (about 2 s).
+ * A wait that runs out records the failure for gq_check_device (GQ_ETIMEOUT)
+ * and the kernel ends early: it still waits, with the default budget, for the
+ * copies and MMAs it has issued, frees its tensor memory and returns.  For
+ * tests of that failure path: a tiny budget makes ordinary waits run out.
+ * Synchronous; call it with no library work in flight.
+ */
+gq_status gq_set_wait_budget(long long cycles);
 
 /*
  * H += 2 X^T X.

@@ -40,6 +40,7 @@ SIGNATURES = {
     "gq_kernel_launches": (ctypes.c_ulonglong, []),
     "gq_status_string": (ctypes.c_char_p, [_i]),
     "gq_check_device": (_i, [_p]),
+    "gq_set_wait_budget": (_i, [ctypes.c_longlong]),
     "gptq_hessian_accumulate": (_i, [_p, _i64, _p, _i, _i64, _i64, _p]),
     "gptq_factor_workspace_size": (_sz, [_i64]),
     "gptq_factor": (_i, [_p, _i64, _f, _p, _p, _p, _sz, _p, ctypes.POINTER(_i64)]),

@@ -99,20 +99,28 @@ cudaError_t sweep_range(const SweepCtx &c, int64_t a, int64_t b) {
 }
 
 // Dead inputs + damping, blocked Cholesky of the reversed matrix, reversal;
-// one synchronization to read the pivot status.
+// one synchronization to read the status.  The part of H the factor reads is
+// checked for Inf / NaN, and so are the `wn` values of Wchk (the layer's
+// weights) when given: GQ_ENONFINITE with *info = 0 (H) or 1 (W).
 gq_status factor_impl(const float *H, int64_t cols, float damp, float *F, uint8_t *dead, void *ws, cudaStream_t s,
-                      int64_t *info, float *Uinv, int block) {
+                      int64_t *info, float *Uinv, int block, const void *Wchk = nullptr, bool w_bf16 = false,
+                      int64_t wn = 0) {
     DeviceStatus *st = (DeviceStatus *)ws;
     float *scratch = (float *)((char *)ws + align_up(sizeof(DeviceStatus)));
     GQ_CUDA_TRY(cudaMemsetAsync(st, 0xFF, sizeof(DeviceStatus), s));
+    if (Wchk) GQ_CUDA_TRY(finite_check_launch(Wchk, w_bf16, wn, st, kNonFiniteW, s));
     GQ_CUDA_TRY(factor_prepare(H, cols, damp, F, dead, st, s));
     GQ_CUDA_TRY(cholesky_lower_inplace(F, cols, st, scratch, s, Uinv, block));
     GQ_CUDA_TRY(factor_finalize(F, cols, s));
-    unsigned long long bad = 0;
-    GQ_CUDA_TRY(cudaMemcpyAsync(&bad, &st->bad_pivot, sizeof(bad), cudaMemcpyDeviceToHost, s));
+    DeviceStatus hst;
+    GQ_CUDA_TRY(cudaMemcpyAsync(&hst, st, sizeof(hst), cudaMemcpyDeviceToHost, s));
     GQ_CUDA_TRY(cudaStreamSynchronize(s));
-    if (bad != ULLONG_MAX) {
-        if (info) *info = cols - 1 - (int64_t)bad;
+    if (hst.finite != ~0u) {
+        if (info) *info = (hst.finite & kNonFiniteH) ? 1 : 0;
+        return GQ_ENONFINITE;
+    }
+    if (hst.bad_pivot != ULLONG_MAX) {
+        if (info) *info = cols - 1 - (int64_t)hst.bad_pivot;
         return GQ_ENOTPD;
     }
     if (info) *info = -1;
@@ -239,7 +247,8 @@ gq_status intrinsic_impl(const void *W, gq_dtype wt, int64_t rows, int64_t cols,
     GQ_CUDA_TRY(cudaMemcpyAsync(&bad_c, &w.cst->bad_pivot, sizeof(bad_c), cudaMemcpyDeviceToHost, s));
     // GPTQ on S: the factorization synchronizes the stream, after which bad_c is valid.
     const bool uinv = factor_emits_uinv(cols, block);
-    gq_status st = factor_impl(S, cols, 0.f, w.F, w.deadS, w.fws, s, info, uinv ? g.Uinv : nullptr, block);
+    gq_status st = factor_impl(S, cols, 0.f, w.F, w.deadS, w.fws, s, info, uinv ? g.Uinv : nullptr, block, W,
+                               wt == GQ_BF16, rows * cols);
     if (bad_c != ULLONG_MAX) {
         if (info) *info = cols + (int64_t)bad_c;
         return GQ_ENOTPD;
@@ -284,6 +293,14 @@ gq_status gq_check_device(gq_stream_t stream) {
     const unsigned int e3 = packed_read_and_clear_error();
     if (e1 == ~0u || e2 == ~0u || e3 == ~0u) return GQ_ECUDA;
     return (e1 | e2 | e3) ? GQ_ETIMEOUT : GQ_OK;
+}
+
+gq_status gq_set_wait_budget(long long cycles) {
+    const long long c = cycles > 0 ? cycles : 4000000000LL;
+    if (hessian_set_wait_budget(c) != cudaSuccess || gemm_set_wait_budget(c) != cudaSuccess ||
+        packed_set_wait_budget(c) != cudaSuccess)
+        return GQ_ECUDA;
+    return GQ_OK;
 }
 
 gq_status gptq_hessian_accumulate(float *H, int64_t cols, const void *X, gq_dtype xt, int64_t n, int64_t ldx,
@@ -360,7 +377,8 @@ gq_status gptq_quantize_layer(const void *W, gq_dtype wt, int64_t rows, int64_t 
     // The sweep workspace starts with its block-inverse region, which the
     // factorization fills directly when its panels coincide with the blocks.
     const bool uinv = factor_emits_uinv(cols, block);
-    st = factor_impl(H, cols, damp, F, dead, fws, cs(stream), info, uinv ? (float *)p : nullptr, block);
+    st = factor_impl(H, cols, damp, F, dead, fws, cs(stream), info, uinv ? (float *)p : nullptr, block, W,
+                     wt == GQ_BF16, rows * cols);
     if (st != GQ_OK) return st;
     return sweep_impl(W, wt, rows, cols, F, dead, bits, group, block, qweight, scales, qzeros, codes, W_hat, row_err, p,
                       cs(stream), uinv);
@@ -480,7 +498,12 @@ gq_status eora_compensate(const float *dW, int64_t rows, int64_t cols, const flo
     if (r <= 0 || r > 64 || r > rows || r > cols) return GQ_EINVAL;
     if (!ws || !aligned(ws, kAlign) || ws_bytes < eora_workspace_bytes(rows, cols, r)) return GQ_EWORKSPACE;
     unsigned long long bad = ULLONG_MAX;
-    if (eora_run(dW, rows, cols, H, r, A, B, sigma, ws, cs(stream), &bad) != cudaSuccess) return GQ_ECUDA;
+    unsigned int finite = ~0u;
+    if (eora_run(dW, rows, cols, H, r, A, B, sigma, ws, cs(stream), &bad, &finite) != cudaSuccess) return GQ_ECUDA;
+    if (finite != ~0u) {
+        if (info) *info = (finite & kNonFiniteH) ? 1 : 0;
+        return GQ_ENONFINITE;
+    }
     if (bad != ULLONG_MAX) {
         if (info) *info = cols - 1 - (int64_t)bad;
         return GQ_ENOTPD;

@@ -23,15 +23,19 @@ namespace gq {
 // Counts one kernel launch enqueued by the library (host side).
 void count_launch();
 
-// Device status block kept in the workspace.  `bad_pivot` holds the first input
-// column (in original index order) whose Cholesky pivot was not positive, or
-// INT64_MAX when every pivot was fine.
+// Device status block kept in the workspace (set to all one bits before use).
+// `bad_pivot` holds the first input column (in original index order) whose
+// Cholesky pivot was not positive, or all ones when every pivot was fine.
+// `finite` keeps all its bits while the inputs are finite: bit 0 is cleared
+// when the part of H the factor reads holds an Inf or NaN, bit 1 when W (or
+// EoRA's dW) does.
 struct DeviceStatus {
     unsigned long long bad_pivot;
     double diag_sum;
     float delta;
-    int pad;
+    unsigned int finite;
 };
+constexpr unsigned int kNonFiniteH = 1u, kNonFiniteW = 2u;
 
 static constexpr size_t kAlign = 256;
 
@@ -124,6 +128,11 @@ bool hessian_bf16_tc_supported(int64_t cols, const void *X, int64_t ldx);
 // could not be read.
 unsigned int read_and_clear_device_error();
 unsigned int gemm_read_and_clear_error();
+// Cycle budget of the bounded pipeline waits of the Hessian, GEMM and packed
+// kernels (each source file holds its own copy), on the current device.
+cudaError_t hessian_set_wait_budget(long long cycles);
+cudaError_t gemm_set_wait_budget(long long cycles);
+cudaError_t packed_set_wait_budget(long long cycles);
 
 // Factor pieces.
 // True when cholesky_lower_inplace can emit the sweep's block inverses.
@@ -140,6 +149,10 @@ cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, flo
                                    float *Uinv = nullptr, int block = 0);
 cudaError_t factor_finalize(float *F, int64_t cols, cudaStream_t s);
 size_t factor_scratch_bytes(int64_t cols);
+// Clears `bit` of st->finite when any of the n values of X (float32 or bf16)
+// is an Inf or NaN.
+cudaError_t finite_check_launch(const void *X, bool bf16, int64_t n, DeviceStatus *st, unsigned int bit,
+                                cudaStream_t s);
 
 // Sweep pieces.
 cudaError_t block_inverses(const float *F, int64_t cols, int block, float *Uinv, cudaStream_t s);
@@ -180,11 +193,13 @@ cudaError_t sign_normalize(float *X, int nvec, int64_t n, int64_t es, int64_t vs
 
 // EoRA (eora.cu).  eora_run synchronizes `s` once, after the factorization of
 // H, and reports a non-positive pivot through *bad_pivot_host (ULLONG_MAX = none,
-// else the pivot index in reversed order); nothing after that is launched then.
+// else the pivot index in reversed order) and non-finite H / dW through
+// *finite_host (DeviceStatus::finite); nothing after that is launched then.
 size_t eora_workspace_bytes(int64_t rows, int64_t cols, int r);
 int eora_subspace_width(int64_t rows, int64_t cols, int r);
 cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H, int r, float *A, float *B,
-                     float *sigma, void *ws, cudaStream_t s, unsigned long long *bad_pivot_host);
+                     float *sigma, void *ws, cudaStream_t s, unsigned long long *bad_pivot_host,
+                     unsigned int *finite_host);
 
 // GPTQ-intrinsic LoRA (lora.cu).
 size_t lora_basis_workspace_bytes(int64_t cols, int r);

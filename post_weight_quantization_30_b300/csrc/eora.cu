@@ -116,7 +116,8 @@ size_t eora_workspace_bytes(int64_t rows, int64_t cols, int r) {
 }
 
 cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H, int r, float *A, float *B,
-                     float *sigma, void *ws, cudaStream_t s, unsigned long long *bad_pivot_host) {
+                     float *sigma, void *ws, cudaStream_t s, unsigned long long *bad_pivot_host,
+                     unsigned int *finite_host) {
     EoraWs w;
     const size_t main_bytes = eora_layout(rows, cols, r, &w, (char *)ws);
     DeviceStatus *qst = (DeviceStatus *)((char *)ws + main_bytes);
@@ -127,16 +128,18 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     // H = F F^T (no damping); every input must be live.
     if ((e = cudaMemsetAsync(w.st, 0xFF, sizeof(DeviceStatus), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(qst, 0xFF, sizeof(DeviceStatus), s)) != cudaSuccess) return e;
+    if ((e = finite_check_launch(dW, false, rows * cols, w.st, kNonFiniteW, s)) != cudaSuccess) return e;
     if ((e = factor_prepare(H, cols, 0.f, w.F, w.dead, w.st, s)) != cudaSuccess) return e;
     dead_to_pivot_kernel<<<grid1d(cols), 256, 0, s>>>(w.dead, cols, w.st);
     count_launch();
     if ((e = cholesky_lower_inplace(w.F, cols, w.st, w.Linv, s)) != cudaSuccess) return e;
     if ((e = factor_finalize(w.F, cols, s)) != cudaSuccess) return e;
-    if ((e = cudaMemcpyAsync(bad_pivot_host, &w.st->bad_pivot, sizeof(unsigned long long), cudaMemcpyDeviceToHost,
-                             s)) != cudaSuccess)
-        return e;
+    DeviceStatus hst;
+    if ((e = cudaMemcpyAsync(&hst, w.st, sizeof(hst), cudaMemcpyDeviceToHost, s)) != cudaSuccess) return e;
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
-    if (*bad_pivot_host != ULLONG_MAX) return cudaSuccess;
+    *bad_pivot_host = hst.bad_pivot;
+    *finite_host = hst.finite;
+    if (hst.finite != ~0u || hst.bad_pivot != ULLONG_MAX) return cudaSuccess;
 
     if (tc) {
         // M = dW F (rows x cols, also split), its transpose split, G = M^T M (cols x cols, also split).

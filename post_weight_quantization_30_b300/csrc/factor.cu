@@ -49,22 +49,63 @@ __global__ void diag_sum_kernel(const float *__restrict__ H, int64_t cols, float
 }
 
 // F[p][q] = (J H_d J)[p][q] = H_d[C-1-p][C-1-q] for q <= p; 0 above the diagonal.
+// Every entry of H it reads (the upper triangle and the diagonal) is also
+// checked: an Inf or NaN clears kNonFiniteH in st->finite.
 __global__ void reverse_damp_kernel(const float *__restrict__ H, int64_t cols, float *__restrict__ F,
-                                    uint8_t *__restrict__ dead, const DeviceStatus *__restrict__ st) {
+                                    uint8_t *__restrict__ dead, DeviceStatus *__restrict__ st) {
     const int64_t p = blockIdx.y;
     const float delta = st->delta;
+    bool bad = false;
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < cols; q += (int64_t)gridDim.x * blockDim.x) {
         float v = 0.f;
         if (q < p) {
             v = H[(cols - 1 - p) * cols + (cols - 1 - q)];
+            bad |= !isfinite(v);
         } else if (q == p) {
             const int64_t i = cols - 1 - p;
             float d = H[i * cols + i];
+            bad |= !isfinite(d);
             if (dead) dead[i] = (d == 0.f);
             v = ((d == 0.f) ? 1.f : d) + delta;
         }
         F[p * cols + q] = v;
     }
+    if (bad) atomicAnd(&st->finite, ~kNonFiniteH);
+}
+
+// Clears `bit` of st->finite if an element of X is an Inf or NaN (all exponent
+// bits set: 0x7F80 in bf16, 0x7F800000 in float32).  16-byte loads over the
+// aligned middle of the buffer, element loads at both ends.
+__global__ void finite_check_kernel(const unsigned char *__restrict__ X, int64_t nbytes, int esize,
+                                    DeviceStatus *__restrict__ st, unsigned int bit) {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nth = (int64_t)gridDim.x * blockDim.x;
+    const uint32_t m32 = esize == 2 ? 0x7F807F80u : 0x7F800000u;
+    const int64_t head = (int64_t)((16 - ((uintptr_t)X & 15)) & 15) < nbytes ? (int64_t)((16 - ((uintptr_t)X & 15)) & 15)
+                                                                            : nbytes;
+    const int64_t nvec = (nbytes - head) / 16;
+    const int64_t tail0 = head + nvec * 16;
+    auto bad_elem = [&](int64_t off) {
+        if (esize == 2) {
+            const uint16_t u = *reinterpret_cast<const uint16_t *>(X + off);
+            return (u & 0x7F80u) == 0x7F80u;
+        }
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(X + off);
+        return (u & 0x7F800000u) == 0x7F800000u;
+    };
+    auto bad_word = [&](uint32_t u) {
+        if (esize == 2) return ((u & 0x7F80u) == 0x7F80u) || ((u & 0x7F800000u) == 0x7F800000u);
+        return (u & m32) == m32;
+    };
+    bool bad = false;
+    for (int64_t off = tid * esize; off < head; off += nth * esize) bad |= bad_elem(off);
+    const uint4 *v = reinterpret_cast<const uint4 *>(X + head);
+    for (int64_t i = tid; i < nvec; i += nth) {
+        const uint4 w = __ldg(v + i);
+        bad |= bad_word(w.x) | bad_word(w.y) | bad_word(w.z) | bad_word(w.w);
+    }
+    for (int64_t off = tail0 + tid * esize; off < nbytes; off += nth * esize) bad |= bad_elem(off);
+    if (bad) atomicAnd(&st->finite, ~bit);
 }
 
 // Cholesky of the kb x kb diagonal block at (k0, k0) (kb <= NB) in shared
@@ -399,6 +440,19 @@ cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, u
     count_launch();
     dim3 grid((unsigned)((cols + 255) / 256 < 8 ? (cols + 255) / 256 : 8), (unsigned)cols);
     reverse_damp_kernel<<<grid, 256, 0, s>>>(H, cols, F, dead, st);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t finite_check_launch(const void *X, bool bf16, int64_t n, DeviceStatus *st, unsigned int bit,
+                                cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int esize = bf16 ? 2 : 4;
+    const int64_t nbytes = n * esize;
+    int64_t blocks = (nbytes / 16 + 255) / 256;
+    if (blocks > 148 * 8) blocks = 148 * 8;
+    if (blocks < 1) blocks = 1;
+    finite_check_kernel<<<(unsigned)blocks, 256, 0, s>>>((const unsigned char *)X, nbytes, esize, st, bit);
     count_launch();
     return cudaGetLastError();
 }

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
     __shared__ __align__(8) uint64_t empty_bar[G_STAGES];
     __shared__ __align__(8) uint64_t tfull[2];
     __shared__ __align__(8) uint64_t tempty[2];
+    __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 4);
         }
+        mbar_init(&drain_bar, 1);
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -114,7 +116,8 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int kt = 0; kt < ktiles; ++kt) {
+            int issued = 0;
+            for (int kt = 0; kt < ktiles; ++kt, ++issued) {
                 const int s = kt % G_STAGES;
                 const uint32_t ph = (uint32_t)(kt / G_STAGES) & 1u;
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u) || *(volatile int *)&abort_flag) {
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
                     tma_load_2d(st + 2 * TILE_A + TILE_B, &blo, x, n0, &full_bar[s]);
                 }
             }
+            drain_loads<G_STAGES>(full_bar, issued);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -185,6 +189,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
                 atomicOr(&g_gemm_error, 1u);
                 abort_flag = 1;
             }
+            drain_mmas(&drain_bar);
         }
         __syncwarp();
     } else {
@@ -355,6 +360,8 @@ bool make_map(CUtensorMap *map, const float *base, int64_t inner, int64_t outer,
 }
 
 }  // namespace
+
+cudaError_t gemm_set_wait_budget(long long cycles) { return tc::set_wait_budget_here(cycles); }
 
 unsigned int gemm_read_and_clear_error() {
     unsigned int v = 0;

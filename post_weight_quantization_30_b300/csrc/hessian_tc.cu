@@ -19,7 +19,8 @@
 //   the columns) with tcgen05.ld after every 512 tokens, add the partial sums
 //   into float32 registers and finally add 2 * sum into H.
 // * Every wait on an mbarrier is bounded (clock64 budget); on expiry the CTA
-//   records an error flag, drains what it issued, frees TMEM and returns.
+//   records an error flag, waits (again bounded) until the TMA loads and MMAs
+//   it issued have completed, frees TMEM and returns.
 #include "tc_common.cuh"
 
 namespace gq {
@@ -56,6 +57,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
     __shared__ __align__(8) uint64_t tfull[2];
     __shared__ __align__(8) uint64_t tempty[2];
+    __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -100,6 +102,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], EPI_WARPS);
         }
+        mbar_init(&drain_bar, 1);
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -117,7 +120,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int kt = 0; kt < ktiles; ++kt) {
+            int issued = 0;
+            for (int kt = 0; kt < ktiles; ++kt, ++issued) {
                 const int s = kt % STAGES;
                 const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u) || *(volatile int *)&abort_flag) {
@@ -134,6 +138,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
                 for (int b = 0; b < 4; ++b)
                     tma_load_2d(st + A_BYTES + b * BOX_BYTES, &xmap, c0 + 64 * b, y, &full_bar[s]);
             }
+            drain_loads<STAGES>(full_bar, issued);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -176,6 +181,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
                 atomicOr(&g_device_error, 1u);
                 abort_flag = 1;
             }
+            drain_mmas(&drain_bar);
         }
         __syncwarp();
     } else {
@@ -259,6 +265,8 @@ unsigned int read_and_clear_device_error() {
     if (v) cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
     return v;
 }
+
+cudaError_t hessian_set_wait_budget(long long cycles) { return tc::set_wait_budget_here(cycles); }
 
 bool hessian_bf16_tc_supported(int64_t cols, const void *X, int64_t ldx) {
     if (cols < 64 || cols > (1 << 20) || cols % 8) return false;

@@ -186,9 +186,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 
 __device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity) {
     if (mbar_test(bar, parity)) return true;
+    const long long budget = *(volatile long long *)&g_wait_budget;
     const long long t0 = clock64();
     while (!mbar_test(bar, parity)) {
-        if (clock64() - t0 > WAIT_BUDGET) return false;
+        if (clock64() - t0 > budget) return false;
     }
     return true;
 }
@@ -215,6 +216,7 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
     __shared__ __align__(8) uint64_t wempty[W_BUFS];       // the MMA is done with it
     __shared__ __align__(8) uint64_t tfull[2];
     __shared__ __align__(8) uint64_t tempty[2];
+    __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     // Scales of this tile's rows for groups gi (slot gi % 2) and gi + 1, staged by
@@ -238,6 +240,7 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], P_EPI);
         }
+        mbar_init(&drain_bar, 1);
         abort_flag = 0;
         epi_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -257,7 +260,8 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int kt = 0; kt < kt_all; ++kt) {
+            int issued = 0;
+            for (int kt = 0; kt < kt_all; ++kt, ++issued) {
                 const int s = kt % P_STAGES;
                 const uint32_t ph = (uint32_t)(kt / P_STAGES) & 1u;
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u) || *(volatile int *)&abort_flag) {
@@ -276,6 +280,7 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
                     tma_load_2d(smem + s * P_STAGE, a == 2 ? &tlo : &thi, 0, m0, &full_bar[s]);
                 }
             }
+            drain_loads<P_STAGES>(full_bar, issued);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -324,6 +329,7 @@ __global__ void __launch_bounds__(P_NWARPS * 32, 1)
                 atomicOr(&g_packed_error, 1u);
                 abort_flag = 1;
             }
+            drain_mmas(&drain_bar);
         }
         __syncwarp();
     } else if (warp < 2 + P_DEQ) {
@@ -684,6 +690,8 @@ size_t packed_layout(int64_t n, int64_t rows, int64_t cols, int group, int r, Pa
 }
 
 }  // namespace
+
+cudaError_t packed_set_wait_budget(long long cycles) { return tc::set_wait_budget_here(cycles); }
 
 unsigned int packed_read_and_clear_error() {
     unsigned int v = 0;

@@ -12,6 +12,17 @@ namespace tc {
 
 constexpr long long WAIT_BUDGET = 4000000000LL;  // clock cycles (~2 s) before a wait gives up
 
+// Cycle budget of the pipeline waits (mbar_wait).  Each source file that
+// includes this header has its own copy; gq_set_wait_budget sets them all.
+// The drains after an abort always use WAIT_BUDGET: they wait for copies and
+// MMAs that were issued and finish by themselves.
+static __device__ long long g_wait_budget = WAIT_BUDGET;
+
+// Host side: sets this source file's copy of g_wait_budget on the current device.
+static inline cudaError_t set_wait_budget_here(long long cycles) {
+    return cudaMemcpyToSymbol(g_wait_budget, &cycles, sizeof(cycles));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -35,14 +46,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: false if the phase did not complete within the budget.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Bounded wait: false if the phase did not complete within `budget` cycles.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, long long budget) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > WAIT_BUDGET) return false;
+        if (clock64() - t0 > budget) return false;
     }
     return true;
+}
+
+// A pipeline wait, bounded by g_wait_budget.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_for(bar, parity, *(volatile long long *)&g_wait_budget);
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
@@ -104,8 +121,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// End of a producer thread: every TMA load it issued into a STAGES-deep ring
+// has landed.  The `issued` loads went to stage kt % STAGES in phase kt / STAGES;
+// only the last STAGES of them can still be in flight, and no later load went
+// to their stages, so each wait ends when that load lands (at once if it was
+// consumed long ago).  Needed after an abort, before the CTA frees its memory.
+template <int STAGES>
+__device__ __forceinline__ void drain_loads(uint64_t *full_bar, int issued) {
+    for (int kt = issued > STAGES ? issued - STAGES : 0; kt < issued; ++kt)
+        mbar_wait_for(&full_bar[kt % STAGES], (uint32_t)(kt / STAGES) & 1u, WAIT_BUDGET);
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// End of an MMA-issuing thread: one more commit to `drain_bar` (a barrier of
+// count 1 used for nothing else), then a wait for it, so every tcgen05.mma the
+// thread issued has completed before TMEM is freed.
+__device__ __forceinline__ void drain_mmas(uint64_t *drain_bar) {
+    mma_commit(drain_bar);
+    mbar_wait_for(drain_bar, 0u, WAIT_BUDGET);
 }
 
 
