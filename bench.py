@@ -35,7 +35,9 @@ sys.path.insert(0, ROOT)
 from synthetic import LAYERS, generate, generate_rows  # noqa: E402
 
 METRIC = "GPTQ sec per layer (Hessian+Cholesky+sweep+pack) at 1 B300; % of roofline"
-DEFAULT_WORKLOAD = "llama7b_q_proj_4096x4096"
+# The largest single-GPU quantization workload: the widest layer (11008 inputs), the largest X (5.77 GB),
+# Hessian and factor.
+DEFAULT_WORKLOAD = "llama7b_down_proj_4096x11008"
 
 
 def _peaks():
@@ -334,6 +336,13 @@ def run_ours(args, rank: int, world: int):
             acc["eora" if not rc else "refine"] += e[3].elapsed_time(e[4])
     phase = {k: v / reps for k, v in acc.items()}
 
+    # One more untimed step with the library's per-launch CUDA events on (a breakdown by
+    # kernel class: summed time, launches and useful flops each launcher declares).
+    torch.cuda.synchronize(dev)
+    with gq.kernel_timing() as kt:
+        step()
+    torch.cuda.synchronize(dev)
+
     # End to end through the public API from pinned host buffers, every step:
     # H2D of X and W, the whole path, D2H of the packed result.  X arrives in
     # E2E_CHUNKS slices of tokens on a copy stream, and H accumulates each slice
@@ -378,13 +387,16 @@ def run_ours(args, rank: int, world: int):
     flops = float(N) * C * (C + 1)  # symmetric work of H += 2 X^T X
     h_avg_s = statistics.mean(h_ms) / 1e3
     achieved = flops / h_avg_s / 1e12
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    bound, peak_kind = "tensor", f"{peak_kind} bf16 sustained"
+    # The Hessian runs for milliseconds inside a step of tens of milliseconds, at the maximum
+    # clock: the burst peak (a seconds-long loop settles at the sustained one).
+    peak = peaks["bf16_tflops"]
+    bound, peak_kind = "tensor", f"{peak_kind} bf16 dense burst"
     if spec.X.dtype != "bf16":
         # float32 X runs the float32 SIMT product: 148 SMs x 128 FMA/clk x 2 flops x 2.032 GHz.
         bound, peak, peak_kind = "alu", round(148 * 128 * 2 * peaks.get("sm_max_mhz", 2032.0) * 1e6 / 1e12, 1), \
             "float32 FMA issue rate from SM count and maximum clock"
     traffic = _read_traffic(args.workload)
+    rooflines = phase_rooflines(spec, phase, kt, peaks, peak_kind, codes=rc > 0, w_hat=(r or rl) > 0)
 
     result = {
         "metric": METRIC,
@@ -408,19 +420,87 @@ def run_ours(args, rank: int, world: int):
         },
         "phases_ms": {k: round(v, 4) for k, v in phase.items()},
         "roofline": {
-            "kernel": "hessian (H += 2 X^T X)",
+            "kernel": "hessian_tc_kernel (H += 2 X^T X)",
             "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
             "flops_per_launch": flops, "traffic": traffic,
         },
+        "rooflines": rooflines,
+        "kernel_classes": {k: {"ms": round(kt.ms[k], 4), "launches": kt.count[k], "flops": kt.flops[k]}
+                           for k in kt.ms if kt.count[k]},
         "e2e": {"value": round(e2e_s, 6), "unit": "s/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
         "input_generation_s": round(gen_s, 1),
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        result["cpu_baseline"] = cpu_baseline(spec, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = cpu_baseline(spec, **ORACLE_SAMPLE)
     return result
+
+
+def sweep_pack_bytes(spec, codes: bool, w_hat: bool) -> float:
+    """Algorithmic HBM bytes of the sweep + packing: W read once, the packed codes, the per-group
+    scales (float32) and zero points, the diagonal of the factor, and the optional codes (1 byte)
+    and Ŵ (float32) outputs."""
+    R, C, b, g = spec.rows, spec.cols, spec.bits, spec.group
+    wbytes = 2 if spec.W.dtype == "bf16" else 4
+    byt = R * C * wbytes + R * C * b / 8 + (C // g) * R * (4 + b / 8) + C * 4
+    if codes:
+        byt += R * C
+    if w_hat:
+        byt += R * C * 4
+    return float(byt)
+
+
+def phase_rooflines(spec, phase: dict, kt, peaks: dict, peak_kind: str, codes: bool, w_hat: bool) -> dict:
+    """Roofline of each phase of the step and of the 3xTF32 GEMMs as a class.
+
+    * factor: one Cholesky of the cols x cols damped H, cols^3 / 3 useful flops, against the useful
+      float32 rate of 3xTF32 on the tensor cores (the measured bf16 burst x 1/2 for TF32, the nominal
+      dense tf32 : bf16 ratio, x 1/3 for the three TF32 products per useful product);
+    * sweep_pack: the algorithmic bytes of sweep_pack_bytes against the measured HBM copy rate; the
+      phase also runs the in-block updates and the deferred trailing GEMMs, and its floor is the
+      chain of cols dependent column steps, reported as chain_floor_ms = cols x the measured time of
+      one column step of the block kernel;
+    * gemm3: every 3xTF32 GEMM launch of one step, the useful flops they declare over their summed
+      CUDA-event time, against the same 3xTF32 rate.
+    """
+    C = spec.cols
+    tf32x3 = peaks["bf16_tflops"] / 2 / 3
+    tf32_kind = f"{peak_kind} bf16 dense burst x 1/2 (tf32) x 1/3 (three TF32 products per useful product)"
+    out = {}
+    if phase.get("factor"):
+        fl = C ** 3 / 3
+        a = fl / (phase["factor"] / 1e3) / 1e12
+        out["factor"] = {"bound": "tensor", "achieved": round(a, 2), "peak": round(tf32x3, 1), "unit": "TFLOP/s",
+                         "frac": round(a / tf32x3, 4), "peak_kind": tf32_kind, "flops_per_call": fl,
+                         "phase_ms": round(phase["factor"], 4),
+                         "diagonal_block_chain_ms": round(kt.ms["diag"], 4), "diagonal_blocks": kt.count["diag"],
+                         "traffic": None}
+    if phase.get("sweep"):
+        byt = sweep_pack_bytes(spec, codes, w_hat)
+        a = byt / (phase["sweep"] / 1e3) / 1e9
+        n_sw = kt.count["sweep"]
+        t_step_ns = kt.ms["sweep"] * 1e6 / (n_sw * spec.block) if n_sw else None
+        out["sweep_pack"] = {"bound": "hbm", "achieved": round(a, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(a / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} HBM copy",
+                             "bytes_per_call": byt, "phase_ms": round(phase["sweep"], 4),
+                             "block_kernel_ms": round(kt.ms["sweep"], 4), "block_launches": n_sw,
+                             "column_step_ns": round(t_step_ns, 2) if t_step_ns else None,
+                             "chain_floor_ms": round(C * t_step_ns / 1e6, 4) if t_step_ns else None,
+                             "traffic": None}
+    if kt.count["gemm3"]:
+        a = kt.flops["gemm3"] / (kt.ms["gemm3"] / 1e3) / 1e12
+        out["gemm3"] = {"bound": "tensor", "achieved": round(a, 2), "peak": round(tf32x3, 1), "unit": "TFLOP/s",
+                        "frac": round(a / tf32x3, 4), "peak_kind": tf32_kind, "launches": kt.count["gemm3"],
+                        "ms": round(kt.ms["gemm3"], 4), "useful_flops": kt.flops["gemm3"], "traffic": None}
+    if kt.count["hessian"]:
+        a = kt.flops["hessian"] / (kt.ms["hessian"] / 1e3) / 1e12
+        out["hessian"] = {"bound": "tensor", "achieved": round(a, 2), "peak": peaks["bf16_tflops"],
+                          "unit": "TFLOP/s", "frac": round(a / peaks["bf16_tflops"], 4),
+                          "peak_kind": f"{peak_kind} bf16 dense burst", "ms": round(kt.ms["hessian"], 4),
+                          "launches": kt.count["hessian"]}
+    return out
 
 
 def _read_traffic(workload: str):
@@ -595,7 +675,7 @@ def run_packed(args, rank: int, world: int):
         "input_generation_s": round(gen_s, 1),
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        result["cpu_baseline"] = cpu_baseline(spec, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = cpu_baseline(spec, **ORACLE_SAMPLE)
     return result
 
 
@@ -633,11 +713,15 @@ def cpu_baseline_packed(spec) -> dict:
 
 
 # ----------------------------------------------------------------- oracle (CPU)
-def cpu_baseline(spec, budget_s: float = 20.0) -> dict:
+def cpu_baseline(spec, n_s: int = 4096, r_s: int = 16, factor_cols: int | None = None) -> dict:
     """The float64 oracle, as it stands, on a bounded sample of the same layer,
-    extrapolated to seconds per layer: H on a token sample (scaled by N / n_s),
-    the full damping + inverse + Cholesky, the sweep on a sample of rows (scaled
-    by rows / r_s), packing of those rows (scaled likewise)."""
+    extrapolated to seconds per layer: H on n_s tokens (scaled by N / n_s); damping
+    + inverse + Cholesky of the whole cols x cols H, or of its leading
+    factor_cols x factor_cols block scaled by (cols / factor_cols)^3 (the work is
+    cubic); the eager sweep on r_s rows (scaled by rows / r_s, and by
+    (cols / factor_cols)^2 when the sweep runs on the leading block: its work per
+    row is quadratic in cols); packing of those rows (scaled by rows / r_s and
+    cols / factor_cols)."""
     if spec.packed_tokens:
         return cpu_baseline_packed(spec)
     from oracle import gptq as og
@@ -645,12 +729,18 @@ def cpu_baseline(spec, budget_s: float = 20.0) -> dict:
     from synthetic import bf16_bits_to_f32
 
     cores = len(os.sched_getaffinity(0))
-    n_s = 4096 if spec.n >= 4096 else spec.n
-    r_s = 16 if spec.rows >= 16 else spec.rows
-    x = bf16_bits_to_f32(generate_rows(spec.X, 0, n_s, workers=1)) if spec.X.dtype == "bf16" else \
-        generate_rows(spec.X, 0, n_s, workers=1)
-    w = generate_rows(spec.W, 0, r_s, workers=1)
-    w = (bf16_bits_to_f32(w) if spec.W.dtype == "bf16" else w).astype(np.float64)
+    n_s = min(n_s, spec.n)
+    r_s = min(r_s, spec.rows)
+    k = spec.cols if factor_cols is None or spec.lora_rank else min(factor_cols, spec.cols)
+    k -= k % spec.group
+    key = (spec.X, spec.W, n_s, r_s)
+    if key not in _SAMPLES:  # the sampled inputs, generated once per process (not timed)
+        x = bf16_bits_to_f32(generate_rows(spec.X, 0, n_s, workers=1)) if spec.X.dtype == "bf16" else \
+            generate_rows(spec.X, 0, n_s, workers=1)
+        w = generate_rows(spec.W, 0, r_s, workers=1)
+        _SAMPLES.clear()
+        _SAMPLES[key] = (x, (bf16_bits_to_f32(w) if spec.W.dtype == "bf16" else w).astype(np.float64))
+    x, w = _SAMPLES[key]
     t0 = time.perf_counter()
     H = og.hessian(x.astype(np.float64)) * (spec.n / n_s)
     t1 = time.perf_counter()
@@ -665,38 +755,50 @@ def cpu_baseline(spec, budget_s: float = 20.0) -> dict:
         res = il.sweep_partial(np.hstack([w, np.zeros((r_s, spec.lora_rank))]), U, spec.bits, spec.group, spec.cols,
                                dead=dead)
     else:
-        Hd, dead = og.prepare_hessian(H, spec.damp)
+        Hd, dead = og.prepare_hessian(H[:k, :k], spec.damp)
         U = og.inverse_cholesky_upper(Hd)
         t2 = time.perf_counter()
-        res = og.sweep(w, U, spec.bits, spec.group, dead=dead)
+        res = og.sweep(w[:, :k], U, spec.bits, spec.group, dead=dead)
     t3 = time.perf_counter()
     opk.pack_qweight(res["codes"], spec.bits)
     t4 = time.perf_counter()
-    per_layer = (t1 - t0) * (spec.n / n_s) + (t2 - t1) + (t3 - t2) * (spec.rows / r_s) + (t4 - t3) * (spec.rows / r_s)
+    c = spec.cols / k
+    ph = {"hessian": (t1 - t0) * spec.n / n_s, "factor": (t2 - t1) * c ** 3,
+          "sweep": (t3 - t2) * spec.rows / r_s * c ** 2, "pack": (t4 - t3) * spec.rows / r_s * c}
+    per_layer = sum(ph.values())
+    if spec.lora_rank:
+        fac = (f"full float64 eigendecomposition for the rank-{spec.lora_rank} basis, inverse + Cholesky of the "
+               f"augmented {spec.cols + spec.lora_rank}x{spec.cols + spec.lora_rank} Hessian; ")
+    elif k == spec.cols:
+        fac = f"full float64 inverse + Cholesky of {spec.cols}x{spec.cols}; "
+    else:
+        fac = (f"float64 inverse + Cholesky of the leading {k}x{k} block of H (x{c ** 3:.4g}, cubic in cols); "
+               f"the sweep on those {k} columns (x{c ** 2:.4g}, quadratic in cols); ")
     return {
         "value": round(per_layer, 3), "unit": "s/layer", "cores": cores, "kind": "oracle",
-        "sample": f"H on {n_s} of {spec.n} tokens (x{spec.n / n_s:g}); " +
-                  (f"full float64 eigendecomposition for the rank-{spec.lora_rank} basis, inverse + Cholesky of the "
-                   f"augmented {spec.cols + spec.lora_rank}x{spec.cols + spec.lora_rank} Hessian; "
-                   if spec.lora_rank else
-                   f"full float64 inverse + Cholesky of {spec.cols}x{spec.cols}; ") +
+        "sample": f"H on {n_s} of {spec.n} tokens (x{spec.n / n_s:g}); " + fac +
                   f"eager sweep + pack on {r_s} of {spec.rows} rows (x{spec.rows / r_s:g})" +
                   ("; the OLrC + Bid-Up cycles not included" if spec.refine_cycles else
                    "; EoRA not included" if spec.eora_rank else ""),
         "sample_s": round(t4 - t0, 2),
-        "phases_s": {"hessian": round((t1 - t0) * spec.n / n_s, 3), "factor": round(t2 - t1, 3),
-                     "sweep": round((t3 - t2) * spec.rows / r_s, 3), "pack": round((t4 - t3) * spec.rows / r_s, 3)},
+        "phases_s": {k_: round(v, 3) for k_, v in ph.items()},
     }
+
+
+# The sample of the oracle timing, in the bench line's cpu_baseline and in each step of the reference
+# arm: bounded so that the driver's --steps 20 --warmup 5 reference run ends within a few minutes.
+ORACLE_SAMPLE = dict(n_s=4096, r_s=16, factor_cols=4096)
+_SAMPLES = {}
 
 
 def run_reference(args):
     spec = LAYERS[args.workload]
     for _ in range(args.warmup):
-        cpu_baseline(spec)
+        cpu_baseline(spec, **ORACLE_SAMPLE)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(spec))
+        vals.append(cpu_baseline(spec, **ORACLE_SAMPLE))
     wall = time.perf_counter() - t0
     v = statistics.mean(x["value"] for x in vals)
     packed = bool(spec.packed_tokens)
@@ -724,7 +826,6 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(LAYERS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

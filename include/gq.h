@@ -91,6 +91,25 @@ gq_status gq_check_device(gq_stream_t stream);
 gq_status gq_set_wait_budget(long long cycles);
 
 /*
+ * Per-kernel-class timing of this library's launches, for measurement.  After
+ * gq_timing_begin, the launchers of the main kernels bracket every launch with
+ * a pair of CUDA events on the launch's stream (all devices, all streams).
+ * gq_timing_end stops recording, waits for the recorded events and writes,
+ * for kernel class k < nkinds, into the host arrays: ms[k] the summed elapsed
+ * time, flops[k] the summed useful floating-point operations the launches
+ * declared, count[k] the number of launches.  Classes: 0 the Hessian kernel
+ * (n cols (cols + 1) flops per call), 1 the 3xTF32 GEMM (2 M N K useful
+ * float32 flops; only the outputs on and below the diagonal for the
+ * triangular updates), 2 the sweep's block kernel (rows bw (bw - 1) flops of
+ * the in-block updates), 3 the diagonal-block Cholesky + inverse (2 kb^3 / 3),
+ * 4 the one-term TF32 GEMM of the subspace iterations (2 M N K).  Other kernels
+ * are not bracketed.  Recording adds event records between launches: time a
+ * workload without it and use this for the breakdown.
+ */
+gq_status gq_timing_begin(void);
+gq_status gq_timing_end(double *ms, double *flops, unsigned long long *count, int nkinds);
+
+/*
  * H += 2 X^T X.
  *
  * The second-order statistics of the layer inputs: the Hessian of the layer's

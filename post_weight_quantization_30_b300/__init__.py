@@ -24,5 +24,6 @@ from ._lib import (  # noqa: F401
     gptq_unpack,
     gptq_weight_error,
     gq_check_device,
+    kernel_timing,
     lib,
 )

@@ -41,6 +41,8 @@ SIGNATURES = {
     "gq_status_string": (ctypes.c_char_p, [_i]),
     "gq_check_device": (_i, [_p]),
     "gq_set_wait_budget": (_i, [ctypes.c_longlong]),
+    "gq_timing_begin": (_i, []),
+    "gq_timing_end": (_i, [_p, _p, _p, _i]),
     "gptq_hessian_accumulate": (_i, [_p, _i64, _p, _i, _i64, _i64, _p]),
     "gptq_factor_workspace_size": (_sz, [_i64]),
     "gptq_factor": (_i, [_p, _i64, _f, _p, _p, _p, _sz, _p, ctypes.POINTER(_i64)]),
@@ -355,6 +357,31 @@ def gptq_quantize_rtn(M: torch.Tensor, bits: int, group: int | None = None) -> d
     _check(lib.gptq_quantize_rtn(_ptr(M), nrows, ncols, bits, group, _ptr(o["M_hat"]), _ptr(o["codes"]),
                                  _ptr(o["scales"]), _ptr(o["zeros"]), _stream(M.device)), "gptq_quantize_rtn")
     return o
+
+
+TIMING_KINDS = ("hessian", "gemm3", "sweep", "diag", "gemm_tf32")
+
+
+class kernel_timing:
+    """Context manager around gq_timing_begin / gq_timing_end: on exit, ``.ms``,
+    ``.flops`` and ``.count`` map each kernel class of TIMING_KINDS to its summed
+    CUDA-event time, declared useful flops and launch count."""
+
+    def __enter__(self):
+        _check(lib.gq_timing_begin(), "gq_timing_begin")
+        return self
+
+    def __exit__(self, *exc):
+        n = len(TIMING_KINDS)
+        ms, fl = (ctypes.c_double * n)(), (ctypes.c_double * n)()
+        cnt = (ctypes.c_ulonglong * n)()
+        st = lib.gq_timing_end(ctypes.cast(ms, _p), ctypes.cast(fl, _p), ctypes.cast(cnt, _p), n)
+        self.ms = dict(zip(TIMING_KINDS, list(ms)))
+        self.flops = dict(zip(TIMING_KINDS, list(fl)))
+        self.count = dict(zip(TIMING_KINDS, [int(c) for c in cnt]))
+        if exc[0] is None:
+            _check(st, "gq_timing_end")
+        return False
 
 
 def gq_check_device(device=None):

@@ -23,6 +23,15 @@ namespace gq {
 // Counts one kernel launch enqueued by the library (host side).
 void count_launch();
 
+// Kernel classes of the optional per-launch timing (timing.cu; gq_timing_end
+// reports them in this order).
+enum TimedKind { TK_HESSIAN = 0, TK_GEMM3 = 1, TK_SWEEP = 2, TK_DIAG = 3, TK_GEMM_TF32 = 4, TK_COUNT = 5 };
+// While recording is on, timing_begin records an event on `s` before a launch
+// and returns a handle (-1 when off); timing_end records the closing event and
+// the launch's useful floating-point operations.
+int timing_begin(int kind, cudaStream_t s);
+void timing_end(int handle, cudaStream_t s, double flops);
+
 // Device status block kept in the workspace (set to all one bits before use).
 // `bad_pivot` holds the first input column (in original index order) whose
 // Cholesky pivot was not positive, or all ones when every pivot was fine.

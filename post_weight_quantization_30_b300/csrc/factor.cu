@@ -487,9 +487,11 @@ cudaError_t chol_panel(const CholCtx &c, int64_t k0, bool rec, bool p_split_read
     const bool more = k1 < cols;
     const int64_t npanel = (cols + NB - 1) / NB;
     float *ur = c.Uinv ? c.Uinv + (npanel - 1 - k0 / NB) * NB * NB : nullptr;
+    const int th = timing_begin(TK_DIAG, c.s);
     potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, c.s>>>(c.F, cols, k0, kb, c.Linv, c.st, more ? c.Lhi : nullptr,
                                                            c.Llo, ur);
     count_launch();
+    timing_end(th, c.s, 2.0 * kb * kb * kb / 3.0);
     if (!more) return cudaGetLastError();
     const int64_t rest = cols - k1;
     float *P = c.F + k1 * cols + k0;
@@ -576,8 +578,10 @@ cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, flo
                 return e;
         } else {
             float *ur = c.Uinv ? c.Uinv + (npanel - 1 - k0 / NB) * NB * NB : nullptr;
+            const int th = timing_begin(TK_DIAG, s);
             potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, s>>>(F, cols, k0, kb, c.Linv, st, nullptr, nullptr, ur);
             count_launch();
+            timing_end(th, s, 2.0 * kb * kb * kb / 3.0);
             if (k1 >= cols) break;
             const int64_t rest = cols - k1;
             float *P = F + k1 * cols + k0;  // rest x kb panel below the diagonal block

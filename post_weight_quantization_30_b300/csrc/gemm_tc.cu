@@ -391,9 +391,14 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
         return cudaErrorInvalidValue;
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
     const int kt_all = (int)((K + GK - 1) / GK);
+    // Useful products: all M x N outputs, or those on and below the diagonal for tri = 1.
+    const double outs = tri == 1 ? (M >= N ? (double)M * N - (double)N * (N - 1) / 2 : (double)M * (M + 1) / 2)
+                                 : (double)M * N;
+    const int th = timing_begin(TK_GEMM3, s);
     gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta,
                                                     tri, Chi, Clo, ldcs, kt_all, 0, split_row0, split_ncols, 0);
     count_launch();
+    timing_end(th, s, 2.0 * outs * (double)K);
     return cudaGetLastError();
 }
 
@@ -421,9 +426,11 @@ cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, cons
     const int per = (kt_all + slices - 1) / slices;
     const int z = (kt_all + per - 1) / per;
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM), (unsigned)z);
+    const int th = timing_begin(one_term ? TK_GEMM_TF32 : TK_GEMM3, s);
     gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, partials, N, (int)M, (int)N, (int)K, 1.f, 0.f,
                                                     0, nullptr, nullptr, 0, per, M * N, 0, 0, one_term ? 1 : 0);
     count_launch();
+    timing_end(th, s, 2.0 * (double)M * (double)N * (double)K);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return sum_slices(partials, z, M * N, C, s);

@@ -298,8 +298,10 @@ cudaError_t hessian_bf16_tc(float *H, int64_t cols, const __nv_bfloat16 *X, int6
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        const int th = timing_begin(TK_HESSIAN, s);
         hessian_tc_kernel<<<tiles, NWARPS * 32, SMEM_BYTES, s>>>(map, H, (int)cols, (int)nc);
         count_launch();
+        timing_end(th, s, (double)nc * (double)cols * (double)(cols + 1));
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

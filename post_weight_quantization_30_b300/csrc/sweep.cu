@@ -429,9 +429,11 @@ cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, in
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    const int th = timing_begin(TK_SWEEP, s);
     sweep_kernel<BITS, TW><<<(unsigned)((rows + ROWS - 1) / ROWS), NTHREADS, smem, s>>>(
         W, rows, cols, c0, bw, Uinv, F, dead, group, D, DL, qweight, scales, qzeros, codes, W_hat, row_err);
     count_launch();
+    timing_end(th, s, (double)rows * bw * (bw - 1));
     return cudaGetLastError();
 }
 

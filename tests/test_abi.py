@@ -198,3 +198,14 @@ def test_binding_rejects_tensors_on_different_devices(gq):
     assert gq._lib._same_device(a, None, torch.empty(2)) == a.device
     with pytest.raises(ValueError):
         gq._lib._same_device(a, torch.empty(4, device="meta"))
+
+
+def test_kernel_timing_without_launches_reports_zeros(gq):
+    with gq.kernel_timing() as kt:
+        pass
+    assert set(kt.ms) == set(gq._lib.TIMING_KINDS)
+    assert all(v == 0 for v in kt.ms.values()) and all(v == 0 for v in kt.count.values())
+    n = ctypes.c_int(0)
+    assert gq.lib.gq_timing_end(None, None, None, 0) == 0
+    assert gq.lib.gq_timing_end(None, None, None, 3) == -1  # GQ_EINVAL: NULL outputs
+    del n
