@@ -32,7 +32,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import LAYERS, generate, generate_rows  # noqa: E402
+from synthetic import CHUNK_ROWS, LAYERS, generate, generate_rows  # noqa: E402
 
 METRIC = "GPTQ sec per layer (Hessian+Cholesky+sweep+pack) at 1 B300; % of roofline"
 # The largest single-GPU quantization workload: the widest layer (11008 inputs), the largest X (5.77 GB),
@@ -154,17 +154,27 @@ def run_ours(args, rank: int, world: int):
     spec = LAYERS[args.workload]
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
+    # --split tokens (N > 1): one layer for the whole job.  Each rank accumulates H over its own
+    # range of tokens, one NCCL all-reduce sums H, and each rank quantizes its own range of rows.
+    split = args.split == "tokens" and world > 1
+    if split and (spec.eora_rank or spec.lora_rank or spec.refine_cycles):
+        raise SystemExit("--split tokens runs the plain GPTQ workloads")
+    from post_weight_quantization_30_b300 import sharding
+
+    t_lo, t_hi = sharding.token_range(spec.n, world, rank, CHUNK_ROWS) if split else (0, spec.n)
+    r_lo, r_hi = sharding.row_range(spec.rows, world, rank) if split else (0, spec.rows)
 
     # Inputs: seeded host generation (spawn pool), then resident in HBM.
     t0 = time.time()
-    def host_tensor(ts):
-        # bf16 tensors travel as their raw 16-bit patterns; float32 as is.
+    def host_tensor(ts, r0=0, r1=None):
+        # Rows [r0, r1) of the tensor; bf16 tensors travel as their raw 16-bit patterns, float32 as is.
+        r1 = ts.rows if r1 is None else r1
         if ts.dtype == "bf16":
-            h = torch.empty((ts.rows, ts.cols), dtype=torch.int16, pin_memory=True)
-            generate(ts, out=h.numpy().view(np.uint16))
+            h = torch.empty((r1 - r0, ts.cols), dtype=torch.int16, pin_memory=True)
+            generate_rows(ts, r0, r1, out=h.numpy().view(np.uint16))
         else:
-            h = torch.empty((ts.rows, ts.cols), dtype=torch.float32, pin_memory=True)
-            generate(ts, out=h.numpy())
+            h = torch.empty((r1 - r0, ts.cols), dtype=torch.float32, pin_memory=True)
+            generate_rows(ts, r0, r1, out=h.numpy())
         return h
 
     def to_dev(h, dst=None):
@@ -178,12 +188,12 @@ def run_ours(args, rank: int, world: int):
         dst.copy_(h, non_blocking=True)
         return dst
 
-    x_host = host_tensor(spec.X)
-    w_host = host_tensor(spec.W)
+    x_host = host_tensor(spec.X, t_lo, t_hi)
+    w_host = host_tensor(spec.W)[r_lo:r_hi] if split else host_tensor(spec.W)
     gen_s = time.time() - t0
     X = to_dev(x_host)
     W = to_dev(w_host)
-    R, C, N = spec.rows, spec.cols, spec.n
+    R, C, N = r_hi - r_lo, spec.cols, t_hi - t_lo  # this rank's rows and tokens
     H = torch.zeros((C, C), dtype=torch.float32, device=dev)
     ws = torch.empty(gq.lib.gptq_quantize_layer_workspace_size(R, C, spec.block), dtype=torch.uint8, device=dev)
     r = spec.eora_rank
@@ -233,6 +243,10 @@ def run_ours(args, rank: int, world: int):
         elif r:
             eora_part(Wsrc)
 
+    def reduce_h():
+        if split:
+            sharding.reduce_hessian(H)  # NCCL all-reduce (sum) on the current stream
+
     def step(ev=None):
         H.zero_()
         if ev is not None:
@@ -240,6 +254,7 @@ def run_ours(args, rank: int, world: int):
         gq.gptq_hessian_accumulate(H, X)
         if ev is not None:
             ev[1].record(stream)
+        reduce_h()
         quantize(W)
 
     for _ in range(args.warmup):
@@ -376,6 +391,7 @@ def run_ours(args, rank: int, world: int):
         for i in range(E2E_CHUNKS):
             stream.wait_event(landed[i])
             gq.gptq_hessian_accumulate(H, Xd[bounds[i]:bounds[i + 1]])
+        reduce_h()
         stream.wait_event(landed[E2E_CHUNKS])
         quantize(Wd)
         for k, v in res_host.items():
@@ -400,23 +416,26 @@ def run_ours(args, rank: int, world: int):
 
     result = {
         "metric": METRIC,
-        "value": round(seconds_per_layer(ms_per_step, world), 6),
+        "value": round(ms_per_step / 1e3 if split else seconds_per_layer(ms_per_step, world), 6),
         "unit": "s/layer",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": False,
-        "scaling": "weak",
+        "scaling": "strong" if split else "weak",
         "vs_baseline": None,
         "dtype": "bf16 x bf16 -> f32 (Hessian); f32 (factor, sweep, 3xTF32 GEMMs" +
                  (", OLrC + Bid-Up)" if rc else ", EoRA)" if r else ", intrinsic LoRA)" if rl else ")"),
         "data": describe_inputs(spec),
         "config": {
-            "workload": args.workload, "rows": R, "cols": C, "tokens": N, "bits": spec.bits, "group": spec.group,
+            "workload": args.workload, "rows": spec.rows, "cols": C, "tokens": spec.n, "bits": spec.bits,
+            "group": spec.group,
             "block": spec.block, "damp": spec.damp, "x_dtype": spec.X.dtype, "w_dtype": spec.W.dtype,
             "l2": "inputs larger than L2 (X %.2f GB > 126 MB), no flush" % (spec.X.nbytes / 1e9),
-            "parallelism": "replicas" if world > 1 else "single GPU",
+            "parallelism": (f"tokens split for H ({N} of {spec.n} on rank {rank}) + one NCCL all-reduce of H, rows "
+                            f"split for the factor-and-sweep ({R} of {spec.rows})" if split else
+                            "replicas" if world > 1 else "single GPU"),
         },
         "phases_ms": {k: round(v, 4) for k, v in phase.items()},
         "roofline": {
@@ -826,6 +845,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(LAYERS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--split", default="replicas", choices=["replicas", "tokens"],
+                    help="N > 1: independent replicas (default) or one layer split over the ranks")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
