@@ -412,7 +412,7 @@ def run_ours(args, rank: int, world: int):
         bound, peak, peak_kind = "alu", round(148 * 128 * 2 * peaks.get("sm_max_mhz", 2032.0) * 1e6 / 1e12, 1), \
             "float32 FMA issue rate from SM count and maximum clock"
     traffic = _read_traffic(args.workload)
-    rooflines = phase_rooflines(spec, phase, kt, peaks, peak_kind, codes=rc > 0, w_hat=(r or rl) > 0)
+    rooflines = phase_rooflines(spec, phase, kt, peaks, _peaks()[1], codes=rc > 0, w_hat=(r or rl) > 0)
 
     result = {
         "metric": METRIC,
