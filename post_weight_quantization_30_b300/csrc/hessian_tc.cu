@@ -3,21 +3,20 @@
 // are built from ([GPTQ-wiki] "Enfoque Técnico"; [LowBit] section 2).
 //
 // Design (sm_103a):
-// * One CTA per output tile of 128 x 256 features, only for tiles that touch the
-//   upper triangle; each element of H is written by exactly one CTA: the
-//   upper triangle (c >= r) directly and the strict lower triangle as the
-//   mirror, so H stays bit-for-bit symmetric and the result is deterministic.
+// * Tiles of 256 x 256 features, only those on or above the diagonal; each
+//   element of H is written by exactly one CTA: the upper triangle (c >= r)
+//   directly and the strict lower triangle as the mirror, so H stays bit-for-bit
+//   symmetric and the result is deterministic.
 // * A = X^T[i-tile, tokens] and B = X[tokens, j-tile] are both read straight
 //   from the row-major X (features contiguous): MN-major operands, loaded by
-//   TMA as 64-token x 64-feature boxes with 128-byte swizzle.  Four-stage
-//   mbarrier pipeline, 48 KB per stage.
-// * Warp 0 / lane 0 issues the TMA loads, warp 1 / lane 0 issues
-//   tcgen05.mma (kind::f16, bf16 x bf16 -> f32, M = 128, N = 256, K = 16) into a
-//   256-column TMEM accumulator; tcgen05.commit releases shared-memory stages
-//   and finally signals the epilogue.
-// * Epilogue: eight warps read their TMEM lanes (one output row each, half of
-//   the columns) with tcgen05.ld after every 512 tokens, add the partial sums
-//   into float32 registers and finally add 2 * sum into H.
+//   TMA as 64-token x 64-feature boxes with 128-byte swizzle.
+// * A cluster of two CTAs computes one tile with tcgen05 cta_group::2 (see the
+//   kernel's comment); warp 0 / lane 0 of each CTA issues its TMA loads, warp 1
+//   / lane 0 of the even CTA issues the MMAs (kind::f16, bf16 x bf16 -> f32,
+//   M = 256, N = 256, K = 16).
+// * Epilogue: eight warps per CTA read their TMEM lanes (one output row each,
+//   half of the columns) with tcgen05.ld after every 512 tokens, add the
+//   partial sums into float32 registers and finally add 2 * sum into H.
 // * Every wait on an mbarrier is bounded (clock64 budget); on expiry the CTA
 //   records an error flag, waits (again bounded) until the TMA loads and MMAs
 //   it issued have completed, frees TMEM and returns.
@@ -30,30 +29,51 @@ __device__ unsigned int g_device_error = 0;  // bit 0: a bounded wait gave up
 namespace {
 using namespace tc;
 
-constexpr int TM = 128, TN = 256, TK = 64;  // tile rows, cols, tokens per stage
-constexpr int STAGES = 4;
-constexpr int BOX_BYTES = TK * 64 * 2;             // one 64-token x 64-feature bf16 box
-constexpr int A_BYTES = 2 * BOX_BYTES;             // 128 features
-constexpr int B_BYTES = 4 * BOX_BYTES;             // 256 features
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 48 KB
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
-constexpr uint32_t TMEM_COLS = 256;
+// ---------------------------------------------------------------------------
+// The CTA-pair kernel.  A cluster of two CTAs computes a 256 x 256 tile of H
+// with tcgen05 cta_group::2: each CTA loads its own 128 features of the A side
+// and its half (128) of the B side's 256 features, and one MMA of M = 256,
+// N = 256 reads both CTAs' shared memory, so every operand byte brought from
+// L2 feeds twice the multiply-adds of the single-CTA 128 x 256 tile (32 KB per
+// CTA per 64 tokens instead of 48 KB).  Each CTA's TMEM receives its 128 rows
+// of the tile (two 256-column buffers).  The tensor core's own accumulation
+// loses about half an ulp of the running sum per step, so each buffer sums KF
+// k-tiles (512 tokens) and the epilogue warps add it into float32 registers
+// (round-to-nearest) while the MMAs fill the other buffer.
+// * Each CTA's TMA loads count on its own full barrier.  In the odd CTA one
+//   thread waits for each of its stages to land and then arrives on the even
+//   CTA's peer barrier of that stage; the even CTA's MMA thread waits for both
+//   (its own stage landed, the odd CTA's announced) before it issues.  The MMA
+//   thread's commits arrive on the empty barriers and accumulator-full
+//   barriers of both CTAs; the epilogue warps of both CTAs release an
+//   accumulator buffer on the even CTA's barrier.
+// * Tiles: the 256-aligned tiles on or above the diagonal, in groups of P_GROUP
+//   tile-rows, column by column within a group.
+// * Every wait is bounded.  At the end each CTA waits for the loads it issued
+//   (its own full barriers) and the even CTA for its MMAs; both meet at a
+//   cluster barrier (the even CTA's MMAs read the odd CTA's shared memory)
+//   before TMEM is freed.
+namespace pair {
+constexpr int PT = 256;                           // tile rows and columns (128 rows per CTA)
+constexpr int TK = 64;                            // tokens per stage
+constexpr int STAGES = 7;
+constexpr int BOX = TK * 64 * 2;                  // one 64-token x 64-feature bf16 box
+constexpr int A_BYTES = 2 * BOX;                  // this CTA's 128 A features
+constexpr int B_BYTES = 2 * BOX;                  // this CTA's 128 of the 256 B features
+constexpr int STAGE = A_BYTES + B_BYTES;          // 32 KB
+constexpr int SMEM = STAGES * STAGE + 1024;
+constexpr uint32_t TCOLS = 256;                   // TMEM columns per accumulator buffer
+constexpr int KF = 8;                             // k-tiles per TMEM period (512 tokens)
+constexpr int P_GROUP = 8;                        // tile-rows per scheduling group
+constexpr int NWARPS = 10, EPI = 8;
+}  // namespace pair
 
-// Warp roles: 0 = TMA producer, 1 = MMA issuer, 2..9 = accumulator warps.
-// The tensor-core accumulator is summed over KF k-tiles (512 tokens) at a
-// time in one of two TMEM buffers; the accumulator warps add each partial
-// sum into float32 registers (round-to-nearest) while the MMAs fill the other
-// buffer.  Long in-TMEM accumulation is avoided because each accumulate step
-// of the tensor core loses about half an ulp of the running sum.
-constexpr int KF = 8;
-constexpr int GROUP = 16;  // tile-rows per scheduling group
-constexpr int NWARPS = 10;
-constexpr int EPI_WARPS = 8;
-
-__global__ void __launch_bounds__(NWARPS * 32, 1)
-    hessian_tc_kernel(const __grid_constant__ CUtensorMap xmap, float *__restrict__ H, int cols, int n) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::NWARPS * 32, 1)
+    hessian_pair_kernel(const __grid_constant__ CUtensorMap xmap, float *__restrict__ H, int cols, int n) {
+    using namespace pair;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];   // this CTA's half of the stage landed
+    __shared__ __align__(8) uint64_t peer_bar[STAGES];   // (even CTA) the odd CTA's half landed
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
     __shared__ __align__(8) uint64_t tfull[2];
     __shared__ __align__(8) uint64_t tempty[2];
@@ -63,44 +83,44 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
 
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool lead = rank == 0;
 
-    // Tile of this CTA among the tiles that touch the upper triangle (bj >=
-    // bjmin(bi) = bi TM / TN), in groups of GROUP tile-rows; within a group
-    // by column, then row.  CTAs that run at the same time then share a
-    // compact set of features of X, which keeps the X stripes they stream in
-    // L2 instead of re-reading all of X from HBM in every wave.
-    const int nbi = (cols + TM - 1) / TM, nbj = (cols + TN - 1) / TN;
-    int t = blockIdx.x, g0 = 0;
-    for (; g0 < nbi; g0 += GROUP) {
-        const int g1 = (g0 + GROUP) < nbi ? (g0 + GROUP) : nbi;
+    // This pair's tile (bi, bj), bj >= bi, among nb x nb 256-aligned tiles.
+    const int nb = (cols + PT - 1) / PT;
+    int t = blockIdx.x >> 1, g0 = 0;
+    for (; g0 < nb; g0 += P_GROUP) {
+        const int g1 = (g0 + P_GROUP) < nb ? (g0 + P_GROUP) : nb;
         int cnt = 0;
-        for (int i = g0; i < g1; ++i) cnt += nbj - (i * TM) / TN;
+        for (int i = g0; i < g1; ++i) cnt += nb - i;
         if (t < cnt) break;
         t -= cnt;
     }
-    const int g1 = (g0 + GROUP) < nbi ? (g0 + GROUP) : nbi;
-    int bi = g0, bj = (g0 * TM) / TN;
-    for (; bj < nbj; ++bj) {
-        int valid = 0;  // rows of the group that reach column bj: a prefix
-        while (g0 + valid < g1 && ((g0 + valid) * TM) / TN <= bj) ++valid;
+    const int g1 = (g0 + P_GROUP) < nb ? (g0 + P_GROUP) : nb;
+    int bi = g0, bj = g0;
+    for (; bj < nb; ++bj) {
+        const int valid = (bj + 1 < g1 ? bj + 1 : g1) - g0;  // tile-rows of the group that reach column bj
         if (t < valid) {
             bi = g0 + t;
             break;
         }
         t -= valid;
     }
-    const int r0 = bi * TM, c0 = bj * TN;
+    const int r0 = bi * PT + (int)rank * 128;   // this CTA's 128 rows of the tile
+    const int c0 = bj * PT;                     // the tile's 256 columns
+    const int cb = c0 + (int)rank * 128;        // this CTA's B half
     const int ktiles = (n + TK - 1) / TK;
     const int periods = (ktiles + KF - 1) / KF;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
+            mbar_init(&peer_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], EPI_WARPS);
+            mbar_init(&tempty[b], 2 * EPI);
         }
         mbar_init(&drain_bar, 1);
         abort_flag = 0;
@@ -108,13 +128,13 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
-                     "r"(2 * TMEM_COLS)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(2 * TCOLS)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     fence_before();
-    __syncthreads();
+    cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
     fence_after();
     const uint32_t tmem = tmem_slot;
 
@@ -129,64 +149,76 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
                     abort_flag = 1;
                     break;
                 }
-                unsigned char *st = smem + s * STAGE_BYTES;
-                mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
+                unsigned char *st = smem + s * STAGE;
+                mbar_arrive_expect_tx(&full_bar[s], STAGE);
                 const int y = kt * TK;
-                tma_load_2d(st + 0 * BOX_BYTES, &xmap, r0, y, &full_bar[s]);
-                tma_load_2d(st + 1 * BOX_BYTES, &xmap, r0 + 64, y, &full_bar[s]);
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    tma_load_2d(st + A_BYTES + b * BOX_BYTES, &xmap, c0 + 64 * b, y, &full_bar[s]);
+                tma_load_2d(st, &xmap, r0, y, &full_bar[s]);
+                tma_load_2d(st + BOX, &xmap, r0 + 64, y, &full_bar[s]);
+                tma_load_2d(st + A_BYTES, &xmap, cb, y, &full_bar[s]);
+                tma_load_2d(st + A_BYTES + BOX, &xmap, cb + 64, y, &full_bar[s]);
             }
             drain_loads<STAGES>(full_bar, issued);
         }
         __syncwarp();
+    } else if (warp == 1 && !lead) {
+        // Odd CTA: each stage that has landed here is announced on the even CTA's peer barrier.
+        if (lane == 0) {
+            for (int kt = 0; kt < ktiles; ++kt) {
+                const int s = kt % STAGES;
+                if (!mbar_wait(&full_bar[s], (uint32_t)(kt / STAGES) & 1u) || *(volatile int *)&abort_flag) {
+                    atomicOr(&g_device_error, 1u);
+                    abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_cluster(cluster_addr(smem_u32(&peer_bar[s]), 0));
+            }
+        }
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc(TM, TN);
+            constexpr uint32_t idesc = make_idesc(2 * 128, PT);
             bool ok = true;
             for (int p = 0; p < periods && ok; ++p) {
                 const int b = p & 1;
                 const uint32_t u = (uint32_t)(p >> 1) & 1u;
-                if (!mbar_wait(&tempty[b], u ^ 1u)) {
+                if (!mbar_wait_cluster(&tempty[b], u ^ 1u)) {
                     ok = false;
                     break;
                 }
                 fence_after();
-                const uint32_t acc = tmem + (uint32_t)(b * TMEM_COLS);
+                const uint32_t acc = tmem + (uint32_t)(b * TCOLS);
                 const int k_end = (p + 1) * KF < ktiles ? (p + 1) * KF : ktiles;
                 for (int kt = p * KF; kt < k_end; ++kt) {
                     const int s = kt % STAGES;
                     const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
-                    if (!mbar_wait(&full_bar[s], ph)) {
+                    if (!mbar_wait(&full_bar[s], ph) || !mbar_wait_cluster(&peer_bar[s], ph)) {
                         ok = false;
                         break;
                     }
                     fence_after();
-                    const uint32_t a0 = smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t a0 = smem_u32(smem + s * STAGE);
                     const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < TK / 16; ++kk) {
-                        // 16 tokens = two 8-row core-matrix groups (SBO = 1024 B apart);
-                        // 64-feature chunks are whole boxes (LBO = box size apart).
-                        const uint64_t ad = smem_desc(a0 + kk * 2048, BOX_BYTES, 1024);
-                        const uint64_t bd = smem_desc(b0 + kk * 2048, BOX_BYTES, 1024);
-                        mma_bf16(acc, ad, bd, idesc, (kt > p * KF || kk > 0) ? 1u : 0u);
+                        const uint64_t ad = smem_desc(a0 + kk * 2048, BOX, 1024);
+                        const uint64_t bd = smem_desc(b0 + kk * 2048, BOX, 1024);
+                        mma_bf16_pair(acc, ad, bd, idesc, (kt > p * KF || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(&empty_bar[s]);
+                    mma_commit_pair(&empty_bar[s], 0x3);
                 }
-                mma_commit(&tfull[b]);
+                if (!ok) break;
+                mma_commit_pair(&tfull[b], 0x3);
             }
             if (!ok) {
                 atomicOr(&g_device_error, 1u);
                 abort_flag = 1;
             }
-            drain_mmas(&drain_bar);
+            mma_commit_pair(&drain_bar, 0x1);
+            mbar_wait_for(&drain_bar, 0u, WAIT_BUDGET);
         }
         __syncwarp();
     } else {
-        // Accumulator warps: TMEM lane quarter = warp % 4 (hardware rule), column
-        // half = (warp - 2) / 4.  Each thread owns one row x 128 columns.
+        // Accumulator warps of both CTAs: TMEM lane quarter = warp % 4, column half = (warp - 2) / 4.
         const int q = warp & 3, half = (warp - 2) >> 2;
         float master[128];
 #pragma unroll
@@ -201,7 +233,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             }
             __syncwarp();
             fence_after();
-            const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TMEM_COLS + half * 128);
+            const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TCOLS + half * 128);
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 float v[32];
@@ -211,7 +243,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             }
             fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[b]);
+            if (lane == 0) mbar_arrive_cluster(cluster_addr(smem_u32(&tempty[b]), 0));
         }
         if (!ok) {
             atomicOr(&g_device_error, 1u);
@@ -220,11 +252,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         __syncwarp();
         // H += 2 * master: upper triangle directly, strict lower as the mirror.
         const int r = r0 + q * 32 + lane;
-        const int cb = c0 + half * 128;
+        const int cc = c0 + half * 128;
         if (ok && r < cols && periods > 0) {
 #pragma unroll
             for (int j = 0; j < 128; ++j) {
-                const int c = cb + j;
+                const int c = cc + j;
                 if (c < cols && c >= r) {
                     const float add = 2.f * master[j];
                     H[(int64_t)r * cols + c] += add;
@@ -234,10 +266,9 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         }
     }
     fence_before();
-    __syncthreads();
+    cluster_sync();  // the even CTA's MMAs are done with both CTAs' memory
     if (warp == 0) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * TMEM_COLS)
-                     : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * TCOLS) : "memory");
     }
 }
 
@@ -280,26 +311,26 @@ cudaError_t hessian_bf16_tc(float *H, int64_t cols, const __nv_bfloat16 *X, int6
     const int64_t max_chunk = (int64_t)1 << 30;  // token coordinates are 32-bit
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(hessian_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(hessian_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             pair::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int nbi = (int)((cols + TM - 1) / TM), nbj = (int)((cols + TN - 1) / TN);
-    int tiles = 0;
-    for (int bi = 0; bi < nbi; ++bi) tiles += nbj - (bi * TM) / TN;
+    const int nb = (int)((cols + pair::PT - 1) / pair::PT);
+    const int tiles = nb * (nb + 1) / 2;
     for (int64_t t0 = 0; t0 < n; t0 += max_chunk) {
         const int64_t nc = (n - t0) < max_chunk ? (n - t0) : max_chunk;
         CUtensorMap map;
         cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)nc};
         cuuint64_t gstride[1] = {(cuuint64_t)ldx * 2};
-        cuuint32_t box[2] = {64, TK};
+        cuuint32_t box[2] = {64, pair::TK};
         cuuint32_t estr[2] = {1, 1};
         CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)(X + t0 * ldx), gdim, gstride, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
         const int th = timing_begin(TK_HESSIAN, s);
-        hessian_tc_kernel<<<tiles, NWARPS * 32, SMEM_BYTES, s>>>(map, H, (int)cols, (int)nc);
+        hessian_pair_kernel<<<2 * tiles, pair::NWARPS * 32, pair::SMEM, s>>>(map, H, (int)cols, (int)nc);
         count_launch();
         timing_end(th, s, (double)nc * (double)cols * (double)(cols + 1));
         cudaError_t e = cudaGetLastError();
