@@ -60,6 +60,16 @@ __device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64
         : "memory");
 }
 
+__device__ __forceinline__ void mma_tf32_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __global__ void __launch_bounds__(G_NWARPS * 32, 1)
     gemm3_kernel(const __grid_constant__ CUtensorMap ahi, const __grid_constant__ CUtensorMap alo,
                  const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo, float *C,
@@ -313,6 +323,297 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
     }
 }
 
+// The same product on CTA pairs, for outputs wider than one tile: a cluster of
+// two CTAs computes a 256 x 256 tile with tcgen05 cta_group::2 (M = 256 over
+// the two CTAs' 128 rows, N = 256 over their halves of the 256 B rows), so each
+// operand byte brought from L2 feeds twice the multiply-adds of the 128 x 128
+// tile: 64 KB per CTA per 32 K-values carry 128 x 256 outputs instead of
+// 128 x 128.  The pipeline is the Hessian pair kernel's: the even CTA's loads
+// count on its full barrier and the odd CTA's directly on the even CTA's peer
+// barrier, the even CTA's MMA thread commits to the barriers of both, the
+// epilogue warps of both release an accumulator buffer on the even CTA's
+// barrier, and the end is two cluster barriers around the even CTA's wait for
+// every stage either CTA issued.  Eight epilogue warps per CTA (one row and 128 columns
+// per thread) add the flushed partial sums and apply C = beta C + alpha A B^T
+// through shared memory, as above.  tri = 1 skips the pair tiles entirely above
+// the diagonal.  No split-K.
+namespace gpair {
+constexpr int PT = 256;                  // pair tile rows and columns
+constexpr int TILE = 128 * GK * 4;       // 16 KB: 128 rows x 32 K-values
+constexpr int STAGE = 4 * TILE;          // A hi, A lo, B hi, B lo (this CTA's halves)
+constexpr int STAGES = 3;
+constexpr int SMEM = STAGES * STAGE + 1024;
+constexpr uint32_t TCOLS = 256;
+constexpr int KF = 8;                    // stages per TMEM period (256 K-values)
+constexpr int NWARPS = 10, EPI = 8;
+constexpr int SLD = 128 + 4;             // staging row stride (floats)
+}  // namespace gpair
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::NWARPS * 32, 1)
+    gemm3_pair_kernel(const __grid_constant__ CUtensorMap ahi, const __grid_constant__ CUtensorMap alo,
+                      const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo, float *C,
+                      int64_t ldc, int M, int N, int K, float alpha, float beta, int tri, float *Chi, float *Clo,
+                      int64_t ldcs, int split_row0, int split_ncols) {
+    using namespace gpair;
+    const uint32_t rank = cluster_ctarank();
+    const bool lead = rank == 0;
+    const int pm0 = blockIdx.y * PT, n0 = (blockIdx.x >> 1) * PT;
+    if (tri == 1 && n0 > pm0 + PT - 1) return;  // the whole pair tile is above the diagonal (both CTAs agree)
+    const int m0 = pm0 + (int)rank * 128;       // this CTA's rows
+    const int nb0 = n0 + (int)rank * 128;       // this CTA's B rows
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t peer_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    __shared__ __align__(8) uint64_t tfull[2];
+    __shared__ __align__(8) uint64_t tempty[2];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ int peer_issued;  // (even CTA) stages the odd CTA issued
+
+    unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ktiles = (K + GK - 1) / GK;
+    const int periods = (ktiles + KF - 1) / KF;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&peer_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 2 * EPI);
+        }
+        mbar_init(&drain_bar, 1);
+        abort_flag = 0;
+        peer_issued = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(2 * TCOLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    cluster_sync();
+    fence_after();
+    const uint32_t tmem = tmem_slot;
+    bool ok = true;
+
+    int issued = 0;  // (warp 0, lane 0) stages this CTA issued
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kt = 0; kt < ktiles; ++kt, ++issued) {
+                const int s = kt % STAGES;
+                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                if (!mbar_wait(&empty_bar[s], ph ^ 1u) || *(volatile int *)&abort_flag) {
+                    atomicOr(&g_gemm_error, 1u);
+                    abort_flag = 1;
+                    break;
+                }
+                unsigned char *st = smem + s * STAGE;
+                const int x = kt * GK;
+                if (lead) {
+                    mbar_arrive_expect_tx(&full_bar[s], STAGE);
+                    tma_load_2d(st, &ahi, x, m0, &full_bar[s]);
+                    tma_load_2d(st + TILE, &alo, x, m0, &full_bar[s]);
+                    tma_load_2d(st + 2 * TILE, &bhi, x, nb0, &full_bar[s]);
+                    tma_load_2d(st + 3 * TILE, &blo, x, nb0, &full_bar[s]);
+                } else {
+                    const uint32_t pb = cluster_addr(smem_u32(&peer_bar[s]), 0);
+                    mbar_arrive_expect_tx_cluster(pb, STAGE);
+                    tma_load_2d_to_peer_bar(st, &ahi, x, m0, pb);
+                    tma_load_2d_to_peer_bar(st + TILE, &alo, x, m0, pb);
+                    tma_load_2d_to_peer_bar(st + 2 * TILE, &bhi, x, nb0, pb);
+                    tma_load_2d_to_peer_bar(st + 3 * TILE, &blo, x, nb0, pb);
+                }
+            }
+            if (!lead) {
+                asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr(smem_u32(&peer_issued), 0)),
+                             "r"(issued)
+                             : "memory");
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && lead) {
+            constexpr uint32_t idesc = idesc_tf32(PT, PT);
+            for (int p = 0; p < periods && ok; ++p) {
+                const int b = p & 1;
+                const uint32_t u = (uint32_t)(p >> 1) & 1u;
+                if (!mbar_wait(&tempty[b], u ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const uint32_t acc = tmem + (uint32_t)(b * TCOLS);
+                const int k_end = (p + 1) * KF < ktiles ? (p + 1) * KF : ktiles;
+                for (int kt = p * KF; kt < k_end; ++kt) {
+                    const int s = kt % STAGES;
+                    const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                    if (!mbar_wait(&full_bar[s], ph) || !mbar_wait(&peer_bar[s], ph)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t a_hi = smem_u32(smem + s * STAGE);
+                    const uint32_t a_lo = a_hi + TILE;
+                    const uint32_t b_hi = a_hi + 2 * TILE;
+                    const uint32_t b_lo = a_hi + 3 * TILE;
+#pragma unroll
+                    for (int kk = 0; kk < GK / 8; ++kk) {
+                        const uint32_t off = kk * 32;
+                        const uint64_t dah = smem_desc(a_hi + off, 16, 1024);
+                        const uint64_t dal = smem_desc(a_lo + off, 16, 1024);
+                        const uint64_t dbh = smem_desc(b_hi + off, 16, 1024);
+                        const uint64_t dbl = smem_desc(b_lo + off, 16, 1024);
+                        const uint32_t first = (kt == p * KF && kk == 0) ? 0u : 1u;
+                        mma_tf32_pair(acc, dal, dbh, idesc, first);
+                        mma_tf32_pair(acc, dah, dbl, idesc, 1u);
+                        mma_tf32_pair(acc, dah, dbh, idesc, 1u);
+                    }
+                    mma_commit_pair(&empty_bar[s], 0x3);
+                }
+                if (!ok) break;
+                mma_commit_pair(&tfull[b], 0x3);
+            }
+            if (!ok) {
+                atomicOr(&g_gemm_error, 1u);
+                abort_flag = 1;
+            }
+            mma_commit_pair(&drain_bar, 0x1);
+            mbar_wait_for(&drain_bar, 0u, WAIT_BUDGET);
+        }
+        __syncwarp();
+    } else {
+        // Epilogue warps of both CTAs: TMEM lane quarter q = warp % 4, column half h.
+        const int q = warp & 3, h = (warp - 2) >> 2;
+        float master[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) master[i] = 0.f;
+        for (int p = 0; p < periods; ++p) {
+            const int b = p & 1;
+            const uint32_t u = (uint32_t)(p >> 1) & 1u;
+            if (!mbar_wait(&tfull[b], u)) {
+                ok = false;
+                break;
+            }
+            __syncwarp();
+            fence_after();
+            const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TCOLS + h * 128);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                float v[32];
+                tmem_ld32(base + ch * 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) master[ch * 32 + i] += v[i];
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(cluster_addr(smem_u32(&tempty[b]), 0));
+        }
+        if (!ok) {
+            atomicOr(&g_gemm_error, 1u);
+            abort_flag = 1;
+        }
+        __syncwarp();
+        // Through shared memory (the pipeline stages are idle now): this warp's 32 rows x
+        // 128 columns, then C read and written one 512-byte row segment at a time.
+        float *stage = reinterpret_cast<float *>(smem) + (size_t)(h * 4 + q) * 32 * SLD;
+        if (ok && periods > 0) {
+#pragma unroll
+            for (int j = 0; j < 128; j += 4)
+                *reinterpret_cast<float4 *>(stage + lane * SLD + j) =
+                    make_float4(master[j], master[j + 1], master[j + 2], master[j + 3]);
+        }
+        __syncwarp();
+        const int c = n0 + h * 128 + lane * 4;  // this lane's 4 columns of every row
+        const bool full4 = (c + 3 < N) && (ldc % 4) == 0 && ((uintptr_t)C % 16) == 0 &&
+                           (!Chi || ((ldcs % 4) == 0 && ((uintptr_t)Chi % 16) == 0 && ((uintptr_t)Clo % 16) == 0));
+        if (ok && periods > 0) {
+            for (int rr0 = 0; rr0 < 32; rr0 += 8) {
+                float4 old[8];
+                if (beta != 0.f) {
+#pragma unroll
+                    for (int uu = 0; uu < 8; ++uu) {
+                        const int r = m0 + q * 32 + rr0 + uu;
+                        old[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (r < M) {
+                            const float *cp = C + (int64_t)r * ldc + c;
+                            if (full4) old[uu] = *reinterpret_cast<const float4 *>(cp);
+                            else {
+                                if (c < N) old[uu].x = cp[0];
+                                if (c + 1 < N) old[uu].y = cp[1];
+                                if (c + 2 < N) old[uu].z = cp[2];
+                                if (c + 3 < N) old[uu].w = cp[3];
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) {
+                    const int rr = rr0 + uu, r = m0 + q * 32 + rr;
+                    if (r >= M || c >= N) continue;
+                    const float4 a = *reinterpret_cast<const float4 *>(stage + rr * SLD + lane * 4);
+                    float v[4] = {alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w};
+                    if (beta != 0.f) {
+                        v[0] = fmaf(beta, old[uu].x, v[0]);
+                        v[1] = fmaf(beta, old[uu].y, v[1]);
+                        v[2] = fmaf(beta, old[uu].z, v[2]);
+                        v[3] = fmaf(beta, old[uu].w, v[3]);
+                    }
+                    float *cp = C + (int64_t)r * ldc + c;
+                    float hh[4], ll[4];
+                    const bool sp = Chi && r >= split_row0 && c < split_ncols;
+                    const int64_t so = (int64_t)(r - split_row0) * ldcs + c;
+                    if (sp) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            hh[e] = tf32_hi(v[e]);
+                            ll[e] = v[e] - hh[e];
+                        }
+                    }
+                    if (full4 && (!sp || c + 3 < split_ncols)) {
+                        *reinterpret_cast<float4 *>(cp) = make_float4(v[0], v[1], v[2], v[3]);
+                        if (sp) {
+                            *reinterpret_cast<float4 *>(Chi + so) = make_float4(hh[0], hh[1], hh[2], hh[3]);
+                            *reinterpret_cast<float4 *>(Clo + so) = make_float4(ll[0], ll[1], ll[2], ll[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (c + e < N) {
+                                cp[e] = v[e];
+                                if (sp && c + e < split_ncols) {
+                                    Chi[so + e] = hh[e];
+                                    Clo[so + e] = ll[e];
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    fence_before();
+    cluster_sync();  // main loops done in both CTAs; the odd CTA's stage count is visible
+    if (warp == 0 && lane == 0 && lead) {
+        drain_loads<STAGES>(full_bar, issued);
+        drain_loads<STAGES>(peer_bar, *(volatile int *)&peer_issued);
+    }
+    __syncwarp();
+    cluster_sync();  // every load has landed; the even CTA's MMAs are done with both CTAs' memory
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * TCOLS) : "memory");
+    }
+}
+
 __global__ void split_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t lds,
                              float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
     const int64_t n = rows * cols;
@@ -383,17 +684,31 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(gemm3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemm3_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gpair::SMEM);
+        if (e != cudaSuccess) return e;
         attr_set = true;
     }
     CUtensorMap mah, mal, mbh, mbl;
     if (!make_map(&mah, Ahi, K, M, lda, GM) || !make_map(&mal, Alo, K, M, lda, GM) ||
         !make_map(&mbh, Bhi, K, N, ldb, GN) || !make_map(&mbl, Blo, K, N, ldb, GN))
         return cudaErrorInvalidValue;
-    dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
-    const int kt_all = (int)((K + GK - 1) / GK);
     // Useful products: all M x N outputs, or those on and below the diagonal for tri = 1.
     const double outs = tri == 1 ? (M >= N ? (double)M * N - (double)N * (N - 1) / 2 : (double)M * (M + 1) / 2)
                                  : (double)M * N;
+    if (M > GM && N > GN) {
+        // Wider than one tile both ways: 256 x 256 tiles on CTA pairs (the boxes stay 128 rows:
+        // each CTA loads its 128 rows of A and its 128 of the pair's 256 rows of B).
+        dim3 pgrid((unsigned)(2 * ((N + gpair::PT - 1) / gpair::PT)), (unsigned)((M + gpair::PT - 1) / gpair::PT));
+        const int th = timing_begin(TK_GEMM3, s);
+        gemm3_pair_kernel<<<pgrid, gpair::NWARPS * 32, gpair::SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N,
+                                                                         (int)K, alpha, beta, tri, Chi, Clo, ldcs,
+                                                                         split_row0, split_ncols);
+        count_launch();
+        timing_end(th, s, 2.0 * outs * (double)K);
+        return cudaGetLastError();
+    }
+    dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
+    const int kt_all = (int)((K + GK - 1) / GK);
     const int th = timing_begin(TK_GEMM3, s);
     gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta,
                                                     tri, Chi, Clo, ldcs, kt_all, 0, split_row0, split_ncols, 0);

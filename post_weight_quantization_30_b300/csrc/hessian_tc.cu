@@ -40,19 +40,21 @@ using namespace tc;
 // loses about half an ulp of the running sum per step, so each buffer sums KF
 // k-tiles (512 tokens) and the epilogue warps add it into float32 registers
 // (round-to-nearest) while the MMAs fill the other buffer.
-// * Each CTA's TMA loads count on its own full barrier.  In the odd CTA one
-//   thread waits for each of its stages to land and then arrives on the even
-//   CTA's peer barrier of that stage; the even CTA's MMA thread waits for both
-//   (its own stage landed, the odd CTA's announced) before it issues.  The MMA
+// * The even CTA's loads count on its full barrier; the odd CTA's loads count
+//   directly on the even CTA's peer barrier of the stage (the odd CTA's
+//   producer arrives there with the stage's byte count before it issues them).
+//   The even CTA's MMA thread waits for both barriers before it issues.  The MMA
 //   thread's commits arrive on the empty barriers and accumulator-full
 //   barriers of both CTAs; the epilogue warps of both CTAs release an
 //   accumulator buffer on the even CTA's barrier.
 // * Tiles: the 256-aligned tiles on or above the diagonal, in groups of P_GROUP
 //   tile-rows, column by column within a group.
-// * Every wait is bounded.  At the end each CTA waits for the loads it issued
-//   (its own full barriers) and the even CTA for its MMAs; both meet at a
-//   cluster barrier (the even CTA's MMAs read the odd CTA's shared memory)
-//   before TMEM is freed.
+// * Every wait is bounded.  At the end the even CTA waits for its MMAs, the odd
+//   CTA publishes how many stages it issued, and after a cluster barrier the
+//   even CTA waits until every stage either CTA issued has landed (both kinds
+//   of barrier are its own); a second cluster barrier (the even CTA's MMAs read
+//   the odd CTA's shared memory, and the odd CTA's loads count on the even
+//   CTA's barriers) precedes the freeing of TMEM.
 namespace pair {
 constexpr int PT = 256;                           // tile rows and columns (128 rows per CTA)
 constexpr int TK = 64;                            // tokens per stage
@@ -80,6 +82,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::NWARPS * 32, 1
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
+    __shared__ int peer_issued;  // (even CTA) stages the odd CTA issued
 
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,6 +127,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::NWARPS * 32, 1
         }
         mbar_init(&drain_bar, 1);
         abort_flag = 0;
+        peer_issued = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -138,9 +142,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::NWARPS * 32, 1
     fence_after();
     const uint32_t tmem = tmem_slot;
 
+    int issued = 0;  // (warp 0, lane 0) stages this CTA issued
     if (warp == 0) {
         if (lane == 0) {
-            int issued = 0;
             for (int kt = 0; kt < ktiles; ++kt, ++issued) {
                 const int s = kt % STAGES;
                 const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
@@ -150,38 +154,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::NWARPS * 32, 1
                     break;
                 }
                 unsigned char *st = smem + s * STAGE;
-                mbar_arrive_expect_tx(&full_bar[s], STAGE);
                 const int y = kt * TK;
-                tma_load_2d(st, &xmap, r0, y, &full_bar[s]);
-                tma_load_2d(st + BOX, &xmap, r0 + 64, y, &full_bar[s]);
-                tma_load_2d(st + A_BYTES, &xmap, cb, y, &full_bar[s]);
-                tma_load_2d(st + A_BYTES + BOX, &xmap, cb + 64, y, &full_bar[s]);
-            }
-            drain_loads<STAGES>(full_bar, issued);
-        }
-        __syncwarp();
-    } else if (warp == 1 && !lead) {
-        // Odd CTA: each stage that has landed here is announced on the even CTA's peer barrier.
-        if (lane == 0) {
-            for (int kt = 0; kt < ktiles; ++kt) {
-                const int s = kt % STAGES;
-                if (!mbar_wait(&full_bar[s], (uint32_t)(kt / STAGES) & 1u) || *(volatile int *)&abort_flag) {
-                    atomicOr(&g_device_error, 1u);
-                    abort_flag = 1;
-                    break;
+                if (lead) {
+                    mbar_arrive_expect_tx(&full_bar[s], STAGE);
+                    tma_load_2d(st, &xmap, r0, y, &full_bar[s]);
+                    tma_load_2d(st + BOX, &xmap, r0 + 64, y, &full_bar[s]);
+                    tma_load_2d(st + A_BYTES, &xmap, cb, y, &full_bar[s]);
+                    tma_load_2d(st + A_BYTES + BOX, &xmap, cb + 64, y, &full_bar[s]);
+                } else {
+                    const uint32_t pb = cluster_addr(smem_u32(&peer_bar[s]), 0);
+                    mbar_arrive_expect_tx_cluster(pb, STAGE);
+                    tma_load_2d_to_peer_bar(st, &xmap, r0, y, pb);
+                    tma_load_2d_to_peer_bar(st + BOX, &xmap, r0 + 64, y, pb);
+                    tma_load_2d_to_peer_bar(st + A_BYTES, &xmap, cb, y, pb);
+                    tma_load_2d_to_peer_bar(st + A_BYTES + BOX, &xmap, cb + 64, y, pb);
                 }
-                mbar_arrive_cluster(cluster_addr(smem_u32(&peer_bar[s]), 0));
+            }
+            if (!lead) {
+                asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr(smem_u32(&peer_issued), 0)),
+                             "r"(issued)
+                             : "memory");
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && lead) {
             constexpr uint32_t idesc = make_idesc(2 * 128, PT);
             bool ok = true;
             for (int p = 0; p < periods && ok; ++p) {
                 const int b = p & 1;
                 const uint32_t u = (uint32_t)(p >> 1) & 1u;
-                if (!mbar_wait_cluster(&tempty[b], u ^ 1u)) {
+                if (!mbar_wait(&tempty[b], u ^ 1u)) {
                     ok = false;
                     break;
                 }
@@ -191,7 +194,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::NWARPS * 32, 1
                 for (int kt = p * KF; kt < k_end; ++kt) {
                     const int s = kt % STAGES;
                     const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
-                    if (!mbar_wait(&full_bar[s], ph) || !mbar_wait_cluster(&peer_bar[s], ph)) {
+                    if (!mbar_wait(&full_bar[s], ph) || !mbar_wait(&peer_bar[s], ph)) {
                         ok = false;
                         break;
                     }
@@ -266,7 +269,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::NWARPS * 32, 1
         }
     }
     fence_before();
-    cluster_sync();  // the even CTA's MMAs are done with both CTAs' memory
+    cluster_sync();  // main loops done in both CTAs; the odd CTA's stage count is visible
+    if (warp == 0 && lane == 0 && lead) {
+        drain_loads<STAGES>(full_bar, issued);
+        drain_loads<STAGES>(peer_bar, *(volatile int *)&peer_issued);
+    }
+    __syncwarp();
+    cluster_sync();  // every load has landed; the even CTA's MMAs are done with both CTAs' memory
     if (warp == 0) {
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * TCOLS) : "memory");
     }

@@ -165,32 +165,27 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Bounded wait (pipeline budget) on a barrier of this CTA that threads of the
-// other CTA arrive on: acquire at cluster scope.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const long long budget = *(volatile long long *)&g_wait_budget;
-    const long long t0 = clock64();
-    while (!mbar_try_wait_cluster(bar, parity)) {
-        if (clock64() - t0 > budget) return false;
-    }
-    return true;
-}
-
 // Arrive on an mbarrier given by its shared::cluster address (this CTA's or the peer's).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Arrive on the peer CTA's mbarrier (shared::cluster address) and add `bytes` to
+// the transaction count its current phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar), "r"(bytes)
+                 : "memory");
+}
+
+// 2-D TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of the other CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_to_peer_bar(void *dst, const CUtensorMap *map, int x, int y,
+                                                        uint32_t cluster_bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(cluster_bar)
+        : "memory");
 }
 
 // MMA over the CTA pair (issued by one thread of the even CTA): A's M = 256 rows
