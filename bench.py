@@ -475,7 +475,7 @@ def phase_rooflines(spec, phase: dict, kt, peaks: dict, peak_kind: str, codes: b
     """Roofline of each phase of the step and of the 3xTF32 GEMMs as a class.
 
     * factor: one Cholesky of the cols x cols damped H, cols^3 / 3 useful flops, against the useful
-      float32 rate of 3xTF32 on the tensor cores (the measured bf16 burst x 1/2 for TF32, the nominal
+      float32 rate of 3xTF32 on the tensor cores (the measured bf16 burst x 1.1 / 2.25, the nominal
       dense tf32 : bf16 ratio, x 1/3 for the three TF32 products per useful product);
     * sweep_pack: the algorithmic bytes of sweep_pack_bytes against the measured HBM copy rate; the
       phase also runs the in-block updates and the deferred trailing GEMMs, and its floor is the
@@ -485,8 +485,9 @@ def phase_rooflines(spec, phase: dict, kt, peaks: dict, peak_kind: str, codes: b
       CUDA-event time, against the same 3xTF32 rate.
     """
     C = spec.cols
-    tf32x3 = peaks["bf16_tflops"] / 2 / 3
-    tf32_kind = f"{peak_kind} bf16 dense burst x 1/2 (tf32) x 1/3 (three TF32 products per useful product)"
+    tf32x3 = peaks["bf16_tflops"] * (1.1 / 2.25) / 3
+    tf32_kind = (f"{peak_kind} bf16 dense burst x 1.1/2.25 (nominal dense tf32 : bf16) x 1/3 (three TF32 products "
+                 f"per useful product)")
     out = {}
     if phase.get("factor"):
         fl = C ** 3 / 3
