@@ -23,6 +23,33 @@ namespace gq {
 // Counts one kernel launch enqueued by the library (host side).
 void count_launch();
 
+// Programmatic dependent launch.  The kernels of the long serial chains (the
+// factor's panels, the sweep's blocks and their GEMMs) are launched with
+// programmatic stream serialization: the next kernel may be scheduled while
+// the previous one is still running, runs its prologue (barriers, TMEM,
+// shared memory) on idle SMs, and calls pdl_wait() before its first access to
+// global memory, which returns once the previous kernel has completed and its
+// writes are visible.  Each of these kernels calls pdl_trigger() first, so
+// that the next launch is not held back until it finishes.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Kernel classes of the optional per-launch timing (timing.cu; gq_timing_end
 // reports them in this order).
 enum TimedKind { TK_HESSIAN = 0, TK_GEMM3 = 1, TK_SWEEP = 2, TK_DIAG = 3, TK_GEMM_TF32 = 4, TK_COUNT = 5 };

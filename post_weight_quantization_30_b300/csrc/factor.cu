@@ -202,6 +202,8 @@ __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restr
                                                                   int kb, float *__restrict__ Linv,
                                                                   DeviceStatus *st, float *__restrict__ Lhi,
                                                                   float *__restrict__ Llo, float *__restrict__ Urev) {
+    pdl_trigger();
+    pdl_wait();  // the block was last updated by the previous kernel
     extern __shared__ __align__(16) float sm[];
     float *A = sm;                 // [NB][LDA]: the block, lower triangle, becomes L
     float *Y = A + NB * LDA;       // [NB][LDA]: L^-1, lower triangle
@@ -488,14 +490,13 @@ cudaError_t chol_panel(const CholCtx &c, int64_t k0, bool rec, bool p_split_read
     const int64_t npanel = (cols + NB - 1) / NB;
     float *ur = c.Uinv ? c.Uinv + (npanel - 1 - k0 / NB) * NB * NB : nullptr;
     const int th = timing_begin(TK_DIAG, c.s);
-    potrf_diag_kernel<<<1, DIAG_THREADS, DIAG_SMEM, c.s>>>(c.F, cols, k0, kb, c.Linv, c.st, more ? c.Lhi : nullptr,
-                                                           c.Llo, ur);
+    cudaError_t e = launch_pdl(potrf_diag_kernel, dim3(1), dim3(DIAG_THREADS), DIAG_SMEM, c.s, c.F, cols, k0, kb,
+                               c.Linv, c.st, more ? c.Lhi : (float *)nullptr, c.Llo, ur);
     count_launch();
     timing_end(th, c.s, 2.0 * kb * kb * kb / 3.0);
-    if (!more) return cudaGetLastError();
+    if (e != cudaSuccess || !more) return e;
     const int64_t rest = cols - k1;
     float *P = c.F + k1 * cols + k0;
-    cudaError_t e;
     if (!p_split_ready && (e = split_tf32(P, rest, kb, cols, c.Phi, c.Plo, NB, c.s)) != cudaSuccess) return e;
     if (rec)
         return gemm3(rest, kb, kb, 1.f, c.Phi, c.Plo, NB, c.Lhi, c.Llo, NB, 0.f, P, cols, 0, c.LThi + k1 * cols + k0,

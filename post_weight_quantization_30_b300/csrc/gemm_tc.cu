@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
                  const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo, float *C,
                  int64_t ldc, int M, int N, int K, float alpha, float beta, int tri, float *Chi, float *Clo,
                  int64_t ldcs, int ktiles_per_z, int64_t c_zstride, int split_row0, int split_ncols, int one_term) {
+    pdl_trigger();
     const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
     if (tri == 1 && n0 > m0 + GM - 1) return;  // tile entirely above the diagonal
     // Split K (gridDim.z > 1): slice z covers k-tiles [z * ktiles_per_z, ...) and
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
     fence_after();
     const uint32_t tmem = tmem_slot;
     bool ok = true;
+    pdl_wait();  // the operands and C come from earlier kernels
 
     if (warp == 0) {
         if (lane == 0) {
@@ -355,6 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::NWARPS * 32, 
                       int64_t ldc, int M, int N, int K, float alpha, float beta, int tri, float *Chi, float *Clo,
                       int64_t ldcs, int split_row0, int split_ncols) {
     using namespace gpair;
+    pdl_trigger();
     const uint32_t rank = cluster_ctarank();
     const bool lead = rank == 0;
     const int pm0 = blockIdx.y * PT, n0 = (blockIdx.x >> 1) * PT;
@@ -405,6 +408,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::NWARPS * 32, 
     fence_after();
     const uint32_t tmem = tmem_slot;
     bool ok = true;
+    pdl_wait();  // the operands and C come from earlier kernels
 
     int issued = 0;  // (warp 0, lane 0) stages this CTA issued
     if (warp == 0) {
@@ -616,6 +620,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::NWARPS * 32, 
 
 __global__ void split_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t lds,
                              float *__restrict__ hi, float *__restrict__ lo, int64_t ldd) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t n = rows * cols;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / cols, c = i % cols;
@@ -700,21 +706,22 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
         // each CTA loads its 128 rows of A and its 128 of the pair's 256 rows of B).
         dim3 pgrid((unsigned)(2 * ((N + gpair::PT - 1) / gpair::PT)), (unsigned)((M + gpair::PT - 1) / gpair::PT));
         const int th = timing_begin(TK_GEMM3, s);
-        gemm3_pair_kernel<<<pgrid, gpair::NWARPS * 32, gpair::SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N,
-                                                                         (int)K, alpha, beta, tri, Chi, Clo, ldcs,
-                                                                         split_row0, split_ncols);
+        const cudaError_t e = launch_pdl(gemm3_pair_kernel, pgrid, dim3(gpair::NWARPS * 32), gpair::SMEM, s, mah, mal,
+                                         mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta, tri, Chi, Clo, ldcs,
+                                         split_row0, split_ncols);
         count_launch();
         timing_end(th, s, 2.0 * outs * (double)K);
-        return cudaGetLastError();
+        return e;
     }
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
     const int kt_all = (int)((K + GK - 1) / GK);
     const int th = timing_begin(TK_GEMM3, s);
-    gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta,
-                                                    tri, Chi, Clo, ldcs, kt_all, 0, split_row0, split_ncols, 0);
+    const cudaError_t e = launch_pdl(gemm3_kernel, grid, dim3(G_NWARPS * 32), G_SMEM, s, mah, mal, mbh, mbl, C, ldc,
+                                     (int)M, (int)N, (int)K, alpha, beta, tri, Chi, Clo, ldcs, kt_all, (int64_t)0,
+                                     split_row0, split_ncols, 0);
     count_launch();
     timing_end(th, s, 2.0 * outs * (double)K);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, const float *Alo, int64_t lda,
@@ -742,11 +749,11 @@ cudaError_t gemm3_splitk(int64_t M, int64_t N, int64_t K, const float *Ahi, cons
     const int z = (kt_all + per - 1) / per;
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM), (unsigned)z);
     const int th = timing_begin(one_term ? TK_GEMM_TF32 : TK_GEMM3, s);
-    gemm3_kernel<<<grid, G_NWARPS * 32, G_SMEM, s>>>(mah, mal, mbh, mbl, partials, N, (int)M, (int)N, (int)K, 1.f, 0.f,
-                                                    0, nullptr, nullptr, 0, per, M * N, 0, 0, one_term ? 1 : 0);
+    cudaError_t e = launch_pdl(gemm3_kernel, grid, dim3(G_NWARPS * 32), G_SMEM, s, mah, mal, mbh, mbl, partials,
+                               (int64_t)N, (int)M, (int)N, (int)K, 1.f, 0.f, 0, (float *)nullptr, (float *)nullptr,
+                               (int64_t)0, per, M * N, 0, 0, one_term ? 1 : 0);
     count_launch();
     timing_end(th, s, 2.0 * (double)M * (double)N * (double)K);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return sum_slices(partials, z, M * N, C, s);
 }
@@ -766,9 +773,9 @@ cudaError_t split_tf32(const float *src, int64_t rows, int64_t cols, int64_t lds
     if (n <= 0) return cudaSuccess;
     int64_t g = (n + 255) / 256;
     if (g > 148 * 16) g = 148 * 16;
-    split_kernel<<<(unsigned)g, 256, 0, s>>>(src, rows, cols, lds, hi, lo, ldd);
+    const cudaError_t e = launch_pdl(split_kernel, dim3((unsigned)g), dim3(256), 0, s, src, rows, cols, lds, hi, lo, ldd);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace gq

@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                                                          int32_t *__restrict__ qweight, float *__restrict__ scales,
                                                          int32_t *__restrict__ qzeros, uint8_t *__restrict__ codes,
                                                          float *__restrict__ W_hat, float *__restrict__ row_err) {
+    pdl_trigger();
+    pdl_wait();  // D was last updated by the previous kernel
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SweepSmem &sm = *reinterpret_cast<SweepSmem *>(smem_raw);
     constexpr float maxq = (float)((1 << BITS) - 1);
@@ -430,11 +432,12 @@ cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, in
         attr_set = true;
     }
     const int th = timing_begin(TK_SWEEP, s);
-    sweep_kernel<BITS, TW><<<(unsigned)((rows + ROWS - 1) / ROWS), NTHREADS, smem, s>>>(
-        W, rows, cols, c0, bw, Uinv, F, dead, group, D, DL, qweight, scales, qzeros, codes, W_hat, row_err);
+    const cudaError_t e = launch_pdl(sweep_kernel<BITS, TW>, dim3((unsigned)((rows + ROWS - 1) / ROWS)), dim3(NTHREADS),
+                                     smem, s, W, rows, cols, c0, bw, Uinv, F, dead, group, D, DL, qweight, scales,
+                                     qzeros, codes, W_hat, row_err);
     count_launch();
     timing_end(th, s, (double)rows * bw * (bw - 1));
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
