@@ -19,9 +19,16 @@ it.
 Readings of points the pages leave open:
 
 * The Hessian is damped like GPTQ's, H~ + damp * mean(diag H~) * I, which
-  makes it positive definite for damp > 0, and factored by the same Cholesky
-  route.  The page's eigendecomposition + QR factorization is a robustness
-  device for very small damping; it is not reproduced.
+  makes it positive definite for damp > 0.  Two factorizations give the upper
+  factor U of its inverse (U^T U = H~_d^-1): GPTQ's (inverse, then Cholesky)
+  and the page's eigendecomposition + QR ("Detalles de Implementación"):
+  H~_d = Q Λ Q^T, M = Λ^(-1/2) Q^T, M = O R with O orthogonal and R upper
+  triangular, so M^T M = R^T R = H~_d^-1 and U = R with a positive diagonal.
+  The second never forms the inverse; its rounding grows with the square root
+  of the condition number instead of the condition number, which is what lets
+  the damping be small.  damp must be > 0: at 0 the augmented Hessian is
+  singular (its last r columns are combinations of the first ones) and the
+  factor of its inverse does not exist.
 * L is an input.  The leading singular subspace of X is not unique when
   singular values are close, so GPTQ-intrinsic LoRA is defined here for a given
   L (orthonormal columns); top_right_singular_vectors gives the page's choice.
@@ -88,15 +95,32 @@ def sweep_partial(W: np.ndarray, U: np.ndarray, bits: int, group: int, n_quant: 
     return dict(codes=codes, scales=scales, zeros=zeros, W_hat=What, row_err=row_err, free=W[:, n_quant:].copy())
 
 
-def intrinsic_lora(W: np.ndarray, H: np.ndarray, L: np.ndarray, bits: int, group: int, damp: float = 0.01) -> dict:
+def inverse_cholesky_upper_eigqr(Hd: np.ndarray) -> np.ndarray:
+    """Upper-triangular U with U^T U = Hd^-1 from the eigendecomposition of Hd and a QR factorization
+    ([GPTQ-LoRA] "Detalles de Implementación"): Hd = Q Λ Q^T, M = Λ^(-1/2) Q^T = O R, U = R with its
+    rows' signs chosen so that the diagonal is positive.  Hd must be positive definite."""
+    Hd = np.asarray(Hd, F64)
+    lam, Q = np.linalg.eigh(0.5 * (Hd + Hd.T))
+    if lam.min() <= 0:
+        raise ValueError("the damped Hessian is not positive definite")
+    M = (Q / np.sqrt(lam)).T
+    R = np.linalg.qr(M, mode="r")
+    return R * np.sign(np.diagonal(R))[:, None]
+
+
+def intrinsic_lora(W: np.ndarray, H: np.ndarray, L: np.ndarray, bits: int, group: int, damp: float = 0.01,
+                   factor: str = "cholesky") -> dict:
     """GPTQ-intrinsic LoRA of one layer for a given L (cols x r).  Returns the sweep outputs for Q,
-    B = R (rows x r), A = L^T (r x cols) and the damped augmented Hessian."""
+    B = R (rows x r), A = L^T (r x cols) and the damped augmented Hessian.  factor: "cholesky"
+    (GPTQ's inverse + Cholesky) or "eigqr" (the page's eigendecomposition + QR)."""
     W = np.asarray(W, F64)
     rows, cols = W.shape
     r = L.shape[1]
+    if not damp > 0:
+        raise ValueError("damp must be > 0: the augmented Hessian itself is singular")
     Ht = augmented_hessian(H, L)
     Hd, dead = og.prepare_hessian(Ht, damp)
-    U = og.inverse_cholesky_upper(Hd)
+    U = inverse_cholesky_upper_eigqr(Hd) if factor == "eigqr" else og.inverse_cholesky_upper(Hd)
     Wt = np.concatenate([W, np.zeros((rows, r))], axis=1)
     out = sweep_partial(Wt, U, bits, group, cols, dead=dead)
     out.update(B=out.pop("free"), A=np.asarray(L, F64).T.copy(), Hd=Hd, dead=dead)

@@ -180,3 +180,64 @@ def test_planted_mistakes_are_caught_by_the_optimality_pin(mutation):
     ref = il.free_columns_optimum(W, out["W_hat"], out["Hd"])
     assert np.linalg.norm(bad - ref) > 1e-3 * np.linalg.norm(ref)
     assert np.linalg.norm(out["B"] - ref) <= 1e-9 * np.linalg.norm(ref)
+
+
+# ---------------------------------------------- eigendecomposition + QR factorization
+def test_eigqr_factor_is_the_upper_factor_of_the_inverse():
+    """U^T U Hd = I, U upper triangular with a positive diagonal: the unique upper factor of Hd^-1,
+    so it equals GPTQ's inverse + Cholesky route where that one is accurate."""
+    rng = np.random.default_rng(30)
+    cols, r = 48, 4
+    H = og.hessian(_calib(300, cols, rng, outliers=2))
+    L, _ = il.top_right_singular_vectors(H, r)
+    Hd, _ = og.prepare_hessian(il.augmented_hessian(H, L), 0.01)
+    U = il.inverse_cholesky_upper_eigqr(Hd)
+    assert np.allclose(np.tril(U, -1), 0.0, atol=0)
+    assert np.all(np.diagonal(U) > 0)
+    assert np.linalg.norm(U.T @ U @ Hd - np.eye(cols + r)) <= 1e-9
+    assert np.allclose(U, og.inverse_cholesky_upper(Hd), rtol=1e-8, atol=1e-12 * np.abs(U).max())
+
+
+def test_eigqr_is_accurate_at_small_damping():
+    """At damping 1e-10 the augmented Hessian has condition number ~1e12: the eigendecomposition + QR
+    factor still satisfies U^T U Hd = I to ~1e-4 (rounding grows like sqrt(cond)), where the inverse +
+    Cholesky route is far worse or fails."""
+    rng = np.random.default_rng(31)
+    cols, r = 64, 6
+    H = og.hessian(_calib(400, cols, rng, outliers=3))
+    L, _ = il.top_right_singular_vectors(H, r)
+    Hd, _ = og.prepare_hessian(il.augmented_hessian(H, L), 1e-10)
+    cond = np.linalg.cond(Hd)
+    assert cond > 1e11
+    U = il.inverse_cholesky_upper_eigqr(Hd)
+    res_qr = np.linalg.norm(U.T @ U @ Hd - np.eye(cols + r))
+    assert res_qr <= 1e-3
+    try:
+        Uc = og.inverse_cholesky_upper(Hd)
+        res_chol = np.linalg.norm(Uc.T @ Uc @ Hd - np.eye(cols + r))
+    except np.linalg.LinAlgError:
+        res_chol = np.inf
+    assert res_qr < res_chol
+
+
+@pytest.mark.parametrize("damp", [1e-2, 1e-4, 1e-6])
+def test_eigqr_sweep_matches_bruteforce_obq_at_small_damping(damp):
+    """The sweep through the eigendecomposition + QR factor gives the codes and free columns of the
+    brute-force OBQ that re-inverts the remaining augmented Hessian after every column."""
+    rng = np.random.default_rng(40)
+    cols, r, bits, group = 8, 2, 3, 4
+    H = og.hessian(_calib(3 * cols, cols, rng, outliers=1))
+    L, _ = il.top_right_singular_vectors(H, r)
+    W = rng.standard_normal((120, cols)) * 0.02
+    out = il.intrinsic_lora(W, H, L, bits, group, damp, factor="eigqr")
+    codes, free = _obq_with_free_columns(np.hstack([W, np.zeros((120, r))]), out["Hd"], bits, group, cols)
+    assert np.array_equal(out["codes"], codes)
+    assert np.allclose(out["B"], free, rtol=1e-6, atol=1e-9)
+
+
+def test_zero_damping_is_rejected():
+    rng = np.random.default_rng(41)
+    H = og.hessian(_calib(100, 16, rng))
+    L, _ = il.top_right_singular_vectors(H, 2)
+    with pytest.raises(ValueError):
+        il.intrinsic_lora(rng.standard_normal((8, 16)), H, L, 2, 8, 0.0, factor="eigqr")
