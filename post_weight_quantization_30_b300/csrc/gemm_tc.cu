@@ -325,6 +325,242 @@ __global__ void __launch_bounds__(G_NWARPS * 32, 1)
     }
 }
 
+// The product for one 128-column tile and a short K (the panel solves and the
+// one-panel updates on the serial chains of the factor and the sweep), where a
+// launch spends most of its time on C.  Two pipeline stages; eight epilogue
+// warps (a 32-row lane quarter and 64 columns each); with beta != 0 the
+// epilogue warps copy their part of C into shared memory (cp.async) while the
+// MMAs run, so C is read from L2 once, overlapped, and the epilogue only adds,
+// splits and stores.  No split-K.
+namespace gsmall {
+constexpr int STAGES = 2;
+constexpr int NWARPS = 10;                     // TMA, MMA, 8 epilogue warps
+constexpr int EPI = 8;
+constexpr int SLD = 64 + 4;                    // staging row stride (floats)
+constexpr int CBUF = EPI * 32 * SLD * 4;       // 32 rows x 64 columns per epilogue warp
+constexpr int SMEM = STAGES * G_STAGE + CBUF + 1024;
+constexpr int MAX_K = G_KF * GK;               // one TMEM period
+}  // namespace gsmall
+
+__global__ void __launch_bounds__(gsmall::NWARPS * 32, 1)
+    gemm3_small_kernel(const __grid_constant__ CUtensorMap ahi, const __grid_constant__ CUtensorMap alo,
+                       const __grid_constant__ CUtensorMap bhi, const __grid_constant__ CUtensorMap blo, float *C,
+                       int64_t ldc, int M, int N, int K, float alpha, float beta, int tri, float *Chi, float *Clo,
+                       int64_t ldcs, int split_row0, int split_ncols) {
+    using namespace gsmall;
+    pdl_trigger();
+    const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
+    if (tri == 1 && n0 > m0 + GM - 1) return;  // tile entirely above the diagonal
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    __shared__ __align__(8) uint64_t tfull;
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    float *cbuf = reinterpret_cast<float *>(smem + STAGES * G_STAGE);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ktiles = (K + GK - 1) / GK;  // <= G_KF: one TMEM period
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        mbar_init(&tfull, 1);
+        mbar_init(&drain_bar, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                     "r"(G_TMEM)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tmem_slot;
+    bool ok = true;
+    pdl_wait();  // the operands and C come from earlier kernels
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int kt = 0; kt < ktiles; ++kt, ++issued) {
+                const int s = kt % STAGES;
+                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                if (!mbar_wait(&empty_bar[s], ph ^ 1u) || *(volatile int *)&abort_flag) {
+                    atomicOr(&g_gemm_error, 1u);
+                    abort_flag = 1;
+                    break;
+                }
+                unsigned char *st = smem + s * G_STAGE;
+                mbar_arrive_expect_tx(&full_bar[s], G_STAGE);
+                const int x = kt * GK;
+                tma_load_2d(st, &ahi, x, m0, &full_bar[s]);
+                tma_load_2d(st + TILE_A, &alo, x, m0, &full_bar[s]);
+                tma_load_2d(st + 2 * TILE_A, &bhi, x, n0, &full_bar[s]);
+                tma_load_2d(st + 2 * TILE_A + TILE_B, &blo, x, n0, &full_bar[s]);
+            }
+            drain_loads<STAGES>(full_bar, issued);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_tf32(GM, GN);
+            for (int kt = 0; kt < ktiles; ++kt) {
+                const int s = kt % STAGES;
+                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                if (!mbar_wait(&full_bar[s], ph)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const uint32_t a_hi = smem_u32(smem + s * G_STAGE);
+                const uint32_t a_lo = a_hi + TILE_A;
+                const uint32_t b_hi = a_hi + 2 * TILE_A;
+                const uint32_t b_lo = b_hi + TILE_B;
+#pragma unroll
+                for (int kk = 0; kk < GK / 8; ++kk) {
+                    const uint32_t off = kk * 32;
+                    const uint64_t dah = smem_desc(a_hi + off, 16, 1024);
+                    const uint64_t dal = smem_desc(a_lo + off, 16, 1024);
+                    const uint64_t dbh = smem_desc(b_hi + off, 16, 1024);
+                    const uint64_t dbl = smem_desc(b_lo + off, 16, 1024);
+                    const uint32_t first = (kt == 0 && kk == 0) ? 0u : 1u;
+                    mma_tf32(tmem, dal, dbh, idesc, first);
+                    mma_tf32(tmem, dah, dbl, idesc, 1u);
+                    mma_tf32(tmem, dah, dbh, idesc, 1u);
+                }
+                mma_commit(&empty_bar[s]);
+            }
+            if (ok) mma_commit(&tfull);
+            if (!ok) {
+                atomicOr(&g_gemm_error, 1u);
+                abort_flag = 1;
+            }
+            drain_mmas(&drain_bar);
+        }
+        __syncwarp();
+    } else {
+        // Epilogue warp: TMEM lane quarter q (rows q*32 + lane), columns h*64 .. h*64 + 63 of the tile.
+        const int q = warp & 3, h = (warp - 2) >> 2;
+        float *stage = cbuf + (size_t)(h * 4 + q) * 32 * SLD;
+        const int r = m0 + q * 32 + lane;   // this thread's row (phase A)
+        const int cl = n0 + h * 64;         // first column of this warp
+        const bool vec = (ldc % 4) == 0 && ((uintptr_t)C % 16) == 0;
+        // C of this thread's row into shared memory while the MMAs run.
+        if (beta != 0.f) {
+            if (r < M) {
+                const float *cp = C + (int64_t)r * ldc + cl;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float *dst = stage + lane * SLD + 4 * i;
+                    const int c = cl + 4 * i;
+                    if (vec && c + 3 < N) {
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(cp + 4 * i)
+                                     : "memory");
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) dst[e] = (c + e < N) ? cp[4 * i + e] : 0.f;
+                    }
+                }
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+        float acc[64];
+        if (!mbar_wait(&tfull, 0u)) ok = false;
+        __syncwarp();
+        fence_after();
+        if (ok) {
+            const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 64);
+            float v[32];
+            tmem_ld32(base, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = v[i];
+            tmem_ld32(base + 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[32 + i] = v[i];
+        }
+        fence_before();
+        if (beta != 0.f) asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();
+        if (!ok) {
+            atomicOr(&g_gemm_error, 1u);
+            abort_flag = 1;
+        }
+        // Phase A (one row per thread): v = alpha acc + beta C, in place in the staging rows.
+        if (ok && ktiles > 0) {
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+                float4 *sp = reinterpret_cast<float4 *>(stage + lane * SLD + j);
+                float4 o = make_float4(alpha * acc[j], alpha * acc[j + 1], alpha * acc[j + 2], alpha * acc[j + 3]);
+                if (beta != 0.f) {
+                    const float4 cv = *sp;
+                    o.x = fmaf(beta, cv.x, o.x);
+                    o.y = fmaf(beta, cv.y, o.y);
+                    o.z = fmaf(beta, cv.z, o.z);
+                    o.w = fmaf(beta, cv.w, o.w);
+                }
+                *sp = o;
+            }
+        }
+        __syncwarp();
+        // Phase B (coalesced): 16 lanes per row, 4 columns each, two rows per step.
+        const int c = cl + (lane & 15) * 4;
+        const bool full4 = vec && (c + 3 < N) &&
+                           (!Chi || ((ldcs % 4) == 0 && ((uintptr_t)Chi % 16) == 0 && ((uintptr_t)Clo % 16) == 0));
+        if (ok && ktiles > 0 && c < N) {
+            for (int rr = lane >> 4; rr < 32; rr += 2) {
+                const int row = m0 + q * 32 + rr;
+                if (row >= M) break;
+                const float4 a = *reinterpret_cast<const float4 *>(stage + rr * SLD + (lane & 15) * 4);
+                const float vv[4] = {a.x, a.y, a.z, a.w};
+                float *cp = C + (int64_t)row * ldc + c;
+                const bool sp = Chi && row >= split_row0 && c < split_ncols;
+                const int64_t so = (int64_t)(row - split_row0) * ldcs + c;
+                float hh[4], ll[4];
+                if (sp) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hh[e] = tf32_hi(vv[e]);
+                        ll[e] = vv[e] - hh[e];
+                    }
+                }
+                if (full4 && (!sp || c + 3 < split_ncols)) {
+                    *reinterpret_cast<float4 *>(cp) = a;
+                    if (sp) {
+                        *reinterpret_cast<float4 *>(Chi + so) = make_float4(hh[0], hh[1], hh[2], hh[3]);
+                        *reinterpret_cast<float4 *>(Clo + so) = make_float4(ll[0], ll[1], ll[2], ll[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (c + e < N) {
+                            cp[e] = vv[e];
+                            if (sp && c + e < split_ncols) {
+                                Chi[so + e] = hh[e];
+                                Clo[so + e] = ll[e];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(G_TMEM) : "memory");
+    }
+}
+
 // The same product on CTA pairs, for outputs wider than one tile: a cluster of
 // two CTAs computes a 256 x 256 tile with tcgen05 cta_group::2 (M = 256 over
 // the two CTAs' 128 rows, N = 256 over their halves of the 256 B rows), so each
@@ -714,6 +950,23 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
         return e;
     }
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
+    if (N <= GN && K <= gsmall::MAX_K) {
+        // One column tile, short K: the latency-bound shape of the serial chains.
+        static bool small_attr = false;
+        if (!small_attr) {
+            cudaError_t e = cudaFuncSetAttribute(gemm3_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 gsmall::SMEM);
+            if (e != cudaSuccess) return e;
+            small_attr = true;
+        }
+        const int th = timing_begin(TK_GEMM3, s);
+        const cudaError_t e = launch_pdl(gemm3_small_kernel, grid, dim3(gsmall::NWARPS * 32), gsmall::SMEM, s, mah,
+                                         mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta, tri, Chi, Clo,
+                                         ldcs, split_row0, split_ncols);
+        count_launch();
+        timing_end(th, s, 2.0 * outs * (double)K);
+        return e;
+    }
     const int kt_all = (int)((K + GK - 1) / GK);
     const int th = timing_begin(TK_GEMM3, s);
     const cudaError_t e = launch_pdl(gemm3_kernel, grid, dim3(G_NWARPS * 32), G_SMEM, s, mah, mal, mbh, mbl, C, ldc,

@@ -12,17 +12,43 @@
 // is swept its columns of D hold the TF32 hi part of ΔW and those of DL the lo
 // part.  Inside the block the ordinary per-column update runs with Uinv_b.
 //
-// Kernel layout: see sweep_rows_kernel (four lanes per row, 8 rows per warp,
-// 32 rows per CTA, every warp an independent chain over the block's columns).
+// Kernel layout.  One CTA = 32 output rows x one block; lane = row, warp =
+// one 32-column segment of the block (4 warps).  A warp sweeps its segment's
+// columns one after the other: every lane quantizes its row's weight
+// (round-half-even; the code decision equals the one from IEEE division
+// w / s, see rint_div), forms the scaled error e_j = (w_j - ŵ_j) F_jj
+// (= (w_j - ŵ_j) / U_jj) and updates the rest of the segment in registers
+// with row j of Uinv_b (shared memory, read as broadcasts).  The segment's
+// errors then go through shared memory and the warps of later segments apply
+// them as one rank-32 update.  A group's min / max spans whole segments and is
+// reduced through shared memory as well.  The epilogue writes ΔW (split) back
+// to D / DL, the optional codes / Ŵ / row errors, the scales, and packs codes
+// and zero points into 32-bit words (coalesced word-rows of 32 output rows).
 #include "common.cuh"
 
 namespace gq {
 namespace {
 
-constexpr int ROWS = 32;                   // rows per CTA (4 warps x 8 rows)
-constexpr int SEG = 32;                    // block columns per lane (a quarter of the block)
+constexpr int ROWS = 32;                   // rows per CTA: one per lane
+constexpr int SEG = 32;                    // block columns per segment: one warp each
 constexpr int MAXB = 128;                  // max block width
+constexpr int NSEG = MAXB / SEG;           // segments (warps) per CTA
+constexpr int NTHREADS = NSEG * 32;        // 128
 constexpr int MAXG = MAXB / 32;            // max groups per block (group >= 32)
+constexpr int ELD = SEG + 1;               // row stride of the error staging (conflict-free column reads)
+
+struct SweepSmem {
+    float U[MAXB][MAXB];            // Uinv_b, upper triangle (lower part zero); read as broadcasts
+    float fdiag[MAXB];              // F_jj = 1 / U_jj
+    float E[NSEG][ROWS][ELD];       // scaled errors of each segment, per row
+    float gmin[NSEG][ROWS];         // group min / max contributions of each segment
+    float gmax[NSEG][ROWS];
+    float gs[ROWS], ginv[ROWS], gz[ROWS];  // grid of the current group, per row
+    float err[NSEG][ROWS];          // per-segment sums of e_j^2
+    uint8_t codes[ROWS][MAXB + 16]; // codes of the block (rows 16-byte aligned, for the packing epilogue)
+    uint8_t zeros[MAXG][ROWS];      // staging for the qzeros packing
+    float scales[MAXG][ROWS];       // staging for coalesced scale stores
+};
 
 // Word w of the little-endian bitstream of BITS-bit values v[0..]: bits [32w, 32w + 32).
 template <int BITS>
@@ -80,31 +106,8 @@ __device__ __forceinline__ float tf32_hi(float x) {
     return __uint_as_float(r);
 }
 
-// The block sweep, four lanes per row.  A warp holds 8 rows; lane
-// 4 r + q holds columns [32 q, 32 q + 32) of the block of row r in registers,
-// so every warp of the CTA (4 warps, 32 rows) runs its own rows' column chain
-// and no barrier is needed inside the block.  At column j = 32 qo + jj the
-// lane of quarter qo quantizes its row's weight, the error goes to the row's
-// other lanes by one shuffle, and every lane updates its 32 columns with row j
-// of Uinv_b (shared memory; the quarters are 36 floats apart so the four
-// quarter addresses of a warp's load fall in different banks).  Columns left
-// of j meet zeros of the triangular Uinv_b and column j itself is no longer
-// read, so the update needs no predicate.  At a group's first column its
-// min / max is reduced over the row's lanes by two shuffles.  The epilogue
-// recomputes ŵ from the codes and the lane's grid and writes ΔW = w0 - ŵ
-// (split), the optional codes / Ŵ / row errors, the scales, the packed words of
-// its own 32 columns (32 b bits = b words) and, through shared memory, the
-// packed zero points of the CTA's 32 rows.
-constexpr int QLD = 36;  // shared-memory floats per quarter row of Uinv_b
-
-struct SweepRowsSmem {
-    float U[MAXB][4 * QLD];   // Uinv_b, quarter-skewed; zero below the diagonal and beyond bw
-    float fdiag[MAXB];        // F_jj = 1 / U_jj
-    uint8_t zeros[MAXG][ROWS];
-};
-
 template <int BITS, typename TW>
-__global__ void __launch_bounds__(128) sweep_rows_kernel(const TW *__restrict__ W, int64_t rows, int64_t cols,
+__global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ W, int64_t rows, int64_t cols,
                                                          int64_t c0, int bw, const float *__restrict__ Uinv,
                                                          const float *__restrict__ F, const uint8_t *__restrict__ dead,
                                                          int group, float *__restrict__ D, float *__restrict__ DL,
@@ -114,24 +117,23 @@ __global__ void __launch_bounds__(128) sweep_rows_kernel(const TW *__restrict__ 
     pdl_trigger();
     pdl_wait();  // D was last updated by the previous kernel
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    SweepRowsSmem &sm = *reinterpret_cast<SweepRowsSmem *>(smem_raw);
+    SweepSmem &sm = *reinterpret_cast<SweepSmem *>(smem_raw);
     constexpr float maxq = (float)((1 << BITS) - 1);
-    const unsigned full = 0xffffffffu;
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rr = warp * 8 + (lane >> 2);  // row within the CTA
-    const int q = lane & 3;                 // quarter of the block this lane holds
+    const int seg = threadIdx.x >> 5, r = threadIdx.x & 31;  // warp = segment, lane = row
     const int64_t row0 = (int64_t)blockIdx.x * ROWS;
-    const int64_t row = row0 + rr;
+    const int64_t row = row0 + r;
     const bool row_on = row < rows;
-    const int nq = bw / SEG;                // quarters in use
-    const bool q_on = q < nq;
-    const int gq = group / SEG;             // quarters per group
+    const int nseg = bw / SEG;
+    const int cl = seg * SEG;  // first block column of this warp
+    const bool seg_on = seg < nseg;
+    const int gseg = group / SEG;  // segments per group
 
-    // Uinv_b into shared memory (quarter-skewed rows) with 16-byte asynchronous copies.
-    for (int idx = threadIdx.x; idx < MAXB * MAXB / 4; idx += 128) {
+    // Uinv_b into shared memory with asynchronous 16-byte copies, all in flight
+    // at once (the block's rows and columns beyond bw are zero-filled).
+    for (int idx = threadIdx.x; idx < MAXB * MAXB / 4; idx += NTHREADS) {
         const int i = idx / (MAXB / 4), j4 = (idx % (MAXB / 4)) * 4;
-        float *dst = &sm.U[i][(j4 / SEG) * QLD + (j4 % SEG)];
+        float *dst = &sm.U[i][j4];
         if (i < bw && j4 < bw) {
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
                          "l"(Uinv + (int64_t)i * bw + j4)
@@ -141,148 +143,180 @@ __global__ void __launch_bounds__(128) sweep_rows_kernel(const TW *__restrict__ 
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    for (int i = threadIdx.x; i < MAXB; i += 128) sm.fdiag[i] = (i < bw) ? F[(c0 + i) * cols + c0 + i] : 1.f;
+    for (int i = threadIdx.x; i < MAXB; i += NTHREADS) sm.fdiag[i] = (i < bw) ? F[(c0 + i) * cols + c0 + i] : 1.f;
 
-    // This lane's 32 columns: w0 (dead inputs zero) and w = w0 + D.
-    float w[SEG];
+    // This warp's segment of the row: the original weights w0 (dead inputs
+    // zero) and the weights as updated by every earlier block, w = w0 + D.
+    float w[SEG], w0[SEG];
     uint32_t dmask = 0;
 #pragma unroll
-    for (int c = 0; c < SEG; ++c) w[c] = 0.f;
-    if (q_on && row_on) {
-        float w0[SEG], t[SEG];
-        load32<TW>(W + row * cols + c0 + q * SEG, w0);
-        load32<float>(D + row * cols + c0 + q * SEG, t);
+    for (int c = 0; c < SEG; ++c) {
+        w[c] = 0.f;
+        w0[c] = 0.f;
+    }
+    if (seg_on && row_on) {
+        float t[SEG];
+        load32<TW>(W + row * cols + c0 + cl, w0);
+        load32<float>(D + row * cols + c0 + cl, t);
         if (dead) {
 #pragma unroll
-            for (int c = 0; c < SEG; ++c) dmask |= (dead[c0 + q * SEG + c] != 0 ? 1u : 0u) << c;
+            for (int c = 0; c < SEG; ++c) dmask |= (dead[c0 + cl + c] != 0 ? 1u : 0u) << c;
         }
 #pragma unroll
-        for (int c = 0; c < SEG; ++c) w[c] = (((dmask >> c) & 1u) ? 0.f : w0[c]) + t[c];
+        for (int c = 0; c < SEG; ++c) {
+            w0[c] = ((dmask >> c) & 1u) ? 0.f : w0[c];
+            w[c] = w0[c] + t[c];
+        }
     }
+    float e2 = 0.f;
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
 
-    float my_s = 1.f, my_inv = 1.f, my_z = 0.f;  // the grid of this lane's quarter
-    uint32_t cw[SEG / 4];                          // codes of this lane's columns, 8 bits each
-#pragma unroll
-    for (int k = 0; k < SEG / 4; ++k) cw[k] = 0u;
-    float e2 = 0.f;
-    const int src_base = lane & ~3;
-
-    for (int qo = 0; qo < nq; ++qo) {
-        if (qo % gq == 0) {
-            // A group starts: min / max over its quarters of the row, as updated by every earlier column.
-            const bool in_g = q >= qo && q < qo + gq && q_on;
-            float lo = 3.402823466e38f, hi = -3.402823466e38f;
-            if (in_g) {
+    for (int s = 0; s < nseg; ++s) {
+        if (s % gseg == 0) {
+            // A group starts at segment s: min / max over its segments s .. s + gseg - 1,
+            // whose weights carry every update from the columns before it.
+            if (seg >= s && seg < s + gseg) {
+                float lo = 3.402823466e38f, hi = -3.402823466e38f;
 #pragma unroll
                 for (int c = 0; c < SEG; ++c) {
                     lo = fminf(lo, w[c]);
                     hi = fmaxf(hi, w[c]);
                 }
+                sm.gmin[seg][r] = lo;
+                sm.gmax[seg][r] = hi;
             }
-            lo = fminf(lo, __shfl_xor_sync(full, lo, 1));
-            hi = fmaxf(hi, __shfl_xor_sync(full, hi, 1));
-            lo = fminf(lo, __shfl_xor_sync(full, lo, 2));
-            hi = fmaxf(hi, __shfl_xor_sync(full, hi, 2));
-            float xmin = fminf(lo, 0.f), xmax = fmaxf(hi, 0.f);
-            if (xmin == 0.f && xmax == 0.f) {
-                xmin = -1.f;
-                xmax = 1.f;
+            __syncthreads();
+            if (seg == s) {
+                float lo = sm.gmin[s][r], hi = sm.gmax[s][r];
+                for (int k = 1; k < gseg; ++k) {
+                    lo = fminf(lo, sm.gmin[s + k][r]);
+                    hi = fmaxf(hi, sm.gmax[s + k][r]);
+                }
+                float xmin = fminf(lo, 0.f), xmax = fmaxf(hi, 0.f);
+                if (xmin == 0.f && xmax == 0.f) {
+                    xmin = -1.f;
+                    xmax = 1.f;
+                }
+                const float sc = __fdiv_rn(xmax - xmin, maxq);
+                sm.gs[r] = sc;
+                sm.ginv[r] = __fdiv_rn(1.f, sc);
+                sm.gz[r] = rintf(__fdiv_rn(-xmin, sc));
+                sm.zeros[(s * SEG) / group][r] = (uint8_t)sm.gz[r];
+                sm.scales[(s * SEG) / group][r] = sc;
             }
-            const float sc = __fdiv_rn(xmax - xmin, maxq);
-            if (in_g) {
-                my_s = sc;
-                my_inv = __fdiv_rn(1.f, sc);
-                my_z = rintf(__fdiv_rn(-xmin, sc));
-            }
-            if (q == qo) sm.zeros[(qo * SEG) / group][rr] = (uint8_t)rintf(__fdiv_rn(-xmin, sc));
         }
-        const bool owner = (q == qo);
-        const float *ub = &sm.U[qo * SEG][q * QLD];
+        if (seg == s) {
+            // The segment's 32 columns, one after the other; every lane (row) quantizes
+            // its own weight, and the error updates the rest of the segment in registers.
+            const float sc = sm.gs[r], inv_s = sm.ginv[r], z = sm.gz[r];
+            float wq[SEG], ebuf[SEG];
+            uint32_t cw[SEG / 4];
 #pragma unroll
-        for (int jj = 0; jj < SEG; ++jj) {
-            float e = 0.f;
-            if (owner) {
-                const float wv = w[jj];
-                const float qv = fminf(fmaxf(rint_div(wv, my_s, my_inv) + my_z, 0.f), maxq);
-                cw[jj / 4] |= ((uint32_t)qv) << (8 * (jj % 4));
-                e = (wv - my_s * (qv - my_z)) * sm.fdiag[qo * SEG + jj];
+            for (int k = 0; k < SEG / 4; ++k) cw[k] = 0u;
+#pragma unroll
+            for (int ci = 0; ci < SEG; ++ci) {
+                const int j = cl + ci;
+                const float wv = w[ci];
+                const float q = fminf(fmaxf(rint_div(wv, sc, inv_s) + z, 0.f), maxq);
+                const float dq = sc * (q - z);
+                wq[ci] = dq;
+                cw[ci / 4] |= ((uint32_t)q) << (8 * (ci % 4));
+                const float e = (wv - dq) * sm.fdiag[j];
+                ebuf[ci] = e;
                 e2 = fmaf(e, e, e2);
-            }
-            e = __shfl_sync(full, e, src_base | qo);
-            const float *ur = ub + jj * (4 * QLD);
+                // Uinv_b is upper triangular: only the later columns of the segment move here.
 #pragma unroll
-            for (int c4 = 0; c4 < SEG; c4 += 4) {
-                const float4 u = *reinterpret_cast<const float4 *>(ur + c4);
-                w[c4 + 0] = fmaf(-e, u.x, w[c4 + 0]);
-                w[c4 + 1] = fmaf(-e, u.y, w[c4 + 1]);
-                w[c4 + 2] = fmaf(-e, u.z, w[c4 + 2]);
-                w[c4 + 3] = fmaf(-e, u.w, w[c4 + 3]);
+                for (int c4 = ((ci + 1) / 4) * 4; c4 < SEG; c4 += 4) {
+                    const float4 u = *reinterpret_cast<const float4 *>(&sm.U[j][cl + c4]);
+                    if (c4 + 0 > ci) w[c4 + 0] = fmaf(-e, u.x, w[c4 + 0]);
+                    if (c4 + 1 > ci) w[c4 + 1] = fmaf(-e, u.y, w[c4 + 1]);
+                    if (c4 + 2 > ci) w[c4 + 2] = fmaf(-e, u.z, w[c4 + 2]);
+                    if (c4 + 3 > ci) w[c4 + 3] = fmaf(-e, u.w, w[c4 + 3]);
+                }
+            }
+#pragma unroll
+            for (int ci = 0; ci < SEG; ++ci) sm.E[s][r][ci] = ebuf[ci];
+            *reinterpret_cast<uint4 *>(&sm.codes[r][cl]) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            *reinterpret_cast<uint4 *>(&sm.codes[r][cl + 16]) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            if (row_on) {
+                float *dp = D + row * cols + c0 + cl;
+                float *lp = DL + row * cols + c0 + cl;
+#pragma unroll
+                for (int c = 0; c < SEG; c += 4) {
+                    // ΔW as its TF32 split: the operand of the deferred-update GEMMs.
+                    float dw[4], dh[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        dw[u] = w0[c + u] - wq[c + u];
+                        dh[u] = tf32_hi(dw[u]);
+                    }
+                    *reinterpret_cast<float4 *>(dp + c) = make_float4(dh[0], dh[1], dh[2], dh[3]);
+                    *reinterpret_cast<float4 *>(lp + c) =
+                        make_float4(dw[0] - dh[0], dw[1] - dh[1], dw[2] - dh[2], dw[3] - dh[3]);
+                    if (W_hat)
+                        *reinterpret_cast<float4 *>(W_hat + row * cols + c0 + cl + c) =
+                            make_float4(wq[c], wq[c + 1], wq[c + 2], wq[c + 3]);
+                }
             }
         }
+        __syncthreads();
+        if (seg > s && seg_on) {
+            // Rank-32 update of this warp's segment by segment s: w -= E_s U[seg s, this segment].
+#pragma unroll 4
+            for (int i = 0; i < SEG; ++i) {
+                const float ei = sm.E[s][r][i];
+                const float *ur = &sm.U[s * SEG + i][cl];
+#pragma unroll
+                for (int c4 = 0; c4 < SEG; c4 += 4) {
+                    const float4 u = *reinterpret_cast<const float4 *>(ur + c4);
+                    w[c4 + 0] = fmaf(-ei, u.x, w[c4 + 0]);
+                    w[c4 + 1] = fmaf(-ei, u.y, w[c4 + 1]);
+                    w[c4 + 2] = fmaf(-ei, u.z, w[c4 + 2]);
+                    w[c4 + 3] = fmaf(-ei, u.w, w[c4 + 3]);
+                }
+            }
+        }
+        __syncthreads();
     }
 
-    // Row errors: the owners' sums over the row's lanes.
-    e2 += __shfl_xor_sync(full, e2, 1);
-    e2 += __shfl_xor_sync(full, e2, 2);
-    if (q == 0 && row_on && row_err) row_err[row] += e2;
-
-    if (q_on && row_on) {
-        // ΔW = w0 - ŵ (split), Ŵ, codes.
-        float w0[SEG];
-        load32<TW>(W + row * cols + c0 + q * SEG, w0);
-        float *dp = D + row * cols + c0 + q * SEG;
-        float *lp = DL + row * cols + c0 + q * SEG;
-#pragma unroll
-        for (int c = 0; c < SEG; c += 4) {
-            float dh[4], dl[4], wq[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float qv = (float)((cw[(c + u) / 4] >> (8 * ((c + u) % 4))) & 0xffu);
-                wq[u] = my_s * (qv - my_z);
-                const float dw = (((dmask >> (c + u)) & 1u) ? 0.f : w0[c + u]) - wq[u];
-                dh[u] = tf32_hi(dw);
-                dl[u] = dw - dh[u];
-            }
-            *reinterpret_cast<float4 *>(dp + c) = make_float4(dh[0], dh[1], dh[2], dh[3]);
-            *reinterpret_cast<float4 *>(lp + c) = make_float4(dl[0], dl[1], dl[2], dl[3]);
-            if (W_hat)
-                *reinterpret_cast<float4 *>(W_hat + row * cols + c0 + q * SEG + c) =
-                    make_float4(wq[0], wq[1], wq[2], wq[3]);
-        }
-        if (codes) {
-            uint8_t *dst = codes + row * cols + c0 + q * SEG;
-            if (((uintptr_t)dst & 15) == 0) {
-                reinterpret_cast<uint4 *>(dst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                reinterpret_cast<uint4 *>(dst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-            } else {  // the library only requires 4-byte alignment of codes
-#pragma unroll
-                for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t *>(dst)[i] = cw[i];
-            }
-        }
-        // The group's scale, written by the lane of its first quarter.
-        if (q % gq == 0) scales[((c0 + q * SEG) / group) * rows + row] = my_s;
-        // qweight: the lane's 32 codes are words [q BITS, q BITS + BITS) of the block's stream.
-        uint32_t words[BITS];
-#pragma unroll
-        for (int k = 0; k < BITS; ++k) words[k] = 0u;
-#pragma unroll
-        for (int i = 0; i < SEG; ++i) {
-            const uint32_t cv = (cw[i / 4] >> (8 * (i % 4))) & 0xffu;
-            const int pos = i * BITS, wi = pos / 32, sh = pos % 32;
-            words[wi] |= cv << sh;
-            if (sh + BITS > 32) words[wi + 1] |= cv >> (32 - sh);
-        }
-        const int64_t w0i = c0 * BITS / 32 + q * BITS;
-#pragma unroll
-        for (int k = 0; k < BITS; ++k) qweight[(w0i + k) * rows + row] = (int32_t)words[k];
-    }
+    // Epilogue: row errors, codes, scales, packed words.
+    sm.err[seg][r] = e2;
     __syncthreads();
-    // qzeros [cols/group][rows*BITS/32]: BITS words per group for these 32 rows.
+    if (seg == 0 && row_on && row_err) {
+        float t = 0.f;
+        for (int k = 0; k < nseg; ++k) t += sm.err[k][r];
+        row_err[row] += t;
+    }
+    if (codes && row_on && seg_on) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(&sm.codes[r][cl]);
+        uint8_t *dst = codes + row * cols + c0 + cl;
+        if (((uintptr_t)dst & 15) == 0) {
+            reinterpret_cast<uint4 *>(dst)[0] = src[0];
+            reinterpret_cast<uint4 *>(dst)[1] = src[1];
+        } else {  // the library only requires 4-byte alignment of codes
+            const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t *>(dst)[i] = s32[i];
+        }
+    }
+
+    // scales [cols/group][rows]: 32 consecutive rows per group.
     const int ng = bw / group;
+    for (int idx = threadIdx.x; idx < ng * ROWS; idx += NTHREADS) {
+        const int g = idx / ROWS, rr = idx % ROWS;
+        if (row0 + rr < rows) scales[((c0 / group) + g) * rows + row0 + rr] = sm.scales[g][rr];
+    }
+    // qweight [cols*BITS/32][rows]: words of this block, one word-row of 32 rows at a time.
+    const int nw = bw * BITS / 32;
+    const int64_t w0i = c0 * BITS / 32;
+    for (int idx = threadIdx.x; idx < nw * ROWS; idx += NTHREADS) {
+        const int wi = idx / ROWS, rr = idx % ROWS;
+        if (row0 + rr < rows) qweight[(w0i + wi) * rows + row0 + rr] = (int32_t)pack_word<BITS>(sm.codes[rr], wi, bw);
+    }
+    // qzeros [cols/group][rows*BITS/32]: BITS words per group for these 32 rows.
     const int64_t zw = rows * BITS / 32;
-    for (int idx = threadIdx.x; idx < ng * BITS; idx += 128) {
+    for (int idx = threadIdx.x; idx < ng * BITS; idx += NTHREADS) {
         const int g = idx / BITS, wi = idx % BITS;
         qzeros[((c0 / group) + g) * zw + row0 * BITS / 32 + wi] = (int32_t)pack_word<BITS>(sm.zeros[g], wi, ROWS);
     }
@@ -390,16 +424,15 @@ cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, in
                          const float *F, const uint8_t *dead, int group, float *D, float *DL, int32_t *qweight,
                          float *scales,
                          int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s) {
-    const size_t smem = sizeof(SweepRowsSmem);
+    const size_t smem = sizeof(SweepSmem);
     static bool attr_set = false;  // per template instance
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(sweep_rows_kernel<BITS, TW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(sweep_kernel<BITS, TW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int th = timing_begin(TK_SWEEP, s);
-    const cudaError_t e = launch_pdl(sweep_rows_kernel<BITS, TW>, dim3((unsigned)((rows + ROWS - 1) / ROWS)), dim3(128),
+    const cudaError_t e = launch_pdl(sweep_kernel<BITS, TW>, dim3((unsigned)((rows + ROWS - 1) / ROWS)), dim3(NTHREADS),
                                      smem, s, W, rows, cols, c0, bw, Uinv, F, dead, group, D, DL, qweight, scales,
                                      qzeros, codes, W_hat, row_err);
     count_launch();
