@@ -97,3 +97,39 @@ def test_traffic_with_a_stale_hash_or_no_record(tmp_path, monkeypatch):
     os.remove(os.path.join(str(tmp_path), "profiles", "hessian_traffic.json"))
     assert bench._read_traffic("llama7b_q_proj_4096x4096") is None
 
+
+
+class _KT:
+    """A stand-in for the library's per-class timing record."""
+
+    def __init__(self, ms, flops, count):
+        self.ms, self.flops, self.count = ms, flops, count
+
+
+def test_phase_rooflines_arithmetic():
+    """Each phase's roofline from its time and algorithmic work: the factor as cols^3/3 flops against
+    the 3xTF32 rate (measured bf16 burst x 1.1/2.25 / 3), sweep + pack as bytes against the HBM copy
+    rate with the chain floor cols x (block-kernel time per column step), the GEMM class as its
+    declared useful flops over its summed time."""
+    from synthetic import LAYERS
+
+    spec = LAYERS["llama7b_down_proj_4096x11008"]
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1800.0}
+    kt = _KT(ms={"hessian": 20.0, "gemm3": 8.0, "sweep": 2.0, "diag": 4.0, "gemm_tf32": 0.0},
+             flops={"hessian": 3.2e13, "gemm3": 9.6e11, "sweep": 0.0, "diag": 0.0, "gemm_tf32": 0.0},
+             count={"hessian": 1, "gemm3": 250, "sweep": 86, "diag": 86, "gemm_tf32": 0})
+    phase = {"hessian": 20.0, "factor": 8.0, "sweep": 6.0}
+    out = bench.phase_rooflines(spec, phase, kt, peaks, "measured", codes=False, w_hat=False)
+    tf32x3 = 1800.0 * 1.1 / 2.25 / 3
+    assert out["factor"]["peak"] == round(tf32x3, 1)
+    assert out["factor"]["achieved"] == round(11008 ** 3 / 3 / 8e-3 / 1e12, 2)
+    byt = 4096 * 11008 * 2 + 4096 * 11008 * 3 / 8 + (11008 // 128) * 4096 * (4 + 3 / 8) + 11008 * 4
+    assert bench.sweep_pack_bytes(spec, False, False) == byt
+    assert out["sweep_pack"]["achieved"] == round(byt / 6e-3 / 1e9, 1)
+    assert out["sweep_pack"]["column_step_ns"] == round(2.0e6 / (86 * 128), 2)
+    assert out["sweep_pack"]["chain_floor_ms"] == round(11008 * (2.0e6 / (86 * 128)) / 1e6, 4)
+    assert out["gemm3"]["achieved"] == round(9.6e11 / 8e-3 / 1e12, 2)
+    assert out["gemm3"]["frac"] == round(out["gemm3"]["achieved"] / tf32x3, 4)
+    assert out["hessian"]["frac"] == round(3.2e13 / 20e-3 / 1e12 / 1800.0, 4)
+    # optional outputs add their bytes
+    assert bench.sweep_pack_bytes(spec, True, True) == byt + 4096 * 11008 * 5
