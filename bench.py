@@ -439,7 +439,7 @@ def run_ours(args, rank: int, world: int):
         },
         "phases_ms": {k: round(v, 4) for k, v in phase.items()},
         "roofline": {
-            "kernel": "hessian_tc_kernel (H += 2 X^T X)",
+            "kernel": "hessian_pair_kernel (H += 2 X^T X)",
             "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
             "flops_per_launch": flops, "traffic": traffic,

@@ -130,7 +130,10 @@ cudaError_t sgemm_splitk(int64_t M, int64_t N, int64_t K, const float *A, int64_
 // C = beta C + alpha A B^T on the tensor cores with float32 accuracy (3xTF32):
 // A (M x K) and B (N x K), K contiguous, each given as its TF32 split
 // (hi, lo) with x = hi + lo.  tri = 1 skips the output tiles entirely above
-// the diagonal.  Optional Chi / Clo (may be NULL) receive the split of the
+// the diagonal; tri = 3 declares B lower triangular (B(k, n) = 0 for k > n,
+// i.e. row n of the N x K operand is zero beyond column n), and the CTA-pair
+// kernel then stops each tile's K loop after the tile's last column (the
+// other kernels take the zero products).  Optional Chi / Clo (may be NULL) receive the split of the
 // result (leading dimension ldcs).  Row strides must be multiples of 4
 // elements and operand bases 16-byte aligned (gemm3_supported).
 bool gemm3_supported(const void *p, int64_t ld);

@@ -46,6 +46,34 @@ __global__ void finish_kernel(const float *__restrict__ lam, int r, float *__res
     for (int64_t j = threadIdx.x; j < cols; j += blockDim.x) A[i * cols + j] *= sc;
 }
 
+// A[i][j] <- A[j][i] for i < j: the upper triangle of a symmetric n x n
+// matrix from its lower one (row stride lda).  One 32 x 32 tile of the upper
+// triangle per block (tiles below the diagonal return at once), read from
+// the mirrored lower tile and transposed through shared memory, so that both
+// the loads and the stores run along rows.
+__global__ void mirror_lower_kernel(float *__restrict__ A, int64_t n, int64_t lda) {
+    __shared__ float t[32][33];
+    const int64_t ti = blockIdx.y, tj = blockIdx.x;  // destination tile (ti, tj), ti <= tj
+    if (ti > tj) return;
+    const int tx = threadIdx.x, ty = threadIdx.y;     // 32 x 8 threads
+    for (int r = ty; r < 32; r += 8) {
+        const int64_t gi = tj * 32 + r, gj = ti * 32 + tx;  // source: rows of tile column tj
+        t[r][tx] = (gi < n && gj < n) ? A[gi * lda + gj] : 0.f;
+    }
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+        const int64_t gi = ti * 32 + r, gj = tj * 32 + tx;
+        if (gi < gj && gj < n) A[gi * lda + gj] = t[tx][r];
+    }
+}
+
+cudaError_t mirror_lower(float *A, int64_t n, int64_t lda, cudaStream_t s) {
+    const unsigned nt = (unsigned)((n + 31) / 32);
+    mirror_lower_kernel<<<dim3(nt, nt), dim3(32, 8), 0, s>>>(A, n, lda);
+    count_launch();
+    return cudaGetLastError();
+}
+
 struct EoraWs {
     DeviceStatus *st;
     float *Linv, *F, *M, *G, *ZT, *ZT2, *Gm, *part, *lam, *Wt, *VrT;
@@ -145,13 +173,18 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
         // M = dW F (rows x cols, also split), its transpose split, G = M^T M (cols x cols, also split).
         if ((e = split_transpose_tf32(w.F, cols, cols, cols, w.FThi, w.FTlo, cols, s)) != cudaSuccess) return e;
         if ((e = split_tf32(dW, rows, cols, cols, w.dWhi, w.dWlo, cols, s)) != cudaSuccess) return e;
-        if ((e = gemm3(rows, cols, cols, 1.f, w.dWhi, w.dWlo, cols, w.FThi, w.FTlo, cols, 0.f, w.M, cols, 0, w.Mhi,
+        // F is upper triangular, so F^T (the B operand) is lower: tri = 3 skips its zero products.
+        if ((e = gemm3(rows, cols, cols, 1.f, w.dWhi, w.dWlo, cols, w.FThi, w.FTlo, cols, 0.f, w.M, cols, 3, w.Mhi,
                        w.Mlo, cols, s)) != cudaSuccess)
             return e;
         if ((e = split_transpose_tf32(w.M, rows, cols, cols, w.Mthi, w.Mtlo, rows, s)) != cudaSuccess) return e;
-        if ((e = gemm3(cols, cols, rows, 1.f, w.Mthi, w.Mtlo, rows, w.Mthi, w.Mtlo, rows, 0.f, w.G, cols, 0, w.Ghi,
+        // G is symmetric: the tiles on and below the diagonal, then the upper triangle mirrored.
+        if ((e = gemm3(cols, cols, rows, 1.f, w.Mthi, w.Mtlo, rows, w.Mthi, w.Mtlo, rows, 0.f, w.G, cols, 1, w.Ghi,
                        w.Glo, cols, s)) != cudaSuccess)
             return e;
+        if ((e = mirror_lower(w.G, cols, cols, s)) != cudaSuccess) return e;
+        if ((e = mirror_lower(w.Ghi, cols, cols, s)) != cudaSuccess) return e;
+        if ((e = mirror_lower(w.Glo, cols, cols, s)) != cudaSuccess) return e;
     } else {
         // M = dW F, G = M^T M (symmetric).
         if ((e = sgemm<float>(rows, cols, cols, 1.f, dW, cols, false, w.F, cols, false, 0.f, w.M, cols, 0, s)) !=

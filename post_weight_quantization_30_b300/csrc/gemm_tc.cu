@@ -574,7 +574,8 @@ __global__ void __launch_bounds__(gsmall::NWARPS * 32, 1)
 // every stage either CTA issued.  Eight epilogue warps per CTA (one row and 128 columns
 // per thread) add the flushed partial sums and apply C = beta C + alpha A B^T
 // through shared memory, as above.  tri = 1 skips the pair tiles entirely above
-// the diagonal.  No split-K.
+// the diagonal; tri = 3 (B lower triangular: B(k, n) = 0 for k > n) stops each
+// tile's K loop after the tile's last column.  No split-K.
 namespace gpair {
 constexpr int PT = 256;                  // pair tile rows and columns
 constexpr int TILE = 128 * GK * 4;       // 16 KB: 128 rows x 32 K-values
@@ -614,7 +615,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gpair::NWARPS * 32, 
 
     unsigned char *smem = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ktiles = (K + GK - 1) / GK;
+    // tri = 3: B(k, n) = 0 for k > n, so this tile's columns n < n0 + PT need k < n0 + PT only.
+    const int keff = (tri == 3 && n0 + PT < K) ? n0 + PT : K;
+    const int ktiles = (keff + GK - 1) / GK;
     const int periods = (ktiles + KF - 1) / KF;
 
     if (threadIdx.x == 0) {
@@ -934,9 +937,13 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
     if (!make_map(&mah, Ahi, K, M, lda, GM) || !make_map(&mal, Alo, K, M, lda, GM) ||
         !make_map(&mbh, Bhi, K, N, ldb, GN) || !make_map(&mbl, Blo, K, N, ldb, GN))
         return cudaErrorInvalidValue;
-    // Useful products: all M x N outputs, or those on and below the diagonal for tri = 1.
+    // Useful products: all M x N outputs, or those on and below the diagonal for tri = 1;
+    // for tri = 3 (B lower triangular) output column n takes min(K, n + 1) products.
     const double outs = tri == 1 ? (M >= N ? (double)M * N - (double)N * (N - 1) / 2 : (double)M * (M + 1) / 2)
                                  : (double)M * N;
+    double prods = outs * (double)K;
+    if (tri == 3)
+        prods = (double)M * (N <= K ? (double)N * (N + 1) / 2 : (double)K * (K + 1) / 2 + (double)(N - K) * K);
     if (M > GM && N > GN) {
         // Wider than one tile both ways: 256 x 256 tiles on CTA pairs (the boxes stay 128 rows:
         // each CTA loads its 128 rows of A and its 128 of the pair's 256 rows of B).
@@ -946,10 +953,12 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
                                          mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta, tri, Chi, Clo, ldcs,
                                          split_row0, split_ncols);
         count_launch();
-        timing_end(th, s, 2.0 * outs * (double)K);
+        timing_end(th, s, 2.0 * prods);
         return e;
     }
     dim3 grid((unsigned)((N + GN - 1) / GN), (unsigned)((M + GM - 1) / GM));
+    // The one-CTA kernels know tri = 0 and 1 only; with tri = 3 they also take the (zero) products k > n.
+    const int tri1 = tri == 1 ? 1 : 0;
     if (N <= GN && K <= gsmall::MAX_K) {
         // One column tile, short K: the latency-bound shape of the serial chains.
         static bool small_attr = false;
@@ -961,19 +970,19 @@ cudaError_t gemm3(int64_t M, int64_t N, int64_t K, float alpha, const float *Ahi
         }
         const int th = timing_begin(TK_GEMM3, s);
         const cudaError_t e = launch_pdl(gemm3_small_kernel, grid, dim3(gsmall::NWARPS * 32), gsmall::SMEM, s, mah,
-                                         mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta, tri, Chi, Clo,
+                                         mal, mbh, mbl, C, ldc, (int)M, (int)N, (int)K, alpha, beta, tri1, Chi, Clo,
                                          ldcs, split_row0, split_ncols);
         count_launch();
-        timing_end(th, s, 2.0 * outs * (double)K);
+        timing_end(th, s, 2.0 * prods);
         return e;
     }
     const int kt_all = (int)((K + GK - 1) / GK);
     const int th = timing_begin(TK_GEMM3, s);
     const cudaError_t e = launch_pdl(gemm3_kernel, grid, dim3(G_NWARPS * 32), G_SMEM, s, mah, mal, mbh, mbl, C, ldc,
-                                     (int)M, (int)N, (int)K, alpha, beta, tri, Chi, Clo, ldcs, kt_all, (int64_t)0,
+                                     (int)M, (int)N, (int)K, alpha, beta, tri1, Chi, Clo, ldcs, kt_all, (int64_t)0,
                                      split_row0, split_ncols, 0);
     count_launch();
-    timing_end(th, s, 2.0 * outs * (double)K);
+    timing_end(th, s, 2.0 * prods);
     return e;
 }
 

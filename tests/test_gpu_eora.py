@@ -93,7 +93,11 @@ def test_planted_gap_matches_oracle_factors(gq):
     assert np.linalg.norm(g["A"] - A_o) / np.linalg.norm(A_o) <= 1e-3
 
 
-@pytest.mark.parametrize("rows,cols,r,bits,group", [(256, 256, 32, 2, 64), (160, 320, 16, 3, 64), (512, 128, 64, 2, 32)])
+# (384, 576): M = dW F and G = M^T M run on CTA pairs over three 256-column tiles, the last one ragged,
+# so the triangular-operand K bound (256, 512, then all 576) and the mirrored upper triangle of G
+# are both exercised.
+@pytest.mark.parametrize("rows,cols,r,bits,group", [(256, 256, 32, 2, 64), (160, 320, 16, 3, 64), (512, 128, 64, 2, 32),
+                                                    (384, 576, 32, 3, 64)])
 def test_gptq_error_of_a_layer(gq, rows, cols, r, bits, group):
     spec = custom_layer("e", rows, cols, 4 * cols, bits=bits, group=group, x_dist="normal",
                         n_outliers=max(1, cols // 100), key=(21, rows, cols))
