@@ -73,6 +73,41 @@ __global__ void reverse_damp_kernel(const float *__restrict__ H, int64_t cols, f
     if (bad) atomicAnd(&st->finite, ~kNonFiniteH);
 }
 
+// The same for cols % 4 == 0 and 16-byte aligned H and F, four entries of a
+// row of F per thread: F[p][q .. q + 3] come from one float4 of H's row
+// C - 1 - p (columns C - 4 - q .. C - 1 - q, reversed), so every thread has
+// its load in flight at once.  Only the entries with q <= p are taken (and
+// checked); the rest of the float4 belongs to H's other triangle.
+__global__ void reverse_damp4_kernel(const float *__restrict__ H, int64_t cols, float *__restrict__ F,
+                                     uint8_t *__restrict__ dead, DeviceStatus *__restrict__ st) {
+    const int64_t p = blockIdx.y;
+    const float delta = st->delta;
+    const float *hrow = H + (cols - 1 - p) * cols;
+    bool bad = false;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < cols / 4; v += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t q = 4 * v;
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+        if (q <= p) {
+            const float4 h = *reinterpret_cast<const float4 *>(hrow + (cols - 4 - q));
+            const float e[4] = {h.w, h.z, h.y, h.x};  // H[C-1-p][C-1-q-u]
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (q + u < p) {
+                    o[u] = e[u];
+                    bad |= !isfinite(e[u]);
+                } else if (q + u == p) {
+                    const int64_t i = cols - 1 - p;
+                    bad |= !isfinite(e[u]);
+                    if (dead) dead[i] = (e[u] == 0.f);
+                    o[u] = ((e[u] == 0.f) ? 1.f : e[u]) + delta;
+                }
+            }
+        }
+        *reinterpret_cast<float4 *>(F + p * cols + q) = make_float4(o[0], o[1], o[2], o[3]);
+    }
+    if (bad) atomicAnd(&st->finite, ~kNonFiniteH);
+}
+
 // Clears `bit` of st->finite if an element of X is an Inf or NaN (all exponent
 // bits set: 0x7F80 in bf16, 0x7F800000 in float32).  16-byte loads over the
 // aligned middle of the buffer, element loads at both ends.
@@ -121,8 +156,9 @@ __global__ void finite_check_kernel(const unsigned char *__restrict__ X, int64_t
 //   2. all warps solve the sub-panel below against it, X = A L_pp^-T, as a
 //      product with the sub-block's inverse (4 x 4 register tiles);
 //   3. all warps update the trailing lower triangle, A -= X X^T (4 x 4 tiles).
-// Finally the off-diagonal 32 x 32 blocks of L^-1 are assembled block row by
-// block row: Y_pq = -Y_pp sum_{q <= m < p} L_pm Y_mq (4 x 4 tiles).
+// The off-diagonal 32 x 32 blocks of L^-1 are assembled block row by block
+// row, Y_pq = -Y_pp sum_{q <= m < p} L_pm Y_mq (4 x 4 tiles): rows 1 and 2 by
+// six warps while warp 0 factors the sub-panel after them, row 3 at the end.
 // The pivot reciprocal square root comes from rsqrtf; the factor is d * rsqrt(d).
 constexpr int DIAG_THREADS = 256;
 constexpr int SP = 32;           // sub-panel width
@@ -195,10 +231,60 @@ __device__ __forceinline__ void warp_trinv32(const float *L, const float *dinv, 
     for (int i = 0; i < SP; ++i) YT[lane * LDA + i] = y[i];
 }
 
-// Optional outputs (may be NULL): Lhi / Llo, the TF32 split of Linv (NB x NB);
-// Urev, the index-reversed inverse Urev[i][j] = Linv[kb-1-i][kb-1-j] (kb x kb,
+// Block row p >= 1 of Y = L^-1 off the diagonal, by threads tid = 0 .. nthr - 1
+// in 4 x 4 tiles: T_q = sum_{m=q}^{p-1} L_pm Y_mq, then Y_pq = -Y_pp T_q, for
+// q < p (32 x 32 blocks; L in A, T scratch [3][SP][SP]).  It reads L's block
+// row p left of the diagonal, Y's block rows before p and Y_pp; `sync`
+// separates the two products among the nthr threads.
+template <typename Sync>
+__device__ __forceinline__ void inverse_block_row(int p, int tid, int nthr, const float *A, float *Y, float *T,
+                                                  Sync sync) {
+    const int ntl = p * (SP / 4) * (SP / 4);
+    for (int tl = tid; tl < ntl; tl += nthr) {
+        const int q = tl / 64, i0 = ((tl / 8) % 8) * 4, c0 = (tl % 8) * 4;
+        float acc[4][4] = {};
+        for (int k = q * SP; k < p * SP; ++k) {
+            const float4 yv = *reinterpret_cast<const float4 *>(Y + k * LDA + q * SP + c0);
+            const float yb[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const float lv = A[(p * SP + i0 + a) * LDA + k];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(lv, yb[b], acc[a][b]);
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+            *reinterpret_cast<float4 *>(T + q * SP * SP + (i0 + a) * SP + c0) =
+                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+    }
+    sync();
+    for (int tl = tid; tl < ntl; tl += nthr) {
+        const int q = tl / 64, i0 = ((tl / 8) % 8) * 4, c0 = (tl % 8) * 4;
+        const float *tq = T + q * SP * SP;
+        float acc[4][4] = {};
+        for (int k = 0; k < i0 + 4; ++k) {
+            const float4 tv = *reinterpret_cast<const float4 *>(tq + k * SP + c0);
+            const float tb[4] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const float yv = Y[(p * SP + i0 + a) * LDA + p * SP + k];  // zero for k > i0 + a
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(yv, tb[b], acc[a][b]);
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+            *reinterpret_cast<float4 *>(Y + (p * SP + i0 + a) * LDA + q * SP + c0) =
+                make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
+    }
+}
+
+// Outputs: Linv, the inverse (NB x NB), written only when Lhi is NULL; when
+// Lhi / Llo are given they receive its TF32 split instead (the form the panel
+// solve reads).  Optional (may be NULL): Urev, the index-reversed inverse Urev[i][j] = Linv[kb-1-i][kb-1-j] (kb x kb,
 // row stride kb): the inverse of the matching diagonal block of F = J L J.
-__global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restrict__ F, int64_t cols, int64_t k0,
+__global__ void __launch_bounds__(DIAG_THREADS, 1) potrf_diag_kernel(float *__restrict__ F, int64_t cols, int64_t k0,
                                                                   int kb, float *__restrict__ Linv,
                                                                   DeviceStatus *st, float *__restrict__ Lhi,
                                                                   float *__restrict__ Llo, float *__restrict__ Urev) {
@@ -265,6 +351,12 @@ __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restr
             // Diagonal block of Y from its transposed copy.
 #pragma unroll 4
             for (int i = 0; i < SP; ++i) Y[(c0 + i) * LDA + c0 + lane] = YT[lane * LDA + i];
+        } else if (c0 >= 2 * SP && (warp & 3) != 0) {
+            // While warp 0 factors this sub-panel, six other warps form the previous block
+            // row of the inverse: everything it reads is final, and nothing the factorization
+            // touches is written.  Warp 4 stays idle: it would share warp 0's scheduler.
+            inverse_block_row(c0 / SP - 1, (warp - 1 - (warp >> 2)) * 32 + lane, 192, A, Y, T,
+                              [] { asm volatile("bar.sync 1, 192;" ::: "memory"); });
         }
         __syncthreads();
         const int r0 = c0 + SP, R = NB - r0;  // rows below the diagonal sub-block
@@ -331,53 +423,13 @@ __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restr
         __syncthreads();
     }
 
-    // Off-diagonal blocks of Y = L^-1, one block row p at a time, 4 x 4 tiles:
-    // T_q = sum_{m=q}^{p-1} L_pm Y_mq, then Y_pq = -Y_pp T_q, for q < p.
-    for (int p = 1; p < NB / SP; ++p) {
-        const int ntl = p * (SP / 4) * (SP / 4);
-        for (int tl = t; tl < ntl; tl += DIAG_THREADS) {
-            const int q = tl / 64, i0 = ((tl / 8) % 8) * 4, c0 = (tl % 8) * 4;
-            float acc[4][4] = {};
-            for (int k = q * SP; k < p * SP; ++k) {
-                const float4 yv = *reinterpret_cast<const float4 *>(Y + k * LDA + q * SP + c0);
-                const float yb[4] = {yv.x, yv.y, yv.z, yv.w};
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    const float lv = A[(p * SP + i0 + a) * LDA + k];
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(lv, yb[b], acc[a][b]);
-                }
-            }
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-                *reinterpret_cast<float4 *>(T + q * SP * SP + (i0 + a) * SP + c0) =
-                    make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-        }
-        __syncthreads();
-        for (int tl = t; tl < ntl; tl += DIAG_THREADS) {
-            const int q = tl / 64, i0 = ((tl / 8) % 8) * 4, c0 = (tl % 8) * 4;
-            const float *tq = T + q * SP * SP;
-            float acc[4][4] = {};
-            for (int k = 0; k < i0 + 4; ++k) {
-                const float4 tv = *reinterpret_cast<const float4 *>(tq + k * SP + c0);
-                const float tb[4] = {tv.x, tv.y, tv.z, tv.w};
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    const float yv = Y[(p * SP + i0 + a) * LDA + p * SP + k];  // zero for k > i0 + a
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(yv, tb[b], acc[a][b]);
-                }
-            }
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-                *reinterpret_cast<float4 *>(Y + (p * SP + i0 + a) * LDA + q * SP + c0) =
-                    make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
-        }
-        __syncthreads();
-    }
+    // The last block row of Y = L^-1 (the earlier ones were formed during the
+    // factorization of the sub-panel after them).
+    inverse_block_row(NB / SP - 1, t, DIAG_THREADS, A, Y, T, [] { __syncthreads(); });
+    __syncthreads();
 
     // Store: F gets the lower factor (its part above the diagonal is zero in A),
-    // Linv the inverse; padding rows / columns are not written to F.
+    // Linv the inverse or its split; padding rows / columns are not written to F.
 #pragma unroll 4
     for (int u = 0; u < NB * NB / 4 / DIAG_THREADS; ++u) {
         const int idx = t + u * DIAG_THREADS;
@@ -398,15 +450,27 @@ __global__ void __launch_bounds__(DIAG_THREADS) potrf_diag_kernel(float *__restr
         if (j + 1 >= kb) yv.y = 0.f;
         if (j + 2 >= kb) yv.z = 0.f;
         if (j + 3 >= kb) yv.w = 0.f;
-        *reinterpret_cast<float4 *>(Linv + idx * 4) = yv;
-        if (Lhi) {
+        if (!Lhi) {
+            *reinterpret_cast<float4 *>(Linv + idx * 4) = yv;
+        } else {
             const float h[4] = {tf32_round(yv.x), tf32_round(yv.y), tf32_round(yv.z), tf32_round(yv.w)};
             *reinterpret_cast<float4 *>(Lhi + idx * 4) = make_float4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<float4 *>(Llo + idx * 4) =
                 make_float4(yv.x - h[0], yv.y - h[1], yv.z - h[2], yv.w - h[3]);
         }
     }
-    if (Urev) {
+    if (Urev && kb == NB) {
+        // Four reversed columns at a time: Urev[i][j .. j + 3] = Y[ri][rj - 3 .. rj] backwards,
+        // rj = NB - 1 - j (rj - 3 is a multiple of 4), zero where the column is above the diagonal.
+        for (int idx = t; idx < NB * NB / 4; idx += DIAG_THREADS) {
+            const int i = idx / (NB / 4), j = (idx % (NB / 4)) * 4;
+            const int ri = NB - 1 - i, rj = NB - 1 - j;
+            const float4 y = *reinterpret_cast<const float4 *>(Y + ri * LDA + rj - 3);
+            const float4 o = make_float4(rj <= ri ? y.w : 0.f, rj - 1 <= ri ? y.z : 0.f, rj - 2 <= ri ? y.y : 0.f,
+                                         rj - 3 <= ri ? y.x : 0.f);
+            *reinterpret_cast<float4 *>(Urev + idx * 4) = o;
+        }
+    } else if (Urev) {
         for (int idx = t; idx < kb * kb; idx += DIAG_THREADS) {
             const int i = idx / kb, j = idx % kb;
             const int ri = kb - 1 - i, rj = kb - 1 - j;
@@ -434,14 +498,49 @@ __global__ void finalize_kernel(float *__restrict__ F, int64_t cols) {
     }
 }
 
+// The same for cols % 4 == 0 and a 16-byte aligned F: the lower-triangle
+// float4 F[p][q .. q + 3] with q + 3 < p goes reversed to F[C-1-p][C-4-q ..
+// C-1-q] (upper triangle, written by this thread only) and is zeroed; the
+// float4 that holds the diagonal entry is done element by element.
+__global__ void finalize4_kernel(float *__restrict__ F, int64_t cols) {
+    const int64_t p = blockIdx.y;
+    const int64_t p2 = cols - 1 - p;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; 4 * v <= p; v += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t q = 4 * v;
+        if (q + 3 < p) {
+            const float4 a = *reinterpret_cast<const float4 *>(F + p * cols + q);
+            *reinterpret_cast<float4 *>(F + p2 * cols + (cols - 4 - q)) = make_float4(a.w, a.z, a.y, a.x);
+            *reinterpret_cast<float4 *>(F + p * cols + q) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            for (int64_t qq = q; qq <= p; ++qq) {
+                if (qq == p) {
+                    if (p < p2) {
+                        const float a = F[p * cols + p], b = F[p2 * cols + p2];
+                        F[p * cols + p] = b;
+                        F[p2 * cols + p2] = a;
+                    }
+                } else {
+                    F[p2 * cols + (cols - 1 - qq)] = F[p * cols + qq];
+                    F[p * cols + qq] = 0.f;
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t factor_prepare(const float *H, int64_t cols, float damp, float *F, uint8_t *dead,
                            DeviceStatus *st, cudaStream_t s) {
     diag_sum_kernel<<<1, 1024, 0, s>>>(H, cols, damp, st);
     count_launch();
-    dim3 grid((unsigned)((cols + 255) / 256 < 8 ? (cols + 255) / 256 : 8), (unsigned)cols);
-    reverse_damp_kernel<<<grid, 256, 0, s>>>(H, cols, F, dead, st);
+    if (cols % 4 == 0 && ((uintptr_t)H % 16) == 0 && ((uintptr_t)F % 16) == 0) {
+        reverse_damp4_kernel<<<dim3((unsigned)((cols / 4 + 255) / 256), (unsigned)cols), 256, 0, s>>>(H, cols, F, dead,
+                                                                                                     st);
+    } else {
+        dim3 grid((unsigned)((cols + 255) / 256 < 8 ? (cols + 255) / 256 : 8), (unsigned)cols);
+        reverse_damp_kernel<<<grid, 256, 0, s>>>(H, cols, F, dead, st);
+    }
     count_launch();
     return cudaGetLastError();
 }
@@ -598,6 +697,11 @@ cudaError_t cholesky_lower_inplace(float *F, int64_t cols, DeviceStatus *st, flo
 }
 
 cudaError_t factor_finalize(float *F, int64_t cols, cudaStream_t s) {
+    if (cols % 4 == 0 && ((uintptr_t)F % 16) == 0) {
+        finalize4_kernel<<<dim3((unsigned)((cols / 4 + 255) / 256), (unsigned)cols), 256, 0, s>>>(F, cols);
+        count_launch();
+        return cudaGetLastError();
+    }
     dim3 grid((unsigned)((cols + 255) / 256 < 8 ? (cols + 255) / 256 : 8), (unsigned)cols);
     finalize_kernel<<<grid, 256, 0, s>>>(F, cols);
     count_launch();

@@ -19,9 +19,12 @@
 // w / s, see rint_div), forms the scaled error e_j = (w_j - ŵ_j) F_jj
 // (= (w_j - ŵ_j) / U_jj) and updates the rest of the segment in registers
 // with row j of Uinv_b (shared memory, read as broadcasts).  The segment's
-// errors then go through shared memory and the warps of later segments apply
-// them as one rank-32 update.  A group's min / max spans whole segments and is
-// reduced through shared memory as well.  The epilogue writes ΔW (split) back
+// errors go through shared memory in chunks of 8 columns: after each chunk
+// the sweeping warp arrives on a named barrier, and the warps of later
+// segments wait on it and apply the chunk as a rank-8 update while the sweep
+// of the next chunk runs, so that only the last chunk's update separates one
+// segment's sweep from the next.  A group's min / max spans whole segments and
+// is reduced through shared memory as well.  The epilogue writes ΔW (split) back
 // to D / DL, the optional codes / Ŵ / row errors, the scales, and packs codes
 // and zero points into 32-bit words (coalesced word-rows of 32 output rows).
 #include "common.cuh"
@@ -36,15 +39,23 @@ constexpr int NSEG = MAXB / SEG;           // segments (warps) per CTA
 constexpr int NTHREADS = NSEG * 32;        // 128
 constexpr int MAXG = MAXB / 32;            // max groups per block (group >= 32)
 constexpr int ELD = SEG + 1;               // row stride of the error staging (conflict-free column reads)
+constexpr int CH = 8;                      // columns per published chunk of errors
+constexpr int NCH = SEG / CH;              // chunks per segment: named barriers 1 .. NCH
 
 struct SweepSmem {
     float U[MAXB][MAXB];            // Uinv_b, upper triangle (lower part zero); read as broadcasts
     float fdiag[MAXB];              // F_jj = 1 / U_jj
-    float E[NSEG][ROWS][ELD];       // scaled errors of each segment, per row
-    float gmin[NSEG][ROWS];         // group min / max contributions of each segment
-    float gmax[NSEG][ROWS];
+    // Three stagings that are never live at the same time share one region, which
+    // keeps the block under a third of the SM's shared memory (three CTAs per SM):
+    union {
+        float E[ROWS][ELD];         // scaled errors of the segment being swept, per row
+        struct {
+            float gmin[NSEG][ROWS]; // group min / max contributions of each segment (group start)
+            float gmax[NSEG][ROWS];
+        };
+        float err[NSEG][ROWS];      // per-segment sums of e_j^2 (epilogue)
+    };
     float gs[ROWS], ginv[ROWS], gz[ROWS];  // grid of the current group, per row
-    float err[NSEG][ROWS];          // per-segment sums of e_j^2
     uint8_t codes[ROWS][MAXB + 16]; // codes of the block (rows 16-byte aligned, for the packing epilogue)
     uint8_t zeros[MAXG][ROWS];      // staging for the qzeros packing
     float scales[MAXG][ROWS];       // staging for coalesced scale stores
@@ -106,6 +117,16 @@ __device__ __forceinline__ float tf32_hi(float x) {
     return __uint_as_float(r);
 }
 
+// Named barriers (ids 1 .. NCH; 0 is __syncthreads): the sweeping warp
+// arrives without waiting, the warps that consume its errors wait.  Both sides
+// give the same thread count, 32 x (1 + consumers).
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 template <int BITS, typename TW>
 __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ W, int64_t rows, int64_t cols,
                                                          int64_t c0, int bw, const float *__restrict__ Uinv,
@@ -115,7 +136,6 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                                                          int32_t *__restrict__ qzeros, uint8_t *__restrict__ codes,
                                                          float *__restrict__ W_hat, float *__restrict__ row_err) {
     pdl_trigger();
-    pdl_wait();  // D was last updated by the previous kernel
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SweepSmem &sm = *reinterpret_cast<SweepSmem *>(smem_raw);
     constexpr float maxq = (float)((1 << BITS) - 1);
@@ -129,6 +149,9 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
     const bool seg_on = seg < nseg;
     const int gseg = group / SEG;  // segments per group
 
+    // Uinv_b, F's diagonal, W and the dead mask were complete before the first
+    // kernel of the sweep started, so they are read before waiting for the
+    // previous kernel; D, which that kernel updates, is read after.
     // Uinv_b into shared memory with asynchronous 16-byte copies, all in flight
     // at once (the block's rows and columns beyond bw are zero-filled).
     for (int idx = threadIdx.x; idx < MAXB * MAXB / 4; idx += NTHREADS) {
@@ -155,13 +178,16 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
         w0[c] = 0.f;
     }
     if (seg_on && row_on) {
-        float t[SEG];
         load32<TW>(W + row * cols + c0 + cl, w0);
-        load32<float>(D + row * cols + c0 + cl, t);
         if (dead) {
 #pragma unroll
             for (int c = 0; c < SEG; ++c) dmask |= (dead[c0 + cl + c] != 0 ? 1u : 0u) << c;
         }
+    }
+    pdl_wait();  // D was last updated by the previous kernel
+    if (seg_on && row_on) {
+        float t[SEG];
+        load32<float>(D + row * cols + c0 + cl, t);
 #pragma unroll
         for (int c = 0; c < SEG; ++c) {
             w0[c] = ((dmask >> c) & 1u) ? 0.f : w0[c];
@@ -206,11 +232,14 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                 sm.scales[(s * SEG) / group][r] = sc;
             }
         }
+        // Threads on the chunk barriers of segment s: its warp and the later live segments' warps.
+        const int nbar = 32 * (nseg - s);
         if (seg == s) {
             // The segment's 32 columns, one after the other; every lane (row) quantizes
             // its own weight, and the error updates the rest of the segment in registers.
+            __syncwarp();  // every lane has read the group's min / max before sm.E overwrites them
             const float sc = sm.gs[r], inv_s = sm.ginv[r], z = sm.gz[r];
-            float wq[SEG], ebuf[SEG];
+            float wq[SEG];
             uint32_t cw[SEG / 4];
 #pragma unroll
             for (int k = 0; k < SEG / 4; ++k) cw[k] = 0u;
@@ -223,7 +252,11 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                 wq[ci] = dq;
                 cw[ci / 4] |= ((uint32_t)q) << (8 * (ci % 4));
                 const float e = (wv - dq) * sm.fdiag[j];
-                ebuf[ci] = e;
+                sm.E[r][ci] = e;
+                if (ci % CH == CH - 1 && nbar > 32) {
+                    __threadfence_block();
+                    named_arrive(1 + ci / CH, nbar);  // chunk ci / CH of the errors is in sm.E
+                }
                 e2 = fmaf(e, e, e2);
                 // Uinv_b is upper triangular: only the later columns of the segment move here.
 #pragma unroll
@@ -235,8 +268,6 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                     if (c4 + 3 > ci) w[c4 + 3] = fmaf(-e, u.w, w[c4 + 3]);
                 }
             }
-#pragma unroll
-            for (int ci = 0; ci < SEG; ++ci) sm.E[s][r][ci] = ebuf[ci];
             *reinterpret_cast<uint4 *>(&sm.codes[r][cl]) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
             *reinterpret_cast<uint4 *>(&sm.codes[r][cl + 16]) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
             if (row_on) {
@@ -259,21 +290,24 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                             make_float4(wq[c], wq[c + 1], wq[c + 2], wq[c + 3]);
                 }
             }
-        }
-        __syncthreads();
-        if (seg > s && seg_on) {
-            // Rank-32 update of this warp's segment by segment s: w -= E_s U[seg s, this segment].
-#pragma unroll 4
-            for (int i = 0; i < SEG; ++i) {
-                const float ei = sm.E[s][r][i];
-                const float *ur = &sm.U[s * SEG + i][cl];
+        } else if (seg > s && seg_on) {
+            // Update of this warp's segment by segment s, w -= E_s U[seg s, this segment],
+            // one chunk of 8 columns as soon as it is published (the sums run in column order).
+            for (int ch = 0; ch < NCH; ++ch) {
+                named_sync(1 + ch, nbar);
 #pragma unroll
-                for (int c4 = 0; c4 < SEG; c4 += 4) {
-                    const float4 u = *reinterpret_cast<const float4 *>(ur + c4);
-                    w[c4 + 0] = fmaf(-ei, u.x, w[c4 + 0]);
-                    w[c4 + 1] = fmaf(-ei, u.y, w[c4 + 1]);
-                    w[c4 + 2] = fmaf(-ei, u.z, w[c4 + 2]);
-                    w[c4 + 3] = fmaf(-ei, u.w, w[c4 + 3]);
+                for (int ii = 0; ii < CH; ++ii) {
+                    const int i = ch * CH + ii;
+                    const float ei = sm.E[r][i];
+                    const float *ur = &sm.U[s * SEG + i][cl];
+#pragma unroll
+                    for (int c4 = 0; c4 < SEG; c4 += 4) {
+                        const float4 u = *reinterpret_cast<const float4 *>(ur + c4);
+                        w[c4 + 0] = fmaf(-ei, u.x, w[c4 + 0]);
+                        w[c4 + 1] = fmaf(-ei, u.y, w[c4 + 1]);
+                        w[c4 + 2] = fmaf(-ei, u.z, w[c4 + 2]);
+                        w[c4 + 3] = fmaf(-ei, u.w, w[c4 + 3]);
+                    }
                 }
             }
         }
@@ -356,14 +390,12 @@ __global__ void __launch_bounds__(256) premultiply_t_kernel(const float *__restr
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-            float a[8], bb[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                a[i] = As[k][ty * 4 + i];
-                a[4 + i] = As[k][64 + ty * 4 + i];
-                bb[i] = Bs[k][tx * 4 + i];
-                bb[4 + i] = Bs[k][64 + tx * 4 + i];
-            }
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[k][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[k][64 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[k][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[k][64 + tx * 4]);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -371,18 +403,34 @@ __global__ void __launch_bounds__(256) premultiply_t_kernel(const float *__restr
         }
         __syncthreads();
     }
+    // Each thread stores its four consecutive m of a row as one float4 when cols % 4 == 0 (a
+    // warp's stores cover 256 contiguous bytes of a row of VT); s0 is a multiple of the block
+    // width, itself a multiple of 32, so a group of four never straddles s0.
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int n = (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
         if (n >= bw) continue;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int64_t m = m0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+        for (int half = 0; half < 2; ++half) {
+            const int64_t m = m0 + half * 64 + tx * 4;
             if (m >= s0) continue;
-            const float v = acc[i][j];
-            const float h = tf32_hi(v);
-            VThi[(s0 + n) * cols + m] = h;
-            VTlo[(s0 + n) * cols + m] = v - h;
+            float h[4], l[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float v = acc[i][half * 4 + j];
+                h[j] = tf32_hi(v);
+                l[j] = v - h[j];
+            }
+            if ((cols & 3) == 0) {
+                *reinterpret_cast<float4 *>(VThi + (s0 + n) * cols + m) = make_float4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<float4 *>(VTlo + (s0 + n) * cols + m) = make_float4(l[0], l[1], l[2], l[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    VThi[(s0 + n) * cols + m + j] = h[j];
+                    VTlo[(s0 + n) * cols + m + j] = l[j];
+                }
+            }
         }
     }
 }
@@ -428,6 +476,9 @@ cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, in
     static bool attr_set = false;  // per template instance
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(sweep_kernel<BITS, TW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        // All of the unified L1 as shared memory, so that three blocks fit on an SM.
+        e = cudaFuncSetAttribute(sweep_kernel<BITS, TW>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
