@@ -224,13 +224,16 @@ gq_status gptq_weight_error(const void *W, gq_dtype wt, int64_t rows, int64_t co
  *   dW     rows x cols float32, read only.
  *   H      cols x cols float32 (both triangles), used as passed (no damping);
  *          must be positive definite, else GQ_ENOTPD with *info = a column.
- *   r      1 <= r <= min(64, rows, cols).
+ *   r      1 <= r <= min(256, rows, cols); above 64 also cols >= r + 64.
  *   A      r x cols float32 output.   B  rows x r float32 output.
  *   sigma  r float32 output, may be NULL: the r largest singular values of the
  *          projected error ΔW', in descending order.
  *   ws     >= eora_compensate_workspace_size(rows, cols, r) bytes.
- * Computed in float32 with a block subspace iteration of width min(2r, cols)
- * (30 iterations) and a Rayleigh-Ritz step.  When σ_r and σ_{r+1} are close,
+ * Computed in float32 with a block subspace iteration of width min(2r, 128,
+ * cols) (30 iterations) and a Rayleigh-Ritz step.  Above r = 64 the singular
+ * vectors come in chunks of 64: each chunk is found by a new iteration whose
+ * block is kept orthogonal to the chunks before it (locking), and the r
+ * values are sorted at the end.  When σ_r and σ_{r+1} are close,
  * the rank-r subspace is not unique and B A may differ from another exact
  * solution by directions of nearly equal σ; the compensated loss and σ do not.
  * Synchronizes `stream` once (after the factorization of H).

@@ -86,8 +86,15 @@ cudaError_t sweep_range(const SweepCtx &c, int64_t a, int64_t b) {
         const int64_t c0 = a * B;
         const int bw = (int)((c.cols - c0) < B ? (c.cols - c0) : B);
         return sweep_block_launch(c.W, c.bf16, c.rows, c.cols, c0, bw, c.Uinv + a * B * B, c.F, c.dead, c.bits, c.group,
-                                  c.D, c.DL, c.qweight, c.scales, c.qzeros, c.codes, c.W_hat, c.row_err, c.s);
+                                  c.D, c.DL, c.qweight, c.scales, c.qzeros, c.codes, c.W_hat, c.row_err, c.VThi,
+                                  c.VTlo, false, c.s);
     }
+    // Two full 128-column blocks, when one wave of CTAs covers the rows: one launch sweeps both
+    // and applies the first one's deferred update to the second itself (no GEMM between them).
+    if (b - a == 2 && B == 128 && (b * B) <= c.cols && sweep_pair_fits(c.rows))
+        return sweep_block_launch(c.W, c.bf16, c.rows, c.cols, a * B, (int)B, c.Uinv + a * B * B, c.F, c.dead, c.bits,
+                                  c.group, c.D, c.DL, c.qweight, c.scales, c.qzeros, c.codes, c.W_hat, c.row_err,
+                                  c.VThi, c.VTlo, true, c.s);
     const int64_t m = (a + b) / 2;
     cudaError_t e = sweep_range(c, a, m);
     if (e != cudaSuccess) return e;
@@ -495,7 +502,9 @@ size_t eora_compensate_workspace_size(int64_t rows, int64_t cols, int r) {
 gq_status eora_compensate(const float *dW, int64_t rows, int64_t cols, const float *H, int r, float *A, float *B,
                           float *sigma, void *ws, size_t ws_bytes, gq_stream_t stream, int64_t *info) {
     if (!dW || !H || !A || !B || rows <= 0 || cols <= 0) return GQ_EINVAL;
-    if (r <= 0 || r > 64 || r > rows || r > cols) return GQ_EINVAL;
+    // Above 64 the eigenpairs come in locked chunks of 64, each from 128 vectors orthogonal to
+    // the chunks before it, which needs cols >= r + 64.
+    if (r <= 0 || r > 256 || r > rows || r > cols || (r > 64 && cols < (int64_t)r + 64)) return GQ_EINVAL;
     if (!ws || !aligned(ws, kAlign) || ws_bytes < eora_workspace_bytes(rows, cols, r)) return GQ_EWORKSPACE;
     unsigned long long bad = ULLONG_MAX;
     unsigned int finite = ~0u;

@@ -199,12 +199,18 @@ cudaError_t block_inverses(const float *F, int64_t cols, int block, float *Uinv,
 // b, written as its TF32 split (VThi, VTlo; cols x cols each, row-major).
 cudaError_t premultiply_t(const float *F, int64_t cols, int block, const float *Uinv, float *VThi, float *VTlo,
                           cudaStream_t s);
-// One block of the sweep.  On exit the block's columns of D hold the TF32 hi
-// part of ΔW and those of DL the lo part.
+// One block of the sweep, or with `pair` the two full 128-column blocks from
+// c0 (Uinv_blk then points at the first of their two inverses) with the
+// deferred update of the second by the first applied in the kernel, from V in
+// VThi + VTlo.  On exit the blocks' columns of D hold the TF32 hi part of ΔW
+// and those of DL the lo part.  `pair` needs sweep_pair_fits(rows): one CTA
+// of 32 rows per SM.
 cudaError_t sweep_block_launch(const void *W, bool w_bf16, int64_t rows, int64_t cols, int64_t c0,
                                int bw, const float *Uinv_blk, const float *F, const uint8_t *dead, int bits, int group,
                                float *D, float *DL, int32_t *qweight, float *scales, int32_t *qzeros,
-                               uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s);
+                               uint8_t *codes, float *W_hat, float *row_err, const float *VThi, const float *VTlo,
+                               bool pair, cudaStream_t s);
+bool sweep_pair_fits(int64_t rows);
 
 // Leading eigenpairs of a symmetric positive semi-definite G (subspace.cu).
 constexpr int kSubspaceMaxK = 128;
@@ -218,9 +224,16 @@ struct SubspaceBufs {
     float *part;                  // subspace_part_floats(k, cols, tc)
     float *Linv;                  // cholesky_scratch_floats(128)
     DeviceStatus *qst;            // status of the Cholesky-QR factorizations
+    // Locked vectors (nl x cols, orthonormal rows) that every block is kept orthogonal
+    // to, so that the iteration finds the next eigenpairs; nl = 0: none.
+    const float *VL = nullptr;
+    int nl = 0;
+    float *Cp = nullptr;          // k x nl scratch of the projection
 };
 // k = min(2 r, 128, cols) vectors for r wanted eigenpairs.
 int subspace_width(int64_t cols, int r);
+// Floats of `part` that the projection against nl locked vectors needs (k-row blocks).
+size_t subspace_projection_part_floats(int k, int nl);
 size_t subspace_part_floats(int k, int64_t cols, bool tc);
 // On return the rows of ZT are orthonormal, lam holds the k Ritz values in
 // descending order and column i of Wt (k x k, row-major) the coefficients of

@@ -74,15 +74,38 @@ cudaError_t mirror_lower(float *A, int64_t n, int64_t lda, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// perm[rank] = i, rank = the position of lam[i] in descending order (ties by index).
+__global__ void rank_desc_kernel(const float *__restrict__ lam, int n, int *__restrict__ perm) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const float v = lam[i];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) rank += (lam[j] > v || (lam[j] == v && j < i)) ? 1 : 0;
+        perm[rank] = i;
+    }
+}
+
+// Row j of dst (cols floats) = row perm[j] of src; lam_dst[j] = lam_src[perm[j]].
+__global__ void gather_rows_kernel(const float *__restrict__ src, const int *__restrict__ perm, int64_t cols,
+                                   float *__restrict__ dst, const float *__restrict__ lam_src,
+                                   float *__restrict__ lam_dst) {
+    const int j = blockIdx.x;
+    const int i = perm[j];
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) dst[j * cols + c] = src[i * cols + c];
+    if (threadIdx.x == 0) lam_dst[j] = lam_src[i];
+}
+
 struct EoraWs {
     DeviceStatus *st;
     float *Linv, *F, *M, *G, *ZT, *ZT2, *Gm, *part, *lam, *Wt, *VrT;
+    float *lamr, *lams, *Cp;  // the r eigenvalues (chunk order, then sorted); projection scratch (k x r)
+    int *perm;                // r: the sort order
     // tensor-core path only (null otherwise)
     float *FThi, *FTlo, *dWhi, *dWlo, *Mhi, *Mlo, *Mthi, *Mtlo, *Ghi, *Glo, *Zhi, *Zlo;
     uint8_t *dead;
 };
 
 constexpr int ASPLIT = 8;   // K slices of A = B^T dW
+constexpr int CHUNK = 64;   // eigenpairs found per subspace iteration (k = 2 CHUNK vectors)
 
 // The tensor-core path needs TMA-compatible row strides for M^T (rows) and H (cols).
 bool eora_tc(int64_t rows, int64_t cols) { return rows % 4 == 0 && cols % 4 == 0; }
@@ -109,10 +132,15 @@ size_t eora_layout(int64_t rows, int64_t cols, int r, EoraWs *w, char *base) {
     t.Gm = (float *)take((size_t)k * k * sizeof(float));
     size_t part = subspace_part_floats(k, cols, tc);
     if ((size_t)ASPLIT * r * cols > part) part = (size_t)ASPLIT * r * cols;
+    if (subspace_projection_part_floats(k, r) > part) part = subspace_projection_part_floats(k, r);
     t.part = (float *)take(part * sizeof(float));
     t.lam = (float *)take((size_t)k * sizeof(float));
     t.Wt = (float *)take((size_t)k * k * sizeof(float));
     t.VrT = (float *)take((size_t)r * cols * sizeof(float));
+    t.lamr = (float *)take((size_t)r * sizeof(float));
+    t.lams = (float *)take((size_t)r * sizeof(float));
+    t.Cp = (float *)take((size_t)k * r * sizeof(float));
+    t.perm = (int *)take((size_t)r * sizeof(int));
     if (tc) {
         t.FThi = (float *)take(cc);
         t.FTlo = (float *)take(cc);
@@ -124,8 +152,10 @@ size_t eora_layout(int64_t rows, int64_t cols, int r, EoraWs *w, char *base) {
         t.Mtlo = (float *)take(rc);
         t.Ghi = (float *)take(cc);
         t.Glo = (float *)take(cc);
-        t.Zhi = (float *)take((size_t)k * cols * sizeof(float));
-        t.Zlo = (float *)take((size_t)k * cols * sizeof(float));
+        // The split of the k-row blocks, and at the end of V_r^T (r rows, r may exceed k).
+        const size_t zr = (size_t)(k > r ? k : r);
+        t.Zhi = (float *)take(zr * cols * sizeof(float));
+        t.Zlo = (float *)take(zr * cols * sizeof(float));
     }
     if (w) *w = t;
     return off;
@@ -196,14 +226,38 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     }
 
     // Leading eigenpairs of G (block subspace iteration + Rayleigh-Ritz).
+    // Up to CHUNK of them per subspace iteration of k vectors; beyond that the
+    // ones found are locked and the next iteration runs orthogonal to them.
     SubspaceBufs sb;
     sb.G = w.G; sb.Ghi = w.Ghi; sb.Glo = w.Glo;
     sb.ZT = w.ZT; sb.ZT2 = w.ZT2; sb.Zhi = w.Zhi; sb.Zlo = w.Zlo;
     sb.Gm = w.Gm; sb.Wt = w.Wt; sb.lam = w.lam; sb.part = w.part; sb.Linv = w.Linv; sb.qst = qst;
-    if ((e = subspace_ritz(sb, k, cols, tc, s)) != cudaSuccess) return e;
-    // V_r^T = W[:, :r]^T Z^T  (r x cols)
-    if ((e = sgemm<float>(r, cols, k, 1.f, w.Wt, k, true, w.ZT, cols, false, 0.f, w.VrT, cols, 0, s)) != cudaSuccess)
-        return e;
+    sb.VL = w.VrT; sb.Cp = w.Cp;
+    for (int nl = 0; nl < r;) {
+        const int take = (r - nl) < CHUNK ? (r - nl) : CHUNK;
+        sb.nl = nl;
+        if ((e = subspace_ritz(sb, k, cols, tc, s)) != cudaSuccess) return e;
+        // Rows nl .. nl + take of V_r^T = W[:, :take]^T Z^T (take x cols), and their eigenvalues.
+        if ((e = sgemm<float>(take, cols, k, 1.f, w.Wt, k, true, w.ZT, cols, false, 0.f, w.VrT + (int64_t)nl * cols,
+                              cols, 0, s)) != cudaSuccess)
+            return e;
+        if ((e = cudaMemcpyAsync(w.lamr + nl, w.lam, (size_t)take * sizeof(float), cudaMemcpyDeviceToDevice, s)) !=
+            cudaSuccess)
+            return e;
+        nl += take;
+    }
+    const float *lam_r = w.lamr;
+    if (r > CHUNK) {
+        // Chunks meet where eigenvalues are nearly equal: one descending order for all r.
+        rank_desc_kernel<<<1, 256, 0, s>>>(w.lamr, r, w.perm);
+        count_launch();
+        gather_rows_kernel<<<r, 256, 0, s>>>(w.VrT, w.perm, cols, w.part, w.lamr, w.lams);
+        count_launch();
+        if ((e = cudaMemcpyAsync(w.VrT, w.part, (size_t)r * cols * sizeof(float), cudaMemcpyDeviceToDevice, s)) !=
+            cudaSuccess)
+            return e;
+        lam_r = w.lams;
+    }
     // B = M V_r (rows x r), signs normalised.
     if (tc) {
         if ((e = split_tf32(w.VrT, r, cols, cols, w.Zhi, w.Zlo, cols, s)) != cudaSuccess) return e;
@@ -215,7 +269,7 @@ cudaError_t eora_run(const float *dW, int64_t rows, int64_t cols, const float *H
     if ((e = sign_normalize(B, r, rows, r, 1, s)) != cudaSuccess) return e;
     // A = Σ^-2 B^T dW  (r x cols)
     if ((e = sgemm_splitk(r, cols, rows, B, r, true, dW, cols, false, A, w.part, ASPLIT, s)) != cudaSuccess) return e;
-    finish_kernel<<<r, 256, 0, s>>>(w.lam, r, sigma, A, cols);
+    finish_kernel<<<r, 256, 0, s>>>(lam_r, r, sigma, A, cols);
     count_launch();
     return cudaGetLastError();
 }

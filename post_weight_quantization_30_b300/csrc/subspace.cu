@@ -10,6 +10,10 @@
 //   T = ZT G ZT^T (k x k), T = W diag(lam) W^T by cyclic Jacobi
 //
 // The Ritz vectors are the rows of W^T ZT; callers take the first r of them.
+// With locked vectors VL (nl x cols, orthonormal) every block is projected
+// onto their orthogonal complement after each product with G, so the
+// iteration converges to the leading eigenpairs of (I - VL^T VL) G (I - VL^T VL):
+// the next ones of G once VL spans leading eigenvectors.
 // On the tensor-core path the products with G run on the tensor cores from the
 // split of G the caller provides: one TF32 product per iteration, 3xTF32
 // (float32 accuracy) for the last three iterations and the Rayleigh-Ritz step.
@@ -293,6 +297,15 @@ cudaError_t cholqr_pass(const SubspaceBufs &w, float *src, float *dst, int k, in
     return sgemm<float>(k, cols, k, 1.f, w.Linv, 128, false, src, cols, false, 0.f, dst, cols, 0, s);
 }
 
+// Z <- Z - (Z VL^T) VL: the k rows of Z (k x cols) made orthogonal to the nl
+// locked rows of VL.  Nothing to do when nl = 0.
+cudaError_t project_out(const SubspaceBufs &w, float *Z, int k, int64_t cols, cudaStream_t s) {
+    if (w.nl <= 0) return cudaSuccess;
+    cudaError_t e = sgemm_splitk(k, w.nl, cols, Z, cols, false, w.VL, cols, true, w.Cp, w.part, SPLITK, s);
+    if (e != cudaSuccess) return e;
+    return sgemm<float>(k, cols, w.nl, -1.f, w.Cp, w.nl, false, w.VL, cols, false, 1.f, Z, cols, 0, s);
+}
+
 // Y = the block ZT (k x cols) times the symmetric G.  On the tensor cores
 // either with float32 accuracy (3xTF32) or, when !accurate, as one TF32
 // product that reads only the hi half of G's split (half the bytes; for
@@ -315,6 +328,8 @@ int subspace_width(int64_t cols, int r) {
     return (int)k;
 }
 
+size_t subspace_projection_part_floats(int k, int nl) { return (size_t)SPLITK * k * nl; }
+
 size_t subspace_part_floats(int k, int64_t cols, bool tc) {
     size_t part = (size_t)SPLITK * k * k;
     if (tc && (size_t)zsplit(cols, k) * k * cols > part) part = (size_t)zsplit(cols, k) * k * cols;
@@ -325,6 +340,7 @@ cudaError_t subspace_ritz(const SubspaceBufs &w, int k, int64_t cols, bool tc, c
     cudaError_t e;
     init_block_kernel<<<grid1d((int64_t)k * cols), 256, 0, s>>>(w.ZT2, k, cols);
     count_launch();
+    if ((e = project_out(w, w.ZT2, k, cols, s)) != cudaSuccess) return e;
     if ((e = cholqr_pass(w, w.ZT2, w.ZT, k, cols, s)) != cudaSuccess) return e;
     if ((e = cholqr_pass(w, w.ZT, w.ZT2, k, cols, s)) != cudaSuccess) return e;
     if ((e = cudaMemcpyAsync(w.ZT, w.ZT2, (size_t)k * cols * sizeof(float), cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
@@ -335,6 +351,7 @@ cudaError_t subspace_ritz(const SubspaceBufs &w, int k, int64_t cols, bool tc, c
         // subspace (each shrinks it by lambda_{k+1} / lambda_i per direction).
         const bool accurate = it >= ITERS - ACCURATE_TAIL;
         if ((e = block_times_g(w, w.ZT, w.ZT2, k, cols, tc, accurate, s)) != cudaSuccess) return e;
+        if ((e = project_out(w, w.ZT2, k, cols, s)) != cudaSuccess) return e;
         if ((e = cholqr_pass(w, w.ZT2, w.ZT, k, cols, s)) != cudaSuccess) return e;
     }
     if ((e = cholqr_pass(w, w.ZT, w.ZT2, k, cols, s)) != cudaSuccess) return e;

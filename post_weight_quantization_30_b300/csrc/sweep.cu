@@ -127,19 +127,20 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-template <int BITS, typename TW>
-__global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ W, int64_t rows, int64_t cols,
-                                                         int64_t c0, int bw, const float *__restrict__ Uinv,
-                                                         const float *__restrict__ F, const uint8_t *__restrict__ dead,
-                                                         int group, float *__restrict__ D, float *__restrict__ DL,
-                                                         int32_t *__restrict__ qweight, float *__restrict__ scales,
-                                                         int32_t *__restrict__ qzeros, uint8_t *__restrict__ codes,
-                                                         float *__restrict__ W_hat, float *__restrict__ row_err) {
-    pdl_trigger();
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    SweepSmem &sm = *reinterpret_cast<SweepSmem *>(smem_raw);
+// The sweep of one block (columns c0 .. c0 + bw) for this CTA's 32 rows, from
+// the block's Uinv_b (U) and F_jj (fdiag) in shared memory and w, the row
+// segment as updated by every earlier column (w0: the original weights).
+// Writes ΔW (split) to D / DL, Ŵ, the row errors and the packed outputs; with
+// KEEP_DW, dwr receives this warp's segment of ΔW (rows inside the layer).
+template <int BITS, bool KEEP_DW>
+__device__ __forceinline__ void sweep_block(SweepSmem &sm, const float (*U)[MAXB], const float *fdiag, float (&w)[SEG],
+                                            const float (&w0)[SEG], float (&dwr)[SEG], int64_t rows, int64_t cols,
+                                            int64_t c0, int bw, int group, float *__restrict__ D,
+                                            float *__restrict__ DL, int32_t *__restrict__ qweight,
+                                            float *__restrict__ scales, int32_t *__restrict__ qzeros,
+                                            uint8_t *__restrict__ codes, float *__restrict__ W_hat,
+                                            float *__restrict__ row_err) {
     constexpr float maxq = (float)((1 << BITS) - 1);
-
     const int seg = threadIdx.x >> 5, r = threadIdx.x & 31;  // warp = segment, lane = row
     const int64_t row0 = (int64_t)blockIdx.x * ROWS;
     const int64_t row = row0 + r;
@@ -148,55 +149,7 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
     const int cl = seg * SEG;  // first block column of this warp
     const bool seg_on = seg < nseg;
     const int gseg = group / SEG;  // segments per group
-
-    // Uinv_b, F's diagonal, W and the dead mask were complete before the first
-    // kernel of the sweep started, so they are read before waiting for the
-    // previous kernel; D, which that kernel updates, is read after.
-    // Uinv_b into shared memory with asynchronous 16-byte copies, all in flight
-    // at once (the block's rows and columns beyond bw are zero-filled).
-    for (int idx = threadIdx.x; idx < MAXB * MAXB / 4; idx += NTHREADS) {
-        const int i = idx / (MAXB / 4), j4 = (idx % (MAXB / 4)) * 4;
-        float *dst = &sm.U[i][j4];
-        if (i < bw && j4 < bw) {
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
-                         "l"(Uinv + (int64_t)i * bw + j4)
-                         : "memory");
-        } else {
-            *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    for (int i = threadIdx.x; i < MAXB; i += NTHREADS) sm.fdiag[i] = (i < bw) ? F[(c0 + i) * cols + c0 + i] : 1.f;
-
-    // This warp's segment of the row: the original weights w0 (dead inputs
-    // zero) and the weights as updated by every earlier block, w = w0 + D.
-    float w[SEG], w0[SEG];
-    uint32_t dmask = 0;
-#pragma unroll
-    for (int c = 0; c < SEG; ++c) {
-        w[c] = 0.f;
-        w0[c] = 0.f;
-    }
-    if (seg_on && row_on) {
-        load32<TW>(W + row * cols + c0 + cl, w0);
-        if (dead) {
-#pragma unroll
-            for (int c = 0; c < SEG; ++c) dmask |= (dead[c0 + cl + c] != 0 ? 1u : 0u) << c;
-        }
-    }
-    pdl_wait();  // D was last updated by the previous kernel
-    if (seg_on && row_on) {
-        float t[SEG];
-        load32<float>(D + row * cols + c0 + cl, t);
-#pragma unroll
-        for (int c = 0; c < SEG; ++c) {
-            w0[c] = ((dmask >> c) & 1u) ? 0.f : w0[c];
-            w[c] = w0[c] + t[c];
-        }
-    }
     float e2 = 0.f;
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
 
     for (int s = 0; s < nseg; ++s) {
         if (s % gseg == 0) {
@@ -251,7 +204,7 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                 const float dq = sc * (q - z);
                 wq[ci] = dq;
                 cw[ci / 4] |= ((uint32_t)q) << (8 * (ci % 4));
-                const float e = (wv - dq) * sm.fdiag[j];
+                const float e = (wv - dq) * fdiag[j];
                 sm.E[r][ci] = e;
                 if (ci % CH == CH - 1 && nbar > 32) {
                     __threadfence_block();
@@ -261,7 +214,7 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                 // Uinv_b is upper triangular: only the later columns of the segment move here.
 #pragma unroll
                 for (int c4 = ((ci + 1) / 4) * 4; c4 < SEG; c4 += 4) {
-                    const float4 u = *reinterpret_cast<const float4 *>(&sm.U[j][cl + c4]);
+                    const float4 u = *reinterpret_cast<const float4 *>(&U[j][cl + c4]);
                     if (c4 + 0 > ci) w[c4 + 0] = fmaf(-e, u.x, w[c4 + 0]);
                     if (c4 + 1 > ci) w[c4 + 1] = fmaf(-e, u.y, w[c4 + 1]);
                     if (c4 + 2 > ci) w[c4 + 2] = fmaf(-e, u.z, w[c4 + 2]);
@@ -281,6 +234,7 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                     for (int u = 0; u < 4; ++u) {
                         dw[u] = w0[c + u] - wq[c + u];
                         dh[u] = tf32_hi(dw[u]);
+                        if (KEEP_DW) dwr[c + u] = dw[u];
                     }
                     *reinterpret_cast<float4 *>(dp + c) = make_float4(dh[0], dh[1], dh[2], dh[3]);
                     *reinterpret_cast<float4 *>(lp + c) =
@@ -299,7 +253,7 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
                 for (int ii = 0; ii < CH; ++ii) {
                     const int i = ch * CH + ii;
                     const float ei = sm.E[r][i];
-                    const float *ur = &sm.U[s * SEG + i][cl];
+                    const float *ur = &U[s * SEG + i][cl];
 #pragma unroll
                     for (int c4 = 0; c4 < SEG; c4 += 4) {
                         const float4 u = *reinterpret_cast<const float4 *>(ur + c4);
@@ -353,6 +307,162 @@ __global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ 
     for (int idx = threadIdx.x; idx < ng * BITS; idx += NTHREADS) {
         const int g = idx / BITS, wi = idx % BITS;
         qzeros[((c0 / group) + g) * zw + row0 * BITS / 32 + wi] = (int32_t)pack_word<BITS>(sm.zeros[g], wi, ROWS);
+    }
+}
+
+// Shared memory of the two-block kernel beyond SweepSmem: the second block's
+// Uinv_b and F_jj, and V[blk a, blk a + 1] (row k, column n) for the
+// first-level deferred update between the two.
+struct PairSmem {
+    float U1[MAXB][MAXB];
+    float Vs[MAXB][MAXB];
+    float fdiag1[MAXB];
+};
+
+// One launch sweeps one block (PAIR = false) or two adjacent full blocks a,
+// a + 1 (PAIR = true).  With PAIR the deferred update of block a + 1 by block
+// a, ΔW_a V[blk a, blk a + 1], is formed in registers (float32 FMA; lane =
+// row, warp = its segment's 32 columns of block a + 1) from ΔW_a staged in
+// shared memory, and added to block a + 1's weights as they are loaded:
+// the first level of the recursive deferred update needs no GEMM launch.
+template <int BITS, typename TW, bool PAIR>
+__global__ void __launch_bounds__(NTHREADS) sweep_kernel(const TW *__restrict__ W, int64_t rows, int64_t cols,
+                                                         int64_t c0, int bw, const float *__restrict__ Uinv,
+                                                         const float *__restrict__ F, const uint8_t *__restrict__ dead,
+                                                         int group, float *__restrict__ D, float *__restrict__ DL,
+                                                         int32_t *__restrict__ qweight, float *__restrict__ scales,
+                                                         int32_t *__restrict__ qzeros, uint8_t *__restrict__ codes,
+                                                         float *__restrict__ W_hat, float *__restrict__ row_err,
+                                                         const float *__restrict__ VThi,
+                                                         const float *__restrict__ VTlo) {
+    pdl_trigger();
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SweepSmem &sm = *reinterpret_cast<SweepSmem *>(smem_raw);
+    PairSmem &ps = *reinterpret_cast<PairSmem *>(smem_raw + sizeof(SweepSmem));  // PAIR only
+
+    const int seg = threadIdx.x >> 5, r = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * ROWS + r;
+    const bool row_on = row < rows;
+    const int cl = seg * SEG;
+    const bool seg_on = seg < bw / SEG;
+
+    // Uinv_b, F's diagonal, W, the dead mask and V were complete before the
+    // first kernel of the sweep started, so they are read before waiting for
+    // the previous kernel; D, which that kernel updates, is read after.
+    // Uinv_b into shared memory with asynchronous 16-byte copies, all in flight
+    // at once (the block's rows and columns beyond bw are zero-filled).
+    auto load_uinv = [&](float (*Ud)[MAXB], const float *Us, int bwu) {
+        for (int idx = threadIdx.x; idx < MAXB * MAXB / 4; idx += NTHREADS) {
+            const int i = idx / (MAXB / 4), j4 = (idx % (MAXB / 4)) * 4;
+            float *dst = &Ud[i][j4];
+            if (i < bwu && j4 < bwu) {
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                             "l"(Us + (int64_t)i * bwu + j4)
+                             : "memory");
+            } else {
+                *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
+    load_uinv(sm.U, Uinv, bw);
+    if (PAIR) load_uinv(ps.U1, Uinv + (int64_t)MAXB * MAXB, MAXB);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    for (int i = threadIdx.x; i < MAXB; i += NTHREADS) sm.fdiag[i] = (i < bw) ? F[(c0 + i) * cols + c0 + i] : 1.f;
+    if (PAIR) {
+        const int64_t c1 = c0 + MAXB;
+        for (int i = threadIdx.x; i < MAXB; i += NTHREADS) ps.fdiag1[i] = F[(c1 + i) * cols + c1 + i];
+        // Vs[k][n] = V[c0 + k][c1 + n] = VThi + VTlo at [c1 + n][c0 + k]: thread n reads row n of
+        // the transposed split, four k at a time, and writes column n of Vs.
+        const int n = threadIdx.x;  // NTHREADS == MAXB
+        const float *hi = VThi + (c1 + n) * cols + c0, *lo = VTlo + (c1 + n) * cols + c0;
+        for (int k = 0; k < MAXB; k += 4) {
+            const float4 h = *reinterpret_cast<const float4 *>(hi + k), l = *reinterpret_cast<const float4 *>(lo + k);
+            ps.Vs[k + 0][n] = h.x + l.x;
+            ps.Vs[k + 1][n] = h.y + l.y;
+            ps.Vs[k + 2][n] = h.z + l.z;
+            ps.Vs[k + 3][n] = h.w + l.w;
+        }
+    }
+
+    // This warp's segment of the row: the original weights w0 (dead inputs
+    // zero) and the weights as updated by every earlier block, w = w0 + D.
+    float w[SEG], w0[SEG], dwr[SEG];
+    uint32_t dmask = 0;
+#pragma unroll
+    for (int c = 0; c < SEG; ++c) {
+        w[c] = 0.f;
+        w0[c] = 0.f;
+        dwr[c] = 0.f;
+    }
+    if (seg_on && row_on) {
+        load32<TW>(W + row * cols + c0 + cl, w0);
+        if (dead) {
+#pragma unroll
+            for (int c = 0; c < SEG; ++c) dmask |= (dead[c0 + cl + c] != 0 ? 1u : 0u) << c;
+        }
+    }
+    pdl_wait();  // D was last updated by the previous kernel
+    if (seg_on && row_on) {
+        float t[SEG];
+        load32<float>(D + row * cols + c0 + cl, t);
+#pragma unroll
+        for (int c = 0; c < SEG; ++c) {
+            w0[c] = ((dmask >> c) & 1u) ? 0.f : w0[c];
+            w[c] = w0[c] + t[c];
+        }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+
+    sweep_block<BITS, PAIR>(sm, sm.U, sm.fdiag, w, w0, dwr, rows, cols, c0, bw, group, D, DL, qweight, scales,
+                            qzeros, codes, W_hat, row_err);
+    if (PAIR) {
+        const int64_t c1 = c0 + MAXB;
+        // Every warp is done with block a's Uinv_b and staging; ΔW_a goes into the space of the former.
+        __syncthreads();
+        float (*dWs)[MAXB + 1] = reinterpret_cast<float (*)[MAXB + 1]>(&sm.U[0][0]);
+#pragma unroll
+        for (int c = 0; c < SEG; ++c) dWs[r][cl + c] = dwr[c];
+        __syncthreads();
+        // add = ΔW_a V[blk a, this warp's columns of blk a + 1] for this lane's row.
+        float add[SEG];
+#pragma unroll
+        for (int c = 0; c < SEG; ++c) add[c] = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < MAXB; ++k) {
+            const float e = dWs[r][k];
+#pragma unroll
+            for (int c4 = 0; c4 < SEG; c4 += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(&ps.Vs[k][cl + c4]);
+                add[c4 + 0] = fmaf(e, v.x, add[c4 + 0]);
+                add[c4 + 1] = fmaf(e, v.y, add[c4 + 1]);
+                add[c4 + 2] = fmaf(e, v.z, add[c4 + 2]);
+                add[c4 + 3] = fmaf(e, v.w, add[c4 + 3]);
+            }
+        }
+        // Block a + 1: w = w0 + (D + ΔW_a V), D holding the updates from before block a.
+        dmask = 0;
+#pragma unroll
+        for (int c = 0; c < SEG; ++c) {
+            w[c] = 0.f;
+            w0[c] = 0.f;
+        }
+        if (row_on) {
+            float t[SEG];
+            load32<TW>(W + row * cols + c1 + cl, w0);
+            load32<float>(D + row * cols + c1 + cl, t);
+            if (dead) {
+#pragma unroll
+                for (int c = 0; c < SEG; ++c) dmask |= (dead[c1 + cl + c] != 0 ? 1u : 0u) << c;
+            }
+#pragma unroll
+            for (int c = 0; c < SEG; ++c) {
+                w0[c] = ((dmask >> c) & 1u) ? 0.f : w0[c];
+                w[c] = w0[c] + (t[c] + add[c]);
+            }
+        }
+        sweep_block<BITS, false>(sm, ps.U1, ps.fdiag1, w, w0, dwr, rows, cols, c1, MAXB, group, D, DL, qweight,
+                                 scales, qzeros, codes, W_hat, row_err);
     }
 }
 
@@ -467,27 +577,29 @@ __global__ void __launch_bounds__(128) block_inverse_kernel(const float *__restr
     }
 }
 
-template <int BITS, typename TW>
+template <int BITS, typename TW, bool PAIR>
 cudaError_t launch_sweep(const TW *W, int64_t rows, int64_t cols, int64_t c0, int bw, const float *Uinv,
                          const float *F, const uint8_t *dead, int group, float *D, float *DL, int32_t *qweight,
-                         float *scales,
-                         int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err, cudaStream_t s) {
-    const size_t smem = sizeof(SweepSmem);
+                         float *scales, int32_t *qzeros, uint8_t *codes, float *W_hat, float *row_err,
+                         const float *VThi, const float *VTlo, cudaStream_t s) {
+    const size_t smem = sizeof(SweepSmem) + (PAIR ? sizeof(PairSmem) : 0);
     static bool attr_set = false;  // per template instance
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(sweep_kernel<BITS, TW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(sweep_kernel<BITS, TW, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
         if (e != cudaSuccess) return e;
-        // All of the unified L1 as shared memory, so that three blocks fit on an SM.
-        e = cudaFuncSetAttribute(sweep_kernel<BITS, TW>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        // All of the unified L1 as shared memory, so that three one-block CTAs fit on an SM.
+        e = cudaFuncSetAttribute(sweep_kernel<BITS, TW, PAIR>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int th = timing_begin(TK_SWEEP, s);
-    const cudaError_t e = launch_pdl(sweep_kernel<BITS, TW>, dim3((unsigned)((rows + ROWS - 1) / ROWS)), dim3(NTHREADS),
-                                     smem, s, W, rows, cols, c0, bw, Uinv, F, dead, group, D, DL, qweight, scales,
-                                     qzeros, codes, W_hat, row_err);
+    const cudaError_t e = launch_pdl(sweep_kernel<BITS, TW, PAIR>, dim3((unsigned)((rows + ROWS - 1) / ROWS)),
+                                     dim3(NTHREADS), smem, s, W, rows, cols, c0, bw, Uinv, F, dead, group, D, DL,
+                                     qweight, scales, qzeros, codes, W_hat, row_err, VThi, VTlo);
     count_launch();
-    timing_end(th, s, (double)rows * bw * (bw - 1));
+    // Column-step work of the block(s), and for two blocks the 2 rows x 128 x 128 flops between them.
+    timing_end(th, s, PAIR ? 2.0 * rows * MAXB * (MAXB - 1) + 2.0 * rows * MAXB * MAXB : (double)rows * bw * (bw - 1));
     return e;
 }
 
@@ -520,20 +632,28 @@ cudaError_t premultiply_t(const float *F, int64_t cols, int block, const float *
 cudaError_t sweep_block_launch(const void *W, bool w_bf16, int64_t rows, int64_t cols, int64_t c0, int bw,
                                const float *Uinv_blk, const float *F, const uint8_t *dead, int bits, int group,
                                float *D, float *DL, int32_t *qweight, float *scales, int32_t *qzeros, uint8_t *codes,
-                               float *W_hat, float *row_err, cudaStream_t s) {
-#define GQ_SWEEP_CASE(B)                                                                                         \
-    if (bits == B) {                                                                                             \
-        if (w_bf16)                                                                                              \
-            return launch_sweep<B, __nv_bfloat16>((const __nv_bfloat16 *)W, rows, cols, c0, bw, Uinv_blk, F, dead, \
-                                                  group, D, DL, qweight, scales, qzeros, codes, W_hat, row_err, s); \
-        return launch_sweep<B, float>((const float *)W, rows, cols, c0, bw, Uinv_blk, F, dead, group, D, DL,       \
-                                      qweight, scales, qzeros, codes, W_hat, row_err, s);                        \
+                               float *W_hat, float *row_err, const float *VThi, const float *VTlo, bool pair,
+                               cudaStream_t s) {
+#define GQ_SWEEP_CALL(B, T, P)                                                                                      \
+    return launch_sweep<B, T, P>((const T *)W, rows, cols, c0, bw, Uinv_blk, F, dead, group, D, DL, qweight, scales, \
+                                 qzeros, codes, W_hat, row_err, VThi, VTlo, s)
+#define GQ_SWEEP_CASE(B)                                      \
+    if (bits == B) {                                          \
+        if (w_bf16) {                                         \
+            if (pair) GQ_SWEEP_CALL(B, __nv_bfloat16, true);  \
+            GQ_SWEEP_CALL(B, __nv_bfloat16, false);           \
+        }                                                     \
+        if (pair) GQ_SWEEP_CALL(B, float, true);              \
+        GQ_SWEEP_CALL(B, float, false);                       \
     }
     GQ_SWEEP_CASE(2)
     GQ_SWEEP_CASE(3)
     GQ_SWEEP_CASE(4)
 #undef GQ_SWEEP_CASE
+#undef GQ_SWEEP_CALL
     return cudaErrorInvalidValue;
 }
+
+bool sweep_pair_fits(int64_t rows) { return (rows + ROWS - 1) / ROWS <= 148; }
 
 }  // namespace gq

@@ -33,3 +33,18 @@ def reversed_upper_factor(Hd: np.ndarray) -> np.ndarray:
     J = np.arange(Hd.shape[0])[::-1]
     L = np.linalg.cholesky(Hd[np.ix_(J, J)])
     return L[np.ix_(J, J)]
+
+
+def check_sigma(sg, sig, r, rtol=1e-3, reach=16):
+    """The GPU's r singular values against the oracle's.  Where sigma_i stands apart from sigma_(i+1)
+    by more than rtol, within rtol of it.  Inside a cluster of nearly equal values an individual value
+    is not determined to rtol by a subspace of finite accuracy, only the cluster is: there sigma_i of
+    the GPU lies between sigma_(i+reach) and sigma_i, each widened by rtol.  The compensated loss is
+    the criterion on the subspace as a whole."""
+    sg = np.asarray(sg, dtype=np.float64)
+    for i in range(r):
+        if sig[i] > sig[i + 1] * (1 + rtol):
+            assert abs(sg[i] - sig[i]) <= rtol * sig[i], (i, sg[i], sig[i])
+        else:
+            lo = sig[min(i + reach, len(sig) - 1)] * (1 - rtol)
+            assert lo <= sg[i] <= sig[i] * (1 + rtol), (i, sg[i], sig[i], lo)

@@ -80,11 +80,14 @@ def test_eora_host_side_validation(gq):
     p = ctypes.c_void_p
     f = gq.lib.eora_compensate
     assert f(p(256), 64, 64, p(256), 0, p(256), p(256), None, p(256), 1 << 30, None, None) == -1   # r = 0
-    assert f(p(256), 256, 256, p(256), 65, p(256), p(256), None, p(256), 1 << 30, None, None) == -1  # r > 64
+    assert f(p(256), 512, 512, p(256), 257, p(256), p(256), None, p(256), 1 << 30, None, None) == -1  # r > 256
+    assert f(p(256), 256, 256, p(256), 200, p(256), p(256), None, p(256), 1 << 30, None, None) == -1  # cols < r + 64
+    assert f(p(256), 256, 256, p(256), 65, p(256), p(256), None, p(256), 16, None, None) == -7  # r = 65 accepted
     assert f(p(256), 8, 64, p(256), 16, p(256), p(256), None, p(256), 1 << 30, None, None) == -1   # r > rows
     assert f(None, 64, 64, p(256), 4, p(256), p(256), None, p(256), 1 << 30, None, None) == -1     # null dW
     assert f(p(256), 64, 64, p(256), 4, p(256), p(256), None, p(256), 16, None, None) == -7        # workspace
     assert gq.lib.eora_compensate_workspace_size(5120, 5120, 64) >= 3 * 5120 * 5120 * 4
+    assert gq.lib.eora_compensate_workspace_size(5120, 5120, 256) > gq.lib.eora_compensate_workspace_size(5120, 5120, 64)
 
 
 def test_intrinsic_lora_host_side_validation(gq):

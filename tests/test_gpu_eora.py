@@ -20,7 +20,7 @@ from oracle import eora as oe
 from oracle import gptq as og
 from synthetic import custom_layer
 
-from tests._helpers import host_arrays
+from tests._helpers import check_sigma, host_arrays
 
 pytestmark = pytest.mark.gpu
 
@@ -91,6 +91,52 @@ def test_planted_gap_matches_oracle_factors(gq):
     # with a clear gap the individual factors match after sign normalisation
     assert np.linalg.norm(g["B"] - B_o) / np.linalg.norm(B_o) <= 1e-3
     assert np.linalg.norm(g["A"] - A_o) / np.linalg.norm(A_o) <= 1e-3
+
+
+@pytest.mark.parametrize("r", [128, 256])
+def test_planted_gap_high_rank(gq, r):
+    """Above r = 64 the eigenpairs come in locked chunks of 64.  A planted spectrum with distinct
+    values (1 % apart, so every chunk boundary has a gap) and a wide gap at r: σ, B A and the
+    factors themselves are unique and compared as at low rank."""
+    rows, cols = 400, 384
+    H = _h_from_x(2048, cols, 13, outliers=4).astype(np.float32)
+    L = np.linalg.cholesky(H.astype(np.float64))
+    rng = np.random.default_rng(14)
+    U, _ = np.linalg.qr(rng.standard_normal((rows, cols)))
+    V, _ = np.linalg.qr(rng.standard_normal((cols, cols)))
+    s = np.concatenate([10.0 * 0.99 ** np.arange(r), 0.05 * 0.99 ** np.arange(cols - r)])
+    dW = np.linalg.solve(L.T, ((U * s) @ V.T).T).T.astype(np.float32).astype(np.float64)
+    g = _run(gq, dW, H, r)
+    A_o, B_o, _ = _check_unique_parts(g, dW, H, r)
+    BA_o = B_o @ A_o
+    assert np.linalg.norm(g["B"] @ g["A"] - BA_o) / np.linalg.norm(BA_o) <= 1e-3
+    assert np.linalg.norm(g["B"] - B_o) / np.linalg.norm(B_o) <= 1e-3
+    assert np.linalg.norm(g["A"] - A_o) / np.linalg.norm(A_o) <= 1e-3
+
+
+def test_gptq_error_rank_256(gq):
+    """Rank 256 ("Aumento de la precisión…", *Calibrar un adaptador Eora*) on a layer's real GPTQ
+    error: the compensated loss never below the oracle's optimum and within 1e-3 of it, σ with the
+    cluster-aware comparison (a GPTQ error's spectrum is flat past the outlier directions)."""
+    rows, cols, r = 384, 640, 256
+    spec = custom_layer("e", rows, cols, 4 * cols, bits=2, group=64, x_dist="normal", n_outliers=6,
+                        key=(23, rows, cols))
+    _, w64 = host_arrays(spec.W)
+    _, x64 = host_arrays(spec.X)
+    H0 = og.hessian(x64)
+    ref = og.quantize_layer(w64, H0, 2, 64, 0.01)
+    dW = (w64 - ref["W_hat"].astype(np.float64)).astype(np.float32).astype(np.float64)
+    H32 = H0.astype(np.float32)
+    g = _run(gq, dW, H32, r)
+    H = H32.astype(np.float64)
+    A_o, B_o, sig = oe.eora(dW, H, r)
+    check_sigma(g["sigma"], sig, r)
+    base = oe.compensated_loss(dW, 0 * A_o, 0 * B_o, H)
+    lg = oe.compensated_loss(dW, g["A"], g["B"], H)
+    lo = oe.compensated_loss(dW, A_o, B_o, H)
+    assert lg >= lo * (1 - 1e-9) - 1e-12 * base
+    assert lg <= lo * (1 + 1e-3) + 1e-9 * base, (lg, lo)
+    assert np.all(np.diff(g["sigma"]) <= 0)
 
 
 # (384, 576): M = dW F and G = M^T M run on CTA pairs over three 256-column tiles, the last one ragged,

@@ -15,13 +15,15 @@ Layers that share a calibration set (q_proj / up_proj, the two Qwen2.5-72B
 shapes, the two Qwen3-32B shapes) share the oracle's H: the tests run in that
 order and the last H is kept.
 
-EoRA at full size (the 5120 x 5120 and 25600 x 5120 layers, r = 64): both sides take the error of
+EoRA at full size (the 5120 x 5120 and 25600 x 5120 layers at the workloads'
+rank r = 64, and the 5120 x 5120 layer at r = 256, the rank of the EoRA
+page's own adapter call): both sides take the error of
 round-to-nearest on the layer's own 2-bit g64 grid (the library's
 gptq_quantize_rtn and the oracle's rtn agree bit for bit), so no input of the
 oracle comes from the GPU; the GPU uses its own H, the oracle its float64 H.
 Compared as in the small EoRA tests: the 64 singular values (1e-3 relative
 where the spectrum has a gap at that index, the interlacing bound inside a
-cluster of nearly equal values, see _check_sigma) and the compensated loss
+cluster of nearly equal values, see tests/_helpers.check_sigma) and the compensated loss
 (never below the oracle's optimum, within 1e-3 of it).
 """
 import numpy as np
@@ -31,6 +33,7 @@ from oracle import eora as oe
 from oracle import gptq as og
 from oracle import pack as opk
 from synthetic import LAYERS, bf16_bits_to_f32, generate
+from tests._helpers import check_sigma
 
 pytestmark = pytest.mark.gpu
 
@@ -116,26 +119,9 @@ def test_full_size_layer(gq, name):
     assert abs(lg - lo) <= 5e-3 * lo, (lg, lo)
 
 
-def _check_sigma(sg, sig, r, rtol=1e-3, reach=16):
-    """The GPU's r singular values against the oracle's.  Where sigma_i stands apart from sigma_(i+1)
-    by more than rtol, within rtol of it.  Inside a cluster of nearly equal values (the tail of a
-    large layer's spectrum can hold several within 1e-4 of one another) an individual value is not
-    determined to rtol by a subspace of finite accuracy, only the cluster is: there sigma_i of the
-    GPU lies between sigma_(i+reach) and sigma_i, each widened by rtol.  The compensated loss below
-    is the criterion on the subspace as a whole."""
-    sg = np.asarray(sg, dtype=np.float64)
-    for i in range(r):
-        if sig[i] > sig[i + 1] * (1 + rtol):
-            assert abs(sg[i] - sig[i]) <= rtol * sig[i], (i, sg[i], sig[i])
-        else:
-            lo = sig[min(i + reach, len(sig) - 1)] * (1 - rtol)
-            assert lo <= sg[i] <= sig[i] * (1 + rtol), (i, sg[i], sig[i], lo)
-
-
-@pytest.mark.parametrize("name", ["qwen32b_5120x5120", "qwen32b_25600x5120"])
-def test_full_size_eora_r64(gq, name):
+@pytest.mark.parametrize("name,r", [("qwen32b_5120x5120", 64), ("qwen32b_25600x5120", 64), ("qwen32b_5120x5120", 256)])
+def test_full_size_eora(gq, name, r):
     spec = LAYERS[name]
-    r = spec.eora_rank
     R, C = spec.rows, spec.cols
     xa, H0 = _calibration(spec.X)
     wa = generate(spec.W)
@@ -157,9 +143,9 @@ def test_full_size_eora_r64(gq, name):
     assert np.array_equal(M_hat_gpu.view(np.uint32), ref["W_hat"].view(np.uint32))
     dW0 = w64 - ref["W_hat"].astype(np.float64)
     A_o, B_o, sig = oe.eora(dW0, H0, r)
-    print(f"EoRA r={r}: sigma_1 {sig[0]:.6e} (GPU {g['sigma'][0]:.6e}), sigma_64 {sig[r - 1]:.6e} "
-          f"(GPU {g['sigma'][r - 1]:.6e}), sigma_64/sigma_65 = {sig[r - 1] / sig[r]:.6f}")
-    _check_sigma(g["sigma"], sig, r)
+    print(f"EoRA r={r}: sigma_1 {sig[0]:.6e} (GPU {g['sigma'][0]:.6e}), sigma_r {sig[r - 1]:.6e} "
+          f"(GPU {g['sigma'][r - 1]:.6e}), sigma_r/sigma_r+1 = {sig[r - 1] / sig[r]:.6f}")
+    check_sigma(g["sigma"], sig, r)
     base = oe.compensated_loss(dW0, 0 * A_o, 0 * B_o, H0)
     lg = oe.compensated_loss(dW0, g["A"], g["B"], H0)
     lo = oe.compensated_loss(dW0, A_o, B_o, H0)
