@@ -501,7 +501,8 @@ def phase_rooflines(spec, phase: dict, kt, peaks: dict, peak_kind: str, codes: b
         byt = sweep_pack_bytes(spec, codes, w_hat)
         a = byt / (phase["sweep"] / 1e3) / 1e9
         n_sw = kt.count["sweep"]
-        t_step_ns = kt.ms["sweep"] * 1e6 / (n_sw * spec.block) if n_sw else None
+        # Every column is one step of the block kernels (a launch sweeps one or two blocks).
+        t_step_ns = kt.ms["sweep"] * 1e6 / C if n_sw else None
         out["sweep_pack"] = {"bound": "hbm", "achieved": round(a, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": round(a / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} HBM copy",
                              "bytes_per_call": byt, "phase_ms": round(phase["sweep"], 4),

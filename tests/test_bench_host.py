@@ -109,7 +109,8 @@ class _KT:
 def test_phase_rooflines_arithmetic():
     """Each phase's roofline from its time and algorithmic work: the factor as cols^3/3 flops against
     the 3xTF32 rate (measured bf16 burst x 1.1/2.25 / 3), sweep + pack as bytes against the HBM copy
-    rate with the chain floor cols x (block-kernel time per column step), the GEMM class as its
+    rate with the chain floor cols x (block-kernel time per column step: the kernels' time over the
+    cols columns they sweep, one or two blocks per launch), the GEMM class as its
     declared useful flops over its summed time."""
     from synthetic import LAYERS
 
@@ -126,8 +127,8 @@ def test_phase_rooflines_arithmetic():
     byt = 4096 * 11008 * 2 + 4096 * 11008 * 3 / 8 + (11008 // 128) * 4096 * (4 + 3 / 8) + 11008 * 4
     assert bench.sweep_pack_bytes(spec, False, False) == byt
     assert out["sweep_pack"]["achieved"] == round(byt / 6e-3 / 1e9, 1)
-    assert out["sweep_pack"]["column_step_ns"] == round(2.0e6 / (86 * 128), 2)
-    assert out["sweep_pack"]["chain_floor_ms"] == round(11008 * (2.0e6 / (86 * 128)) / 1e6, 4)
+    assert out["sweep_pack"]["column_step_ns"] == round(2.0e6 / 11008, 2)
+    assert out["sweep_pack"]["chain_floor_ms"] == round(11008 * (2.0e6 / 11008) / 1e6, 4)
     assert out["gemm3"]["achieved"] == round(9.6e11 / 8e-3 / 1e12, 2)
     assert out["gemm3"]["frac"] == round(out["gemm3"]["achieved"] / tf32x3, 4)
     assert out["hessian"]["frac"] == round(3.2e13 / 20e-3 / 1e12 / 1800.0, 4)
