@@ -15,7 +15,7 @@
 //   / lane 0 of the even CTA issues the MMAs (kind::f16, bf16 x bf16 -> f32,
 //   M = 256, N = 256, K = 16).
 // * Epilogue: eight warps per CTA read their TMEM lanes (one output row each,
-//   half of the columns) with tcgen05.ld after every 512 tokens, add the
+//   half of the columns) with tcgen05.ld after every 1024 tokens, add the
 //   partial sums into float32 registers and finally add 2 * sum into H.
 // * Every wait on an mbarrier is bounded (clock64 budget); on expiry the CTA
 //   records an error flag, waits (again bounded) until the TMA loads and MMAs
@@ -38,8 +38,11 @@ using namespace tc;
 // CTA per 64 tokens instead of 48 KB).  Each CTA's TMEM receives its 128 rows
 // of the tile (two 256-column buffers).  The tensor core's own accumulation
 // loses about half an ulp of the running sum per step, so each buffer sums KF
-// k-tiles (512 tokens) and the epilogue warps add it into float32 registers
-// (round-to-nearest) while the MMAs fill the other buffer.
+// k-tiles (1024 tokens) and the epilogue warps add it into float32 registers
+// (round-to-nearest) while the MMAs fill the other buffer.  The error of H grows
+// with the period (1.0e-6 relative at 512 tokens, 2.1e-6 at 1024, measured on
+// 262144 tokens); the longer period halves the flushes and took 5 % off the
+// kernel's time.
 // * The even CTA's loads count on its full barrier; the odd CTA's loads count
 //   directly on the even CTA's peer barrier of the stage (the odd CTA's
 //   producer arrives there with the stage's byte count before it issues them).
@@ -76,7 +79,7 @@ constexpr int B_BYTES = 2 * CH;                   // this CTA's 128 of the 256 B
 constexpr int STAGE = A_BYTES + B_BYTES;          // 64 KB at 128 tokens
 constexpr int SMEM = STAGES * STAGE + 1024;
 constexpr uint32_t TCOLS = 256;                   // TMEM columns per accumulator buffer
-constexpr int KF = 512 / TK;                      // k-tiles per TMEM period (512 tokens)
+constexpr int KF = 1024 / TK;                     // k-tiles per TMEM period (1024 tokens)
 constexpr int P_GROUP = 8;                        // tile-rows per scheduling group
 constexpr int NWARPS = 10, EPI = 8;
 }  // namespace pair
