@@ -807,7 +807,7 @@ def cpu_baseline(spec, n_s: int = 4096, r_s: int = 16, factor_cols: int | None =
 
 
 # The sample of the oracle timing, in the bench line's cpu_baseline and in each step of the reference
-# arm: bounded so that the driver's --steps 20 --warmup 5 reference run ends within a few minutes.
+# arm: bounded so that a reference run of --steps 20 --warmup 5 ends within a few minutes.
 ORACLE_SAMPLE = dict(n_s=4096, r_s=16, factor_cols=4096)
 _SAMPLES = {}
 
