@@ -355,11 +355,23 @@ cudaError_t subspace_ritz(const SubspaceBufs &w, int k, int64_t cols, bool tc, c
         if ((e = cholqr_pass(w, w.ZT2, w.ZT, k, cols, s)) != cudaSuccess) return e;
     }
     if ((e = cholqr_pass(w, w.ZT, w.ZT2, k, cols, s)) != cudaSuccess) return e;
+    if (w.nl > 0) {
+        // With locked vectors the block can hold directions that the iteration drove down to
+        // rounding level (when the complement has fewer large eigenvalues than k): the shifted
+        // pass leaves them short of unit length, and rounding gives them components along the
+        // locked vectors.  Two more passes, each after a projection, make the block orthonormal
+        // and orthogonal to the locked vectors before the Rayleigh-Ritz step.
+        if ((e = project_out(w, w.ZT2, k, cols, s)) != cudaSuccess) return e;
+        if ((e = cholqr_pass(w, w.ZT2, w.ZT, k, cols, s)) != cudaSuccess) return e;
+        if ((e = project_out(w, w.ZT, k, cols, s)) != cudaSuccess) return e;
+        if ((e = cholqr_pass(w, w.ZT, w.ZT2, k, cols, s)) != cudaSuccess) return e;
+    }
     if ((e = cudaMemcpyAsync(w.ZT, w.ZT2, (size_t)k * cols * sizeof(float), cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
         return e;
 
     // Rayleigh-Ritz: T = Z^T G Z (k x k), eigenpairs by Jacobi.
     if ((e = block_times_g(w, w.ZT, w.ZT2, k, cols, tc, true, s)) != cudaSuccess) return e;
+    if ((e = project_out(w, w.ZT2, k, cols, s)) != cudaSuccess) return e;
     if ((e = sgemm_splitk(k, k, cols, w.ZT2, cols, false, w.ZT, cols, true, w.Gm, w.part, SPLITK, s)) != cudaSuccess)
         return e;
     static bool attr_set = false;

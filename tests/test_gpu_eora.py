@@ -207,3 +207,21 @@ def test_ragged_shape_uses_simt_path(gq):
     H = _h_from_x(400, cols, 9, outliers=1).astype(np.float32)
     g = _run(gq, dW, H, r)
     _check_unique_parts(g, dW, H, r)
+
+
+def test_high_rank_ragged_shape_simt_path(gq):
+    """Rank above 64 (two locked chunks) with rows not a multiple of 4: the products, the projection
+    against the first chunk and B = M V_r run on the float32 SIMT path; a planted spectrum with
+    distinct values and a gap at r, compared as at low rank."""
+    rows, cols, r = 402, 256, 96
+    H = _h_from_x(1024, cols, 17, outliers=2).astype(np.float32)
+    L = np.linalg.cholesky(H.astype(np.float64))
+    rng = np.random.default_rng(18)
+    U, _ = np.linalg.qr(rng.standard_normal((rows, cols)))
+    V, _ = np.linalg.qr(rng.standard_normal((cols, cols)))
+    s = np.concatenate([10.0 * 0.98 ** np.arange(r), 0.05 * 0.98 ** np.arange(cols - r)])
+    dW = np.linalg.solve(L.T, ((U * s) @ V.T).T).T.astype(np.float32).astype(np.float64)
+    g = _run(gq, dW, H, r)
+    A_o, B_o, _ = _check_unique_parts(g, dW, H, r)
+    BA_o = B_o @ A_o
+    assert np.linalg.norm(g["B"] @ g["A"] - BA_o) / np.linalg.norm(BA_o) <= 1e-3
