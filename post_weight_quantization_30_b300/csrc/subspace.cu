@@ -294,6 +294,10 @@ cudaError_t cholqr_pass(const SubspaceBufs &w, float *src, float *dst, int k, in
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = cholesky_lower_inplace(w.Gm, k, w.qst, w.Linv, s)) != cudaSuccess) return e;
+    // dst = L^-1 src: one 128-row tile of outputs per 128 columns is fewer CTAs than SMs, so K (= k)
+    // is split as the block products split theirs, the slices summed in a fixed order.
+    const int z = zsplit(cols, k);
+    if (z > 1) return sgemm_splitk(k, cols, k, w.Linv, 128, false, src, cols, false, dst, w.part, z, s);
     return sgemm<float>(k, cols, k, 1.f, w.Linv, 128, false, src, cols, false, 0.f, dst, cols, 0, s);
 }
 
@@ -331,8 +335,9 @@ int subspace_width(int64_t cols, int r) {
 size_t subspace_projection_part_floats(int k, int nl) { return (size_t)SPLITK * k * nl; }
 
 size_t subspace_part_floats(int k, int64_t cols, bool tc) {
+    (void)tc;
     size_t part = (size_t)SPLITK * k * k;
-    if (tc && (size_t)zsplit(cols, k) * k * cols > part) part = (size_t)zsplit(cols, k) * k * cols;
+    if ((size_t)zsplit(cols, k) * k * cols > part) part = (size_t)zsplit(cols, k) * k * cols;
     return part;
 }
 
