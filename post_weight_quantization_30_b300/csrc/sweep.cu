@@ -27,6 +27,10 @@
 // is reduced through shared memory as well.  The epilogue writes ΔW (split) back
 // to D / DL, the optional codes / Ŵ / row errors, the scales, and packs codes
 // and zero points into 32-bit words (coalesced word-rows of 32 output rows).
+// When all CTAs fit one wave, a launch can also sweep two adjacent blocks and
+// apply the first one's deferred update to the second in the kernel (the
+// two-block form below), which takes the first level of the recursive GEMMs
+// off the serial chain.
 #include "common.cuh"
 
 namespace gq {
